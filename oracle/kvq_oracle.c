@@ -1,0 +1,740 @@
+/*
+ * kvq_oracle.c -- the ORACLE for the quantised KV cache.  TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded CPU restatement of what the cache computes, used to
+ * check the CUDA library.  Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg may load it; the library itself never does.  It shares no code,
+ * header, table or constant with the CUDA path: the byte layout below is re-derived
+ * here from the written layout specification, and every arithmetic step follows the
+ * pages it cites.
+ *
+ * Sources (web pages on KV-cache quantisation):
+ *   [QC]   "Quantising the Cache" (course plate XXIV.3), sections "Workshop",
+ *          "Twice the users for nearly nothing" and "Terms".
+ *   [QKV]  "Quantizing the KV cache", sections "The other big memory user" (KV bytes
+ *          equation), "How the KV cache is quantized", "Keys and values are shaped
+ *          differently", "going deeper / Per-channel and per-token grouping" (the Q_b
+ *          equation) and "Why values per token".
+ *   [KIVI] "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache" summary,
+ *          section "How It Works".
+ *
+ * Arithmetic contract (so that quantised codes can be compared bit for bit):
+ *   - quantisation runs in IEEE binary32 with round-to-nearest-even, no contraction
+ *     (built with -ffp-contract=off, no fast-math);
+ *   - attention runs in binary64 on the dequantised binary32 values.
+ *
+ * Parity pins: every function here is pinned by tests/test_oracle_pins.py, except the
+ * two readings listed as "parity unpinned" in the design notes (the 48%/16% toy error
+ * figures, whose data the pages do not give, and the micro-model loss table).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------------------
+ * Configuration, mirroring the library's kvq_config field by field.
+ * ---------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t scheme;     /* 0 = KIVI asymmetric, 1 = INT8 symmetric per token, 2 = FP8 E4M3 */
+    int32_t layers;
+    int32_t batch;
+    int32_t q_heads;
+    int32_t kv_heads;
+    int32_t head_dim;
+    int32_t bits;       /* KIVI: 2, 4 or 8 */
+    int32_t group_k;    /* KIVI: G, tokens per key group (per-channel statistics) */
+    int32_t group_v;    /* KIVI: Gv, channels per value group (per-token statistics) */
+    int32_t residual;   /* KIVI: R, newest tokens kept in full precision */
+    int32_t max_tokens; /* per-sequence capacity T */
+    int32_t in_dtype;   /* 0 = bf16, 1 = fp32 (inputs K, V and q) */
+} kvqo_config;
+
+enum { SCHEME_KIVI = 0, SCHEME_INT8 = 1, SCHEME_FP8 = 2 };
+enum { DT_BF16 = 0, DT_F32 = 1 };
+enum { ST_CAPACITY = 1u, ST_RING_FULL = 2u, ST_NONFINITE = 4u };
+enum { FLAG_NO_AUTOFLUSH = 1u };
+
+/* ------------------------------------------------------------------------------------
+ * [QKV] "The other big memory user": the KV bytes equation,
+ *   KV bytes = 2 x layers x KV heads x head size x tokens x bytes per value.
+ * ---------------------------------------------------------------------------------- */
+double kvqo_kv_bytes(double layers, double kv_heads, double head_size, double tokens,
+                     double bytes_per_value)
+{
+    return 2.0 * layers * kv_heads * head_size * tokens * bytes_per_value;
+}
+
+/* [QC] "Workshop": how many conversations of `tokens` tokens fit beside the weights on
+ * a GPU of `gpu_bytes` used to `use_fraction`, cache scales ignored. */
+int64_t kvqo_concurrency(double gpu_bytes, double use_fraction, double weight_bytes,
+                         double layers, double kv_heads, double head_size, double tokens,
+                         double bytes_per_value)
+{
+    double free_bytes = gpu_bytes * use_fraction - weight_bytes;
+    double per_conv = kvqo_kv_bytes(layers, kv_heads, head_size, tokens, bytes_per_value);
+    return (int64_t)floor(free_bytes / per_conv);
+}
+
+/* ------------------------------------------------------------------------------------
+ * IEEE binary16, from its definition: 1 sign bit, 5 exponent bits (bias 15), 10
+ * fraction bits; subnormals are m * 2^-24.  Rounding modes: 0 nearest-even,
+ * -1 toward -infinity, +1 toward +infinity.
+ * ---------------------------------------------------------------------------------- */
+float kvqo_half_to_float(uint16_t h)
+{
+    int sign = (h >> 15) & 1, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 31) v = m ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)m, -24);
+    else v = ldexp(1024.0 + m, e - 25);
+    return (float)(sign ? -v : v);
+}
+
+static uint16_t half_encode_magnitude(double r) /* r exactly representable, finite */
+{
+    if (r == 0.0) return 0;
+    if (r < ldexp(1.0, -14)) return (uint16_t)(r / ldexp(1.0, -24));
+    int k;
+    frexp(r, &k);                 /* r = f * 2^k, f in [0.5, 1) */
+    int e = k - 1;                /* r in [2^e, 2^(e+1)) */
+    double m = r / ldexp(1.0, e) - 1.0;
+    return (uint16_t)(((e + 15) << 10) | (int)(m * 1024.0));
+}
+
+uint16_t kvqo_half_round(float xf, int mode)
+{
+    double x = xf;
+    uint16_t sign = signbit(xf) ? 0x8000 : 0;
+    if (isnan(x)) return 0x7e00;
+    double ax = fabs(x);
+    /* rounding the magnitude up or down, as the mode and the sign require */
+    int up_mag;   /* 1: ceil, 0: floor, -1: nearest-even */
+    if (mode == 0) up_mag = -1;
+    else if (mode > 0) up_mag = sign ? 0 : 1;
+    else up_mag = sign ? 1 : 0;
+    if (isinf(x)) return sign | 0x7c00;  /* infinity converts exactly in every mode */
+    if (ax == 0.0) return sign;
+    double q; /* quantum of the binade holding ax */
+    if (ax < ldexp(1.0, -14)) q = ldexp(1.0, -24);
+    else {
+        int k;
+        frexp(ax, &k);
+        q = ldexp(1.0, (k - 1) - 10);
+    }
+    double y = ax / q;            /* exact: power-of-two division of a binary32 value */
+    double lo = floor(y), hi = ceil(y), pick;
+    if (up_mag == 1) pick = hi;
+    else if (up_mag == 0) pick = lo;
+    else {
+        double dlo = y - lo, dhi = hi - y;
+        if (dlo < dhi) pick = lo;
+        else if (dhi < dlo) pick = hi;
+        else pick = (fmod(lo, 2.0) == 0.0) ? lo : hi;
+    }
+    double r = pick * q;
+    if (r > 65504.0) {            /* beyond the largest finite binary16 */
+        if (up_mag == 0) return sign | 0x7bff;
+        return sign | 0x7c00;
+    }
+    return sign | half_encode_magnitude(r);
+}
+
+/* bfloat16 is the top half of a binary32 pattern */
+static float bf16_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* ------------------------------------------------------------------------------------
+ * [QKV] "How the KV cache is quantized": FP8 E4M3 (the OCP 8-bit format with 4
+ * exponent bits, bias 7, 3 fraction bits, no infinities, NaN = S.1111.111, largest
+ * finite 448).  Encoding rounds to nearest-even and saturates finite overflow (and
+ * infinities) to +-448; NaN encodes as 0x7f.
+ * ---------------------------------------------------------------------------------- */
+float kvqo_e4m3_to_float(uint8_t c)
+{
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(8.0 + m, e - 10);
+    return (float)(sign ? -v : v);
+}
+
+uint8_t kvqo_e4m3_from_float(float xf)
+{
+    if (isnan(xf)) return 0x7f;
+    uint8_t sign = signbit(xf) ? 0x80 : 0;
+    double ax = fabs((double)xf);
+    if (ax >= 448.0) return sign | 0x7e;  /* saturate (includes infinity) */
+    if (ax == 0.0) return sign;
+    double q;
+    if (ax < ldexp(1.0, -6)) q = ldexp(1.0, -9);
+    else {
+        int k;
+        frexp(ax, &k);
+        q = ldexp(1.0, (k - 1) - 3);
+    }
+    double y = ax / q, lo = floor(y), hi = ceil(y), pick;
+    double dlo = y - lo, dhi = hi - y;
+    if (dlo < dhi) pick = lo;
+    else if (dhi < dlo) pick = hi;
+    else pick = (fmod(lo, 2.0) == 0.0) ? lo : hi;
+    double r = pick * q;
+    if (r > 448.0) r = 448.0;
+    if (r < ldexp(1.0, -6)) return sign | (uint8_t)(r / ldexp(1.0, -9));
+    int k;
+    frexp(r, &k);
+    int e = k - 1;
+    int m = (int)((r / ldexp(1.0, e) - 1.0) * 8.0);
+    return sign | (uint8_t)(((e + 7) << 3) | m);
+}
+
+/* ------------------------------------------------------------------------------------
+ * [QKV] "Per-channel and per-token grouping", the Q_b equation:
+ *   s = (max x - min x) / (2^b - 1),  Q_b(x) = round((x - min x) / s) * s + min x.
+ * Stored parameters are binary16: the offset is min x rounded toward -infinity and the
+ * scale is s rounded toward +infinity (computed from the stored offset), so the stored
+ * grid [z, z + (2^b-1) s] still covers [min x, max x].  `round` is nearest-even.  A
+ * constant group (s = 0) gets all-zero codes.
+ * x[i * stride], i < n; codes written one per byte.
+ * ---------------------------------------------------------------------------------- */
+void kvqo_qb_group(const float* x, int n, int stride, int bits, uint16_t* scale_out,
+                   uint16_t* zero_out, uint8_t* codes)
+{
+    float mn = x[0], mx = x[0];
+    for (int i = 1; i < n; i++) {
+        mn = fminf(mn, x[i * stride]);
+        mx = fmaxf(mx, x[i * stride]);
+    }
+    int levels = (1 << bits) - 1;
+    uint16_t z = kvqo_half_round(mn, -1);
+    float zf = kvqo_half_to_float(z);
+    float range = mx - zf;                    /* one binary32 subtraction */
+    float s32 = range / (float)levels;        /* one binary32 division */
+    uint16_t s = kvqo_half_round(s32, +1);
+    float sf = kvqo_half_to_float(s);
+    for (int i = 0; i < n; i++) {
+        int code = 0;
+        if (sf != 0.0f) {
+            float y = (x[i * stride] - zf) / sf;
+            float r = rintf(y);               /* nearest-even in the default mode */
+            if (r < 0.0f) r = 0.0f;
+            if (r > (float)levels) r = (float)levels;
+            code = (int)r;
+        }
+        codes[i] = (uint8_t)code;
+    }
+    *scale_out = s;
+    *zero_out = z;
+}
+
+/* Dequantisation of one element: code * s + z, a binary32 multiply then a binary32 add. */
+float kvqo_qb_dequant(int code, uint16_t scale, uint16_t zero)
+{
+    float p = (float)code * kvqo_half_to_float(scale);
+    return p + kvqo_half_to_float(zero);
+}
+
+/* [QC] "Workshop" and "Terms / Per-token": symmetric round-to-nearest with one scale
+ * for all of a token's values in a head.  Reading: codes in [-127, 127], scale =
+ * max|x| / 127 in binary32, code = round-half-even(x / scale); an all-zero vector gets
+ * scale 0 and zero codes. */
+void kvqo_int8_token(const float* x, int n, float* scale_out, int8_t* codes)
+{
+    float a = 0.0f;
+    for (int i = 0; i < n; i++) a = fmaxf(a, fabsf(x[i]));
+    float s = a / 127.0f;
+    for (int i = 0; i < n; i++) {
+        int code = 0;
+        if (s != 0.0f) {
+            float r = rintf(x[i] / s);
+            if (r < -127.0f) r = -127.0f;
+            if (r > 127.0f) r = 127.0f;
+            code = (int)r;
+        }
+        codes[i] = (int8_t)code;
+    }
+    *scale_out = s;
+}
+
+/* ------------------------------------------------------------------------------------
+ * The cache image.  Restated here from the written layout specification (regions
+ * aligned to 256 bytes, little-endian):
+ *   header 256 B: u32 status at byte 0.
+ *   state: for (layer l, sequence b): int32 n (tokens cached), int32 qn (tokens held in
+ *          packed groups; n for INT8/FP8), at byte 8 * (l * batch + b).
+ *   KIVI:  group records, one per (l, b, kv head h, group slot g), NG = (T - R) / G slots:
+ *            K codes  G*D*b/8 bytes, token-major: (token t, channel c) at bit (t*D + c)*b
+ *            V codes  D*G*b/8 bytes, channel-major: (channel c, token t) at bit (c*G + t)*b
+ *            K params 4*D bytes: fp16 scale[D], then fp16 zero[D]
+ *            V params 4*G*NGv bytes: fp16 scale[G][NGv], then fp16 zero[G][NGv]
+ *          then the bf16 ring: (l, b, h, slot s) holds K row[D] then V row[D], C = R + G
+ *          slots; token t (qn <= t < n) sits in slot t mod C.
+ *   INT8:  per (l, b, h) block over T16 = T rounded up to 16:
+ *            K codes int8 [T16][D], V codes int8 [T16][D], K scale f32 [T16], V scale f32 [T16]
+ *   FP8:   scale table f32 [layers][kv heads][2] (K, V), then per (l, b, h) block:
+ *            K codes e4m3 [T16][D], V codes e4m3 [T16][D]
+ * Bits are numbered LSB-first within a byte: bit i is bit (i mod 8) of byte i / 8.
+ * ---------------------------------------------------------------------------------- */
+typedef struct {
+    int64_t header, state, scales, data, ring, total;  /* byte offsets of the regions */
+    int64_t unit;           /* bytes of one (l, b, h) block in the data region */
+    int64_t rec, kc, vc, kp, vp, ng, cap, ngv, t16;
+} layout_t;
+
+static int64_t up256(int64_t x) { return (x + 255) / 256 * 256; }
+
+static layout_t make_layout(const kvqo_config* c)
+{
+    layout_t L;
+    memset(&L, 0, sizeof L);
+    int64_t units = (int64_t)c->layers * c->batch * c->kv_heads;
+    int64_t D = c->head_dim;
+    L.header = 0;
+    L.state = 256;
+    int64_t pos = L.state + up256((int64_t)c->layers * c->batch * 8);
+    L.t16 = ((int64_t)c->max_tokens + 15) / 16 * 16;
+    if (c->scheme == SCHEME_KIVI) {
+        int64_t G = c->group_k, b = c->bits;
+        L.ngv = D / c->group_v;
+        L.cap = c->residual + G;
+        L.ng = c->max_tokens > c->residual ? (c->max_tokens - c->residual) / G : 0;
+        L.kc = G * D * b / 8;
+        L.vc = D * G * b / 8;
+        L.kp = 4 * D;
+        L.vp = 4 * G * L.ngv;
+        L.rec = L.kc + L.vc + L.kp + L.vp;
+        L.unit = L.ng * L.rec;
+        L.data = pos;
+        pos += up256(units * L.unit);
+        L.ring = pos;
+        pos += up256(units * L.cap * 4 * D);
+    } else if (c->scheme == SCHEME_INT8) {
+        L.unit = L.t16 * (2 * D + 8);
+        L.data = pos;
+        pos += up256(units * L.unit);
+    } else {
+        L.scales = pos;
+        pos += up256((int64_t)c->layers * c->kv_heads * 8);
+        L.unit = L.t16 * 2 * D;
+        L.data = pos;
+        pos += up256(units * L.unit);
+    }
+    L.total = pos;
+    return L;
+}
+
+int64_t kvqo_image_bytes(const kvqo_config* c) { return make_layout(c).total; }
+
+/* region offsets, for tests that look inside the image */
+void kvqo_image_regions(const kvqo_config* c, int64_t* out /* [6] */)
+{
+    layout_t L = make_layout(c);
+    out[0] = L.state;
+    out[1] = L.scales;
+    out[2] = L.data;
+    out[3] = L.ring;
+    out[4] = L.total;
+    out[5] = L.unit;
+}
+
+static int32_t* state_of(const kvqo_config* c, uint8_t* img, int l, int b)
+{
+    return (int32_t*)(img + 256 + 8 * ((int64_t)l * c->batch + b));
+}
+
+static uint8_t* unit_base(const kvqo_config* c, const layout_t* L, uint8_t* img, int l, int b,
+                          int h)
+{
+    int64_t u = ((int64_t)l * c->batch + b) * c->kv_heads + h;
+    return img + L->data + u * L->unit;
+}
+
+static void put_bits(uint8_t* base, int64_t bit, int bits, int code)
+{
+    for (int i = 0; i < bits; i++) {
+        int64_t at = bit + i;
+        uint8_t mask = (uint8_t)(1u << (at % 8));
+        if ((code >> i) & 1) base[at / 8] |= mask;
+        else base[at / 8] &= (uint8_t)~mask;
+    }
+}
+
+static int get_bits(const uint8_t* base, int64_t bit, int bits)
+{
+    int v = 0;
+    for (int i = 0; i < bits; i++) {
+        int64_t at = bit + i;
+        v |= ((base[at / 8] >> (at % 8)) & 1) << i;
+    }
+    return v;
+}
+
+static void put_u16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)v; p[1] = (uint8_t)(v >> 8); }
+static uint16_t get_u16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* one input row (K or V of sequence b, new token j, kv head h) as binary32 values */
+static void input_row(const kvqo_config* c, const void* src, int n_new, int bi, int j, int h,
+                      float* out)
+{
+    int D = c->head_dim, H = c->kv_heads;
+    int64_t off = (((int64_t)bi * n_new + j) * H + h) * D;
+    if (c->in_dtype == DT_BF16) {
+        const uint16_t* p = (const uint16_t*)src + off;
+        for (int i = 0; i < D; i++) out[i] = bf16_to_float(p[i]);
+    } else {
+        const float* p = (const float*)src + off;
+        for (int i = 0; i < D; i++) out[i] = p[i];
+    }
+}
+
+static uint16_t float_to_bf16_exact(float f)  /* inputs are bf16 already: keep the top half */
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16);
+}
+
+/* The key group starting at token t0 (G tokens) and the matching value rows, taken from
+ * the ring for tokens before n and from the new input for the rest. */
+static void kivi_quantise_group(const kvqo_config* c, const layout_t* L, uint8_t* img, int l,
+                                int b, int h, int64_t t0, int64_t n, const void* k_new,
+                                const void* v_new, int n_new, int bi)
+{
+    int D = c->head_dim, G = c->group_k, Gv = c->group_v, bits = c->bits;
+    int64_t ngv = L->ngv;
+    float* K = (float*)malloc(sizeof(float) * G * D);
+    float* V = (float*)malloc(sizeof(float) * G * D);
+    uint8_t* codes = (uint8_t*)malloc((size_t)(G > D ? G : D));
+    int64_t u = ((int64_t)l * c->batch + b) * c->kv_heads + h;
+    for (int i = 0; i < G; i++) {
+        int64_t t = t0 + i;
+        if (t < n) {
+            const uint8_t* slot = img + L->ring + (u * L->cap + t % L->cap) * 4 * D;
+            for (int ch = 0; ch < D; ch++) {
+                K[i * D + ch] = bf16_to_float(get_u16(slot + 2 * ch));
+                V[i * D + ch] = bf16_to_float(get_u16(slot + 2 * D + 2 * ch));
+            }
+        } else {
+            input_row(c, k_new, n_new, bi, (int)(t - n), h, K + i * D);
+            input_row(c, v_new, n_new, bi, (int)(t - n), h, V + i * D);
+        }
+    }
+    int64_t g = t0 / G;
+    uint8_t* rec = unit_base(c, L, img, l, b, h) + g * L->rec;
+    uint8_t* kcodes = rec;
+    uint8_t* vcodes = rec + L->kc;
+    uint8_t* kpar = rec + L->kc + L->vc;
+    uint8_t* vpar = kpar + L->kp;
+    /* keys: per channel over the G tokens ([QKV] per-channel grouping, [KIVI]) */
+    for (int ch = 0; ch < D; ch++) {
+        uint16_t s, z;
+        kvqo_qb_group(K + ch, G, D, bits, &s, &z, codes);
+        put_u16(kpar + 2 * ch, s);
+        put_u16(kpar + 2 * D + 2 * ch, z);
+        for (int i = 0; i < G; i++) put_bits(kcodes, ((int64_t)i * D + ch) * bits, bits, codes[i]);
+    }
+    /* values: per token over groups of Gv channels */
+    for (int i = 0; i < G; i++) {
+        for (int j = 0; j < ngv; j++) {
+            uint16_t s, z;
+            kvqo_qb_group(V + (int64_t)i * D + (int64_t)j * Gv, Gv, 1, bits, &s, &z, codes);
+            put_u16(vpar + 2 * (i * ngv + j), s);
+            put_u16(vpar + 2 * (G * ngv) + 2 * (i * ngv + j), z);
+            for (int cc = 0; cc < Gv; cc++) {
+                int ch = j * Gv + cc;
+                put_bits(vcodes, ((int64_t)ch * G + i) * bits, bits, codes[cc]);
+            }
+        }
+    }
+    free(K);
+    free(V);
+    free(codes);
+}
+
+static int any_nonfinite(const float* x, int n)
+{
+    for (int i = 0; i < n; i++)
+        if (!isfinite(x[i])) return 1;
+    return 0;
+}
+
+void kvqo_image_init(const kvqo_config* c, uint8_t* img)
+{
+    layout_t L = make_layout(c);
+    memset(img, 0, (size_t)L.total);
+}
+
+/* Append n_valid[i] (or n_new) new tokens to sequences seq_begin + i.  Inputs are laid
+ * out [seq_count][n_new][kv_heads][head_dim].  Returns the status bits it raised.
+ * KIVI ([QKV] grouping and residual window, [KIVI] residual length): tokens go to the
+ * full-precision window; whenever the window would reach R + G tokens its oldest G are
+ * quantised as one group, so the newest R tokens are never quantised.  With the
+ * no-autoflush flag, groups are left in the window for kvqo_flush. */
+uint32_t kvqo_append(const kvqo_config* c, uint8_t* img, int l, int seq_begin, int seq_count,
+                     const void* k_new, const void* v_new, int n_new, const int32_t* n_valid,
+                     const float* fp8_scales, uint32_t flags)
+{
+    layout_t L = make_layout(c);
+    int D = c->head_dim, H = c->kv_heads;
+    uint32_t st = 0;
+    float* row = (float*)malloc(sizeof(float) * D);
+    if (c->scheme == SCHEME_FP8 && fp8_scales) {
+        float* tab = (float*)(img + L.scales) + (int64_t)l * H * 2;
+        for (int i = 0; i < 2 * H; i++) tab[i] = fp8_scales[i];
+    }
+    for (int bi = 0; bi < seq_count; bi++) {
+        int b = seq_begin + bi;
+        int m = n_valid ? n_valid[bi] : n_new;
+        int32_t* s = state_of(c, img, l, b);
+        int64_t n = s[0], qn = s[1];
+        if (n + m > c->max_tokens) { st |= ST_CAPACITY; continue; }
+        /* non-finite inputs are flagged; the values are still stored */
+        for (int h = 0; h < H; h++)
+            for (int j = 0; j < m; j++) {
+                input_row(c, k_new, n_new, bi, j, h, row);
+                if (any_nonfinite(row, D)) st |= ST_NONFINITE;
+                input_row(c, v_new, n_new, bi, j, h, row);
+                if (any_nonfinite(row, D)) st |= ST_NONFINITE;
+            }
+        if (c->scheme == SCHEME_KIVI) {
+            int64_t G = c->group_k, R = c->residual, cap = L.cap;
+            int64_t qn2 = qn;
+            if (!(flags & FLAG_NO_AUTOFLUSH)) {
+                int64_t over = n + m - qn - R;
+                if (over >= G) qn2 = qn + G * (over / G);
+            } else if (n + m - qn > cap) {
+                st |= ST_RING_FULL;
+                continue;
+            }
+            for (int h = 0; h < H; h++) {
+                for (int64_t t0 = qn; t0 < qn2; t0 += G)
+                    kivi_quantise_group(c, &L, img, l, b, h, t0, n, k_new, v_new, n_new, bi);
+                int64_t u = ((int64_t)l * c->batch + b) * H + h;
+                for (int64_t t = (n > qn2 ? n : qn2); t < n + m; t++) {
+                    uint8_t* slot = img + L.ring + (u * cap + t % cap) * 4 * D;
+                    input_row(c, k_new, n_new, bi, (int)(t - n), h, row);
+                    for (int ch = 0; ch < D; ch++) put_u16(slot + 2 * ch, float_to_bf16_exact(row[ch]));
+                    input_row(c, v_new, n_new, bi, (int)(t - n), h, row);
+                    for (int ch = 0; ch < D; ch++)
+                        put_u16(slot + 2 * D + 2 * ch, float_to_bf16_exact(row[ch]));
+                }
+            }
+            s[0] = (int32_t)(n + m);
+            s[1] = (int32_t)qn2;
+        } else if (c->scheme == SCHEME_INT8) {
+            int8_t* codes = (int8_t*)malloc((size_t)D);
+            for (int h = 0; h < H; h++) {
+                uint8_t* base = unit_base(c, &L, img, l, b, h);
+                for (int j = 0; j < m; j++) {
+                    int64_t t = n + j;
+                    for (int kv = 0; kv < 2; kv++) {
+                        float sc;
+                        input_row(c, kv ? v_new : k_new, n_new, bi, j, h, row);
+                        kvqo_int8_token(row, D, &sc, codes);
+                        memcpy(base + kv * L.t16 * D + t * D, codes, (size_t)D);
+                        memcpy(base + 2 * L.t16 * D + kv * L.t16 * 4 + t * 4, &sc, 4);
+                    }
+                }
+            }
+            free(codes);
+            s[0] = (int32_t)(n + m);
+            s[1] = (int32_t)(n + m);
+        } else {
+            const float* tab = (const float*)(img + L.scales) + (int64_t)l * H * 2;
+            for (int h = 0; h < H; h++) {
+                uint8_t* base = unit_base(c, &L, img, l, b, h);
+                for (int j = 0; j < m; j++) {
+                    int64_t t = n + j;
+                    for (int kv = 0; kv < 2; kv++) {
+                        float sc = tab[2 * h + kv];
+                        input_row(c, kv ? v_new : k_new, n_new, bi, j, h, row);
+                        for (int ch = 0; ch < D; ch++)
+                            base[kv * L.t16 * D + t * D + ch] = kvqo_e4m3_from_float(row[ch] / sc);
+                    }
+                }
+            }
+            s[0] = (int32_t)(n + m);
+            s[1] = (int32_t)(n + m);
+        }
+    }
+    free(row);
+    uint32_t* status = (uint32_t*)img;
+    *status |= st;
+    return st;
+}
+
+/* Quantise every full group still waiting in the window ([QKV] "quantizes them as a
+ * group once the window fills"): while the window holds at least R + G tokens, its
+ * oldest G become one packed group. */
+void kvqo_flush(const kvqo_config* c, uint8_t* img, int l)
+{
+    if (c->scheme != SCHEME_KIVI) return;
+    layout_t L = make_layout(c);
+    for (int b = 0; b < c->batch; b++) {
+        int32_t* s = state_of(c, img, l, b);
+        int64_t n = s[0], qn = s[1];
+        while (n - qn >= (int64_t)c->residual + c->group_k) {
+            for (int h = 0; h < c->kv_heads; h++)
+                kivi_quantise_group(c, &L, img, l, b, h, qn, n, NULL, NULL, 0, 0);
+            qn += c->group_k;
+        }
+        s[1] = (int32_t)qn;
+    }
+}
+
+/* The dequantised key and value of token t of (layer l, sequence b, kv head h), i.e. the
+ * numbers attention sees ([QKV] Q_b equation for KIVI; code * scale otherwise). */
+void kvqo_dequant_token(const kvqo_config* c, const uint8_t* img, int l, int b, int h, int64_t t,
+                        float* kout, float* vout)
+{
+    layout_t L = make_layout(c);
+    int D = c->head_dim;
+    const int32_t* s = state_of(c, (uint8_t*)img, l, b);
+    int64_t qn = s[1];
+    const uint8_t* base = unit_base(c, &L, (uint8_t*)img, l, b, h);
+    if (c->scheme == SCHEME_KIVI) {
+        int G = c->group_k, Gv = c->group_v, bits = c->bits;
+        if (t < qn) {
+            const uint8_t* rec = base + (t / G) * L.rec;
+            const uint8_t* kpar = rec + L.kc + L.vc;
+            const uint8_t* vpar = kpar + L.kp;
+            int i = (int)(t % G);
+            for (int ch = 0; ch < D; ch++) {
+                int kc = get_bits(rec, ((int64_t)i * D + ch) * bits, bits);
+                kout[ch] = kvqo_qb_dequant(kc, get_u16(kpar + 2 * ch), get_u16(kpar + 2 * D + 2 * ch));
+                int vc = get_bits(rec + L.kc, ((int64_t)ch * G + i) * bits, bits);
+                int j = ch / Gv;
+                vout[ch] = kvqo_qb_dequant(vc, get_u16(vpar + 2 * (i * L.ngv + j)),
+                                           get_u16(vpar + 2 * (G * L.ngv) + 2 * (i * L.ngv + j)));
+            }
+        } else {
+            int64_t u = ((int64_t)l * c->batch + b) * c->kv_heads + h;
+            const uint8_t* slot = img + L.ring + (u * L.cap + t % L.cap) * 4 * D;
+            for (int ch = 0; ch < D; ch++) {
+                kout[ch] = bf16_to_float(get_u16(slot + 2 * ch));
+                vout[ch] = bf16_to_float(get_u16(slot + 2 * D + 2 * ch));
+            }
+        }
+    } else if (c->scheme == SCHEME_INT8) {
+        const int8_t* kc = (const int8_t*)base + t * D;
+        const int8_t* vc = (const int8_t*)base + L.t16 * D + t * D;
+        float ks, vs;
+        memcpy(&ks, base + 2 * L.t16 * D + t * 4, 4);
+        memcpy(&vs, base + 2 * L.t16 * D + L.t16 * 4 + t * 4, 4);
+        for (int ch = 0; ch < D; ch++) {
+            kout[ch] = (float)kc[ch] * ks;
+            vout[ch] = (float)vc[ch] * vs;
+        }
+    } else {
+        const float* tab = (const float*)(img + L.scales) + (int64_t)l * c->kv_heads * 2;
+        for (int ch = 0; ch < D; ch++) {
+            kout[ch] = kvqo_e4m3_to_float(base[t * D + ch]) * tab[2 * h];
+            vout[ch] = kvqo_e4m3_to_float(base[L.t16 * D + t * D + ch]) * tab[2 * h + 1];
+        }
+    }
+}
+
+/* Single-query decode attention over the cache ([QKV] "Why values per token"):
+ *   score_t = softmax_scale * q . Khat_t,  p = softmax(score),  o = sum_t p_t Vhat_t,
+ * in binary64 over every cached token of the sequence.  Query head hq reads kv head
+ * hq / (q_heads / kv_heads) (grouped-query sharing, [QKV] "Two levers").  A sequence
+ * with no tokens yields a zero output.  q is [batch][q_heads][head_dim] (binary32 values
+ * of the caller's query); out is [batch][q_heads][head_dim]. */
+void kvqo_decode(const kvqo_config* c, const uint8_t* img, int l, int seq_begin, int seq_count,
+                 const float* q, double softmax_scale, double* out)
+{
+    int D = c->head_dim, Hq = c->q_heads, gqa = c->q_heads / c->kv_heads;
+    float* kr = (float*)malloc(sizeof(float) * D);
+    float* vr = (float*)malloc(sizeof(float) * D);
+    for (int b = seq_begin; b < seq_begin + seq_count; b++) {
+        const int32_t* s = state_of(c, (uint8_t*)img, l, b);
+        int64_t n = s[0];
+        for (int h = 0; h < c->kv_heads; h++) {
+            double* sc = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * gqa : 1));
+            for (int64_t t = 0; t < n; t++) {
+                kvqo_dequant_token(c, img, l, b, h, t, kr, vr);
+                for (int g = 0; g < gqa; g++) {
+                    const float* qq = q + ((int64_t)b * Hq + h * gqa + g) * D;
+                    double acc = 0.0;
+                    for (int ch = 0; ch < D; ch++) acc += (double)qq[ch] * (double)kr[ch];
+                    sc[t * gqa + g] = softmax_scale * acc;
+                }
+            }
+            for (int g = 0; g < gqa; g++) {
+                double* o = out + ((int64_t)b * Hq + h * gqa + g) * D;
+                for (int ch = 0; ch < D; ch++) o[ch] = 0.0;
+                if (n == 0) continue;
+                double mx = -INFINITY;
+                for (int64_t t = 0; t < n; t++) mx = fmax(mx, sc[t * gqa + g]);
+                double den = 0.0;
+                for (int64_t t = 0; t < n; t++) den += exp(sc[t * gqa + g] - mx);
+                for (int64_t t = 0; t < n; t++) {
+                    kvqo_dequant_token(c, img, l, b, h, t, kr, vr);
+                    double p = exp(sc[t * gqa + g] - mx) / den;
+                    for (int ch = 0; ch < D; ch++) o[ch] += p * (double)vr[ch];
+                }
+            }
+            free(sc);
+        }
+    }
+    free(kr);
+    free(vr);
+}
+
+/* Merge of partial softmax results over disjoint token chunks by log-sum-exp: chunk i
+ * holds m_i = max score, l_i = sum exp(score - m_i), o_i = sum exp(score - m_i) v.
+ * Result o = sum_i o_i e^(m_i - M) / sum_i l_i e^(m_i - M), M = max m_i.  Used to pin
+ * that splitting the context gives the unsplit answer. */
+void kvqo_lse_merge(int chunks, int D, const double* m, const double* lsum, const double* o,
+                    double* out)
+{
+    double M = -INFINITY;
+    for (int i = 0; i < chunks; i++) M = fmax(M, m[i]);
+    double den = 0.0;
+    for (int ch = 0; ch < D; ch++) out[ch] = 0.0;
+    for (int i = 0; i < chunks; i++) {
+        if (lsum[i] == 0.0) continue;
+        double w = exp(m[i] - M);
+        den += lsum[i] * w;
+        for (int ch = 0; ch < D; ch++) out[ch] += o[(int64_t)i * D + ch] * w;
+    }
+    if (den > 0.0)
+        for (int ch = 0; ch < D; ch++) out[ch] /= den;
+}
+
+/* Partial softmax over tokens [t0, t1) for one query row, for the merge pin above. */
+void kvqo_partial(const kvqo_config* c, const uint8_t* img, int l, int b, int hq, int64_t t0,
+                  int64_t t1, const float* qrow, double softmax_scale, double* m_out,
+                  double* l_out, double* o_out)
+{
+    int D = c->head_dim, gqa = c->q_heads / c->kv_heads, h = hq / gqa;
+    float* kr = (float*)malloc(sizeof(float) * D);
+    float* vr = (float*)malloc(sizeof(float) * D);
+    double M = -INFINITY;
+    for (int64_t t = t0; t < t1; t++) {
+        kvqo_dequant_token(c, img, l, b, h, t, kr, vr);
+        double acc = 0.0;
+        for (int ch = 0; ch < D; ch++) acc += (double)qrow[ch] * (double)kr[ch];
+        M = fmax(M, softmax_scale * acc);
+    }
+    double lsum = 0.0;
+    for (int ch = 0; ch < D; ch++) o_out[ch] = 0.0;
+    for (int64_t t = t0; t < t1; t++) {
+        kvqo_dequant_token(c, img, l, b, h, t, kr, vr);
+        double acc = 0.0;
+        for (int ch = 0; ch < D; ch++) acc += (double)qrow[ch] * (double)kr[ch];
+        double w = exp(softmax_scale * acc - M);
+        lsum += w;
+        for (int ch = 0; ch < D; ch++) o_out[ch] += w * (double)vr[ch];
+    }
+    *m_out = M;
+    *l_out = lsum;
+    free(kr);
+    free(vr);
+}
