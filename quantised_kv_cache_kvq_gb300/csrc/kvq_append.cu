@@ -1,0 +1,524 @@
+// kvq_append.cu -- quantise-and-pack kernels: appending tokens to the cache and flushing
+// full groups out of the KIVI window.
+//
+// Arithmetic (bit-exact contract): binary32 min/max, one IEEE subtraction and one IEEE
+// division per step with round-to-nearest (the __f*_rn intrinsics), round-half-even to
+// integer, binary16 parameters rounded with __float2half_rd / _ru.  This file is built
+// with --fmad=false so no multiply-add is ever contracted.
+//
+// Quantisers:
+//  * KIVI Q_b ("Quantizing the KV cache", "Per-channel and per-token grouping"):
+//    s = (max - min) / (2^b - 1), code = round((x - min) / s); keys per channel over a
+//    group of G tokens, values per token over Gv channels ("Keys and values are shaped
+//    differently"; "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache",
+//    "How It Works").  The window keeps the newest tokens in bf16 and quantises the
+//    oldest G as a group whenever it would reach R + G tokens.
+//  * INT8 per-token symmetric ("Quantising the Cache", "Workshop"): scale = max|x| / 127.
+//  * FP8 E4M3 with a per-(layer, KV head) scale ("Quantizing the KV cache", "How the KV
+//    cache is quantized").
+#include <cuda_fp8.h>
+
+#include "kvq_internal.cuh"
+#include "kvq_launch.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kThreads = 128;
+
+__device__ __forceinline__ float load_input(const void* p, int64_t idx, int dtype) {
+    if (dtype == KVQ_DTYPE_BF16)
+        return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(p)[idx]);
+    return reinterpret_cast<const float*>(p)[idx];
+}
+
+// Element offset of channel 0 of input row (sequence bi, new-token j, kv head h).
+__device__ __forceinline__ int64_t input_row(const Layout& lo, int n_new, int bi, int64_t j, int h) {
+    return (((int64_t)bi * n_new + j) * lo.H + h) * lo.D;
+}
+
+// Tokens a sequence takes in this append, or -1 when it is skipped (capacity or a full
+// window); sets the matching status bit in *st.
+__device__ __forceinline__ int tokens_taken(const Layout& lo, int n, int qn, int m, uint32_t flags,
+                                            uint32_t* st) {
+    if ((int64_t)n + m > lo.T) {
+        *st |= KVQ_STATUS_CAPACITY;
+        return -1;
+    }
+    if (lo.scheme == KVQ_SCHEME_KIVI && (flags & KVQ_NO_AUTOFLUSH) && n + m - qn > lo.C) {
+        *st |= KVQ_STATUS_RING_FULL;
+        return -1;
+    }
+    return m;
+}
+
+// qn after taking m tokens (the window is flushed while it would hold >= R + G tokens).
+__device__ __forceinline__ int qn_after(const Layout& lo, int n, int qn, int m, uint32_t flags) {
+    if (lo.scheme != KVQ_SCHEME_KIVI) return n + m;
+    if (flags & KVQ_NO_AUTOFLUSH) return qn;
+    int over = n + m - qn - lo.R;
+    return over >= lo.G ? qn + lo.G * (over / lo.G) : qn;
+}
+
+// Q_b parameters of one group: offset = min rounded down to binary16, scale = (max -
+// offset) / levels rounded up to binary16.
+struct QbParams {
+    __half s, z;
+    float sf, zf;
+};
+__device__ __forceinline__ QbParams qb_params(float mn, float mx, float levels) {
+    QbParams p;
+    p.z = __float2half_rd(mn);
+    p.zf = __half2float(p.z);
+    float s32 = __fdiv_rn(__fsub_rn(mx, p.zf), levels);
+    p.s = __float2half_ru(s32);
+    p.sf = __half2float(p.s);
+    return p;
+}
+__device__ __forceinline__ uint32_t qb_code(float x, const QbParams& p, int levels) {
+    if (p.sf == 0.0f) return 0u;
+    int c = __float2int_rn(__fdiv_rn(__fsub_rn(x, p.zf), p.sf));
+    c = c < 0 ? 0 : (c > levels ? levels : c);
+    return static_cast<uint32_t>(c);
+}
+
+__device__ __forceinline__ bool nonfinite(float x) { return !isfinite(x); }
+
+// Source of window/input token t of unit (l, b, h) for the group quantiser.
+struct TokenSource {
+    const uint8_t* ring_unit;  // first slot of the unit's window
+    const void* k_new;
+    const void* v_new;
+    int64_t n;                 // tokens before this append
+    int n_new, bi;
+};
+// Quantise the KIVI group of G tokens starting at absolute token t0 of unit (l, b, h)
+// into its record.  Token t < s.n comes from window slot t % C, later tokens from the
+// new input rows.  Cooperative over the whole block; `codes` is G*D bytes of shared
+// memory.  Returns the non-finite flag seen by this thread.
+__device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int b, int h,
+                                   int64_t t0, const TokenSource& s, uint8_t* codes) {
+    const int D = lo.D, G = lo.G, Gv = lo.Gv, bits = lo.bits;
+    const int levels = (1 << bits) - 1;
+    const float flevels = static_cast<float>(levels);
+    const int64_t u = unit_index(lo, l, b, h);
+    uint8_t* rec = cache + lo.data_off + u * lo.unit + (t0 / G) * (int64_t)lo.rec;
+    __half* kpar = reinterpret_cast<__half*>(rec + lo.kc + lo.vc);
+    __half* vpar = reinterpret_cast<__half*>(rec + lo.kc + lo.vc + lo.kp);
+    uint32_t bad = 0;
+    auto kval = [&](int i, int c) -> float {
+        int64_t t = t0 + i;
+        if (t < s.n)
+            return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(
+                s.ring_unit + (t % lo.C) * (int64_t)(4 * D))[c]);
+        return load_input(s.k_new, input_row(lo, s.n_new, s.bi, t - s.n, h) + c, lo.dtype);
+    };
+    auto vval = [&](int i, int c) -> float {
+        int64_t t = t0 + i;
+        if (t < s.n)
+            return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(
+                s.ring_unit + (t % lo.C) * (int64_t)(4 * D) + 2 * D)[c]);
+        return load_input(s.v_new, input_row(lo, s.n_new, s.bi, t - s.n, h) + c, lo.dtype);
+    };
+
+    // keys: one thread per channel, statistics over the G tokens of the group
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        float mn = kval(0, c), mx = mn;
+        bad |= nonfinite(mn);
+        for (int i = 1; i < G; ++i) {
+            float x = kval(i, c);
+            bad |= nonfinite(x);
+            mn = fminf(mn, x);
+            mx = fmaxf(mx, x);
+        }
+        QbParams p = qb_params(mn, mx, flevels);
+        kpar[c] = p.s;
+        kpar[D + c] = p.z;
+        for (int i = 0; i < G; ++i) codes[i * D + c] = static_cast<uint8_t>(qb_code(kval(i, c), p, levels));
+    }
+    __syncthreads();
+    // pack token-major: code index i*D + c at bit (i*D + c)*bits, 16-byte stores
+    {
+        const int per16 = 128 / bits;  // codes per 16-byte chunk
+        const int chunks = G * D / per16;
+        for (int k = threadIdx.x; k < chunks; k += blockDim.x) {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            const uint8_t* src = codes + k * per16;
+            for (int e = 0; e < per16; ++e) w[(e * bits) >> 5] |= static_cast<uint32_t>(src[e]) << ((e * bits) & 31);
+            reinterpret_cast<uint4*>(rec)[k] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    __syncthreads();
+    // values: one warp per token, each lane holds D/32 consecutive channels; a channel
+    // group of Gv spans Gv / (D/32) lanes and its min/max is a shuffle reduction
+    {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int cpl = D / 32;               // channels per lane
+        const int lpg = Gv / cpl;             // lanes per value group
+        for (int i = warp; i < G; i += blockDim.x / 32) {
+            float x[8];
+            float mn = INFINITY, mx = -INFINITY;
+            for (int e = 0; e < cpl; ++e) {
+                x[e] = vval(i, lane * cpl + e);
+                bad |= nonfinite(x[e]);
+                mn = fminf(mn, x[e]);
+                mx = fmaxf(mx, x[e]);
+            }
+            for (int off = 1; off < lpg; off <<= 1) {
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            }
+            QbParams p = qb_params(mn, mx, flevels);
+            const int gv = (lane * cpl) / Gv;
+            if ((lane % lpg) == 0) {
+                vpar[i * lo.NGv + gv] = p.s;
+                vpar[G * lo.NGv + i * lo.NGv + gv] = p.z;
+            }
+            // channel-major staging: code of (channel c, token i) at c*G + i
+            for (int e = 0; e < cpl; ++e)
+                codes[(lane * cpl + e) * G + i] = static_cast<uint8_t>(qb_code(x[e], p, levels));
+        }
+    }
+    __syncthreads();
+    {
+        uint8_t* vrec = rec + lo.kc;
+        const int per16 = 128 / bits;
+        const int chunks = G * D / per16;
+        for (int k = threadIdx.x; k < chunks; k += blockDim.x) {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            const uint8_t* src = codes + k * per16;
+            for (int e = 0; e < per16; ++e) w[(e * bits) >> 5] |= static_cast<uint32_t>(src[e]) << ((e * bits) & 31);
+            reinterpret_cast<uint4*>(vrec)[k] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    __syncthreads();
+    return bad;
+}
+
+// Copy input row j (new token t = n + j) of (bi, h) into window slot t % C; one warp.
+__device__ __forceinline__ uint32_t ring_write_row(const Layout& lo, uint8_t* cache, int l, int b,
+                                                   int h, int64_t t, int64_t n, const void* k_new,
+                                                   const void* v_new, int n_new, int bi, int lane) {
+    const int D = lo.D;
+    uint16_t* slot = reinterpret_cast<uint16_t*>(cache + lo.ring_off +
+                                                 (unit_index(lo, l, b, h) * lo.C + t % lo.C) *
+                                                     (int64_t)(4 * D));
+    const int64_t src = input_row(lo, n_new, bi, t - n, h);
+    const uint16_t* ks = reinterpret_cast<const uint16_t*>(k_new) + src;
+    const uint16_t* vs = reinterpret_cast<const uint16_t*>(v_new) + src;
+    uint32_t bad = 0;
+    for (int c = lane; c < D; c += 32) {
+        uint16_t kb = ks[c], vb = vs[c];
+        bad |= nonfinite(bf16_bits_to_float(kb)) | nonfinite(bf16_bits_to_float(vb));
+        slot[c] = kb;
+        slot[D + c] = vb;
+    }
+    return bad;
+}
+
+// INT8 / FP8: quantise one token row of (l, b, h) at absolute position t; one warp.
+__device__ __forceinline__ uint32_t quantise_row(const Layout& lo, uint8_t* cache, int l, int b,
+                                                 int h, int64_t t, const void* src_k,
+                                                 const void* src_v, int64_t row,
+                                                 const float* fp8_scales, int lane) {
+    const int D = lo.D;
+    uint8_t* base = cache + lo.data_off + unit_index(lo, l, b, h) * lo.unit;
+    uint32_t bad = 0;
+    for (int kv = 0; kv < 2; ++kv) {
+        const void* src = kv ? src_v : src_k;
+        uint8_t* codes = base + (int64_t)kv * lo.T16 * D + t * D;
+        if (lo.scheme == KVQ_SCHEME_INT8) {
+            float x[8];
+            const int cpl = (D + 31) / 32;
+            float a = 0.0f;
+            for (int e = 0; e < cpl; ++e) {
+                int c = lane + 32 * e;
+                x[e] = c < D ? load_input(src, row + c, lo.dtype) : 0.0f;
+                bad |= nonfinite(x[e]);
+                a = fmaxf(a, fabsf(x[e]));
+            }
+            for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+            float s = __fdiv_rn(a, 127.0f);
+            for (int e = 0; e < cpl; ++e) {
+                int c = lane + 32 * e;
+                if (c >= D) continue;
+                int code = 0;
+                if (s != 0.0f) {
+                    code = __float2int_rn(__fdiv_rn(x[e], s));
+                    code = code < -127 ? -127 : (code > 127 ? 127 : code);
+                }
+                codes[c] = static_cast<uint8_t>(static_cast<int8_t>(code));
+            }
+            if (lane == 0)
+                reinterpret_cast<float*>(base + 2 * (int64_t)lo.T16 * D)[(int64_t)kv * lo.T16 + t] = s;
+        } else {
+            const float s = fp8_scales[2 * h + kv];
+            for (int c = lane; c < D; c += 32) {
+                float x = load_input(src, row + c, lo.dtype);
+                bad |= nonfinite(x);
+                codes[c] = static_cast<uint8_t>(
+                    __nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3));
+            }
+        }
+    }
+    return bad;
+}
+
+struct AppendArgs {
+    Layout lo;
+    uint8_t* cache;
+    int layer, seq_begin, seq_count, n_new;
+    const void* k_new;
+    const void* v_new;
+    const int32_t* n_valid;
+    const float* fp8_scales;
+    uint32_t flags;
+};
+
+__device__ __forceinline__ int new_tokens(const AppendArgs& a, int bi) {
+    return a.n_valid ? a.n_valid[bi] : a.n_new;
+}
+
+// Small appends: one block per sequence does everything, so the window reads of a flush
+// are ordered before the window writes of the same append by a block barrier.
+__global__ void __launch_bounds__(kThreads) k_append_small(AppendArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const Layout& lo = a.lo;
+    const int bi = blockIdx.x, b = a.seq_begin + bi;
+    int32_t* st = state_ptr(lo, a.cache, a.layer, b);
+    const int n = st[0], qn = st[1];
+    uint32_t status = 0;
+    int m = new_tokens(a, bi);
+    m = m < 0 ? 0 : (m > a.n_new ? a.n_new : m);
+    if (tokens_taken(lo, n, qn, m, a.flags, &status) < 0) {
+        if (threadIdx.x == 0) atomicOr(reinterpret_cast<uint32_t*>(a.cache), status);
+        return;
+    }
+    uint32_t bad = 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    if (lo.scheme == KVQ_SCHEME_KIVI) {
+        const int qn2 = qn_after(lo, n, qn, m, a.flags);
+        for (int h = 0; h < lo.H; ++h) {
+            TokenSource s;
+            s.ring_unit = a.cache + lo.ring_off + unit_index(lo, a.layer, b, h) * lo.C * (int64_t)(4 * lo.D);
+            s.k_new = a.k_new;
+            s.v_new = a.v_new;
+            s.n = n;
+            s.n_new = a.n_new;
+            s.bi = bi;
+            for (int64_t t0 = qn; t0 < qn2; t0 += lo.G)
+                bad |= quantise_group(lo, a.cache, a.layer, b, h, t0, s, smem);
+        }
+        __syncthreads();
+        const int64_t first = n > qn2 ? n : qn2;
+        const int64_t rows = (int64_t)n + m - first;
+        for (int64_t r = warp; r < rows * lo.H; r += nwarps) {
+            const int h = static_cast<int>(r % lo.H);
+            const int64_t t = first + r / lo.H;
+            bad |= ring_write_row(lo, a.cache, a.layer, b, h, t, n, a.k_new, a.v_new, a.n_new, bi, lane);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            st[0] = n + m;
+            st[1] = qn2;
+        }
+    } else {
+        if (lo.scheme == KVQ_SCHEME_FP8_E4M3 && bi == 0)
+            for (int i = threadIdx.x; i < 2 * lo.H; i += blockDim.x)
+                reinterpret_cast<float*>(a.cache + lo.scales_off)[(int64_t)a.layer * lo.H * 2 + i] = a.fp8_scales[i];
+        for (int r = warp; r < m * lo.H; r += nwarps) {
+            const int h = r % lo.H, j = r / lo.H;
+            bad |= quantise_row(lo, a.cache, a.layer, b, h, (int64_t)n + j, a.k_new, a.v_new,
+                                input_row(lo, a.n_new, bi, j, h), a.fp8_scales, lane);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            st[0] = n + m;
+            st[1] = n + m;
+        }
+    }
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0 && bad) atomicOr(reinterpret_cast<uint32_t*>(a.cache), KVQ_STATUS_NONFINITE);
+}
+
+// Bulk appends, step 1 (KIVI): one block per (group to quantise, kv head, sequence).
+__global__ void __launch_bounds__(kThreads) k_append_groups(AppendArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const Layout& lo = a.lo;
+    const int bi = blockIdx.z, b = a.seq_begin + bi, h = blockIdx.y;
+    const int32_t* st = state_ptr(lo, a.cache, a.layer, b);
+    const int n = st[0], qn = st[1];
+    uint32_t dummy = 0;
+    int m = new_tokens(a, bi);
+    m = m < 0 ? 0 : (m > a.n_new ? a.n_new : m);
+    if (tokens_taken(lo, n, qn, m, a.flags, &dummy) < 0) return;
+    const int qn2 = qn_after(lo, n, qn, m, a.flags);
+    const int64_t t0 = qn + (int64_t)blockIdx.x * lo.G;
+    if (t0 >= qn2) return;
+    TokenSource s;
+    s.ring_unit = a.cache + lo.ring_off + unit_index(lo, a.layer, b, h) * lo.C * (int64_t)(4 * lo.D);
+    s.k_new = a.k_new;
+    s.v_new = a.v_new;
+    s.n = n;
+    s.n_new = a.n_new;
+    s.bi = bi;
+    uint32_t bad = quantise_group(lo, a.cache, a.layer, b, h, t0, s, smem);
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0 && bad) atomicOr(reinterpret_cast<uint32_t*>(a.cache), KVQ_STATUS_NONFINITE);
+}
+
+// Bulk appends, step 2: rows that do not become part of a group -- window rows (KIVI)
+// or quantised rows (INT8, FP8).  One warp per (row, kv head); grid (row blocks, seq).
+__global__ void __launch_bounds__(kThreads) k_append_rows(AppendArgs a) {
+    const Layout& lo = a.lo;
+    const int bi = blockIdx.y, b = a.seq_begin + bi;
+    const int32_t* st = state_ptr(lo, a.cache, a.layer, b);
+    const int n = st[0], qn = st[1];
+    uint32_t dummy = 0;
+    int m = new_tokens(a, bi);
+    m = m < 0 ? 0 : (m > a.n_new ? a.n_new : m);
+    if (tokens_taken(lo, n, qn, m, a.flags, &dummy) < 0) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    uint32_t bad = 0;
+    if (lo.scheme == KVQ_SCHEME_KIVI) {
+        const int qn2 = qn_after(lo, n, qn, m, a.flags);
+        const int64_t first = n > qn2 ? n : qn2;
+        const int64_t rows = (int64_t)n + m - first;
+        if (r < rows * lo.H) {
+            const int h = static_cast<int>(r % lo.H);
+            bad = ring_write_row(lo, a.cache, a.layer, b, h, first + r / lo.H, n, a.k_new, a.v_new,
+                                 a.n_new, bi, lane);
+        }
+    } else if (r < (int64_t)m * lo.H) {
+        const int h = static_cast<int>(r % lo.H);
+        const int64_t j = r / lo.H;
+        bad = quantise_row(lo, a.cache, a.layer, b, h, n + j, a.k_new, a.v_new,
+                           input_row(lo, a.n_new, bi, j, h), a.fp8_scales, lane);
+    }
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0 && bad) atomicOr(reinterpret_cast<uint32_t*>(a.cache), KVQ_STATUS_NONFINITE);
+}
+
+// Bulk appends, step 3: new per-sequence counts and status bits (and the FP8 scale table).
+__global__ void k_append_commit(AppendArgs a) {
+    const Layout& lo = a.lo;
+    if (lo.scheme == KVQ_SCHEME_FP8_E4M3 && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < 2 * lo.H; i += blockDim.x)
+            reinterpret_cast<float*>(a.cache + lo.scales_off)[(int64_t)a.layer * lo.H * 2 + i] = a.fp8_scales[i];
+    const int bi = blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t status = 0;
+    if (bi < a.seq_count) {
+        const int b = a.seq_begin + bi;
+        int32_t* st = state_ptr(lo, a.cache, a.layer, b);
+        const int n = st[0], qn = st[1];
+        int m = new_tokens(a, bi);
+        m = m < 0 ? 0 : (m > a.n_new ? a.n_new : m);
+        if (tokens_taken(lo, n, qn, m, a.flags, &status) >= 0) {
+            st[1] = qn_after(lo, n, qn, m, a.flags);
+            st[0] = n + m;
+        }
+    }
+    if (status) atomicOr(reinterpret_cast<uint32_t*>(a.cache), status);
+}
+
+// Explicit flush (KIVI): one block per (group index, kv head, sequence) quantises window
+// groups [qn + g*G, ...) while n - qn >= R + G; a second kernel commits qn.
+__global__ void __launch_bounds__(kThreads) k_flush_groups(Layout lo, uint8_t* cache, int layer) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int32_t* st = state_ptr(lo, cache, layer, b);
+    const int n = st[0], qn = st[1];
+    const int ready = (n - qn - lo.R) >= lo.G ? (n - qn - lo.R) / lo.G : 0;
+    if (static_cast<int>(blockIdx.x) >= ready) return;
+    TokenSource s;
+    s.ring_unit = cache + lo.ring_off + unit_index(lo, layer, b, h) * lo.C * (int64_t)(4 * lo.D);
+    s.k_new = nullptr;
+    s.v_new = nullptr;
+    s.n = n;
+    s.n_new = 0;
+    s.bi = 0;
+    uint32_t bad = quantise_group(lo, cache, layer, b, h, qn + (int64_t)blockIdx.x * lo.G, s, smem);
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0 && bad) atomicOr(reinterpret_cast<uint32_t*>(cache), KVQ_STATUS_NONFINITE);
+}
+
+__global__ void k_flush_commit(Layout lo, uint8_t* cache, int layer) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= lo.B) return;
+    int32_t* st = state_ptr(lo, cache, layer, b);
+    const int n = st[0], qn = st[1];
+    const int ready = (n - qn - lo.R) >= lo.G ? (n - qn - lo.R) / lo.G : 0;
+    st[1] = qn + ready * lo.G;
+}
+
+}  // namespace
+
+static size_t group_smem(const Layout& lo) {
+    return lo.scheme == KVQ_SCHEME_KIVI ? static_cast<size_t>(lo.G) * lo.D : 0;
+}
+
+static int set_smem(const void* fn, size_t bytes) {
+    if (bytes > 48 * 1024 &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+            cudaSuccess)
+        return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+int launch_append(const Layout& lo, uint8_t* cache, int layer, int seq_begin, int seq_count,
+                  const void* k_new, const void* v_new, int n_new, const int32_t* n_valid,
+                  const float* fp8_scales, uint32_t flags, cudaStream_t stream) {
+    if (seq_count == 0) return KVQ_OK;
+    AppendArgs a;
+    a.lo = lo;
+    a.cache = cache;
+    a.layer = layer;
+    a.seq_begin = seq_begin;
+    a.seq_count = seq_count;
+    a.n_new = n_new;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.n_valid = n_valid;
+    a.fp8_scales = fp8_scales;
+    a.flags = flags;
+    const size_t smem = group_smem(lo);
+    if (n_new <= kSmallAppend) {
+        if (set_smem(reinterpret_cast<const void*>(k_append_small), smem)) return KVQ_ERR_CUDA;
+        k_append_small<<<seq_count, kThreads, smem, stream>>>(a);
+        return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+    }
+    if (lo.scheme == KVQ_SCHEME_KIVI) {
+        // at most (window - 1 + n_new) / G groups leave the window in one append
+        const int64_t max_groups = ((int64_t)lo.C - 1 + n_new) / lo.G;
+        if (max_groups > 0) {
+            if (set_smem(reinterpret_cast<const void*>(k_append_groups), smem)) return KVQ_ERR_CUDA;
+            dim3 grid(static_cast<unsigned>(max_groups), lo.H, seq_count);
+            k_append_groups<<<grid, kThreads, smem, stream>>>(a);
+        }
+        const int64_t rows = (int64_t)(n_new < lo.C ? n_new : lo.C) * lo.H;
+        dim3 grid2(static_cast<unsigned>((rows + 3) / 4), seq_count);
+        k_append_rows<<<grid2, kThreads, 0, stream>>>(a);
+    } else {
+        const int64_t rows = (int64_t)n_new * lo.H;
+        dim3 grid2(static_cast<unsigned>((rows + 3) / 4), seq_count);
+        k_append_rows<<<grid2, kThreads, 0, stream>>>(a);
+    }
+    k_append_commit<<<(seq_count + 127) / 128, 128, 0, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+int launch_flush(const Layout& lo, uint8_t* cache, int layer, cudaStream_t stream) {
+    if (lo.scheme != KVQ_SCHEME_KIVI) return KVQ_OK;
+    // the window never holds more than R + G tokens, so at most one group per sequence
+    // and kv head is ready
+    const int max_groups = 1;
+    const size_t smem = group_smem(lo);
+    if (set_smem(reinterpret_cast<const void*>(k_flush_groups), smem)) return KVQ_ERR_CUDA;
+    dim3 grid(max_groups, lo.H, lo.B);
+    k_flush_groups<<<grid, kThreads, smem, stream>>>(lo, cache, layer);
+    k_flush_commit<<<(lo.B + 127) / 128, 128, 0, stream>>>(lo, cache, layer);
+    return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace kvq

@@ -1,0 +1,17 @@
+// kvq_decode_kivi4.cu -- decode kernels for 4-bit KIVI caches (one translation unit per bit
+// width so the build compiles them in parallel).
+#include "kvq_decode.cuh"
+
+namespace kvq {
+
+int launch_decode_kivi4(const DecodeArgs& a, cudaStream_t stream) {
+    const bool wide = a.lo.gqa > 4;
+    switch (a.lo.D) {
+        case 64: return wide ? launch_decode_t<64, 4, 2>(a, stream) : launch_decode_t<64, 4, 1>(a, stream);
+        case 128: return wide ? launch_decode_t<128, 4, 2>(a, stream) : launch_decode_t<128, 4, 1>(a, stream);
+        case 256: return wide ? launch_decode_t<256, 4, 2>(a, stream) : launch_decode_t<256, 4, 1>(a, stream);
+        default: return KVQ_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace kvq

@@ -1,0 +1,198 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle, element by element.
+
+Packed caches are compared byte for byte (the whole cache image, status word included);
+attention outputs within |gpu - oracle| <= 2e-3 + 1e-2 |oracle| per element.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from harness import Pair, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def gen(seed):
+    return torch.Generator().manual_seed(seed)
+
+
+# ------------------------------------------------------------------------- KIVI
+KIVI_CASES = [
+    # bits, D, gqa, G, Gv, R
+    (2, 128, 4, 32, 32, 128),
+    (2, 128, 4, 32, 16, 32),
+    (4, 128, 4, 128, 128, 128),
+    (4, 64, 2, 16, 16, 0),
+    (8, 128, 8, 64, 64, 40),
+    (2, 256, 1, 32, 64, 16),
+    (4, 256, 8, 16, 32, 48),
+    (8, 64, 4, 48, 64, 20),
+]
+
+
+@pytest.mark.parametrize("bits,D,gqa,G,Gv,R", KIVI_CASES)
+def test_kivi_bulk_then_steps(bits, D, gqa, G, Gv, R):
+    H = 2
+    p = Pair("kivi", layers=2, batch=3, q_heads=H * gqa, kv_heads=H, head_dim=D, max_tokens=700,
+             bits=bits, group_k=G, group_v=Gv, residual=R)
+    g = gen(bits * 1000 + D + gqa)
+    # ragged prefill of layer 1 through the bulk path, then single-token decode steps
+    k, v = p.rand_kv(3, 517, g)
+    p.append(1, k, v, n_valid=[517, 300, 1])
+    p.assert_same_image()
+    for step in range(G + 3):
+        k, v = p.rand_kv(3, 1, g)
+        p.append(1, k, v)
+        if step % 7 == 0 or step == G + 2:
+            p.assert_same_image()
+            out, ref = p.decode(1, p.rand_q(g))
+            assert_close(out, ref, what="kivi step %d" % step)
+    # layer 0 untouched: zero output
+    out, ref = p.decode(0, p.rand_q(g))
+    assert not out.any() and not ref.any()
+    assert p.status() == 0
+
+
+def test_kivi_small_appends_and_window_edges():
+    # appends of 1..16 tokens (the single-kernel path) across window fills and flushes
+    p = Pair("kivi", batch=2, q_heads=8, kv_heads=2, head_dim=128, max_tokens=400, bits=2,
+             group_k=32, group_v=32, residual=64)
+    g = gen(5)
+    total = 0
+    for m in [1, 16, 5, 16, 16, 16, 13, 1, 1, 9, 16, 16, 16, 16, 16, 3]:
+        k, v = p.rand_kv(2, m, g)
+        p.append(0, k, v)
+        total += m
+        p.assert_same_image()
+        out, ref = p.decode(0, p.rand_q(g))
+        assert_close(out, ref, what="after %d tokens" % total)
+
+
+def test_kivi_no_autoflush_and_explicit_flush():
+    p = Pair("kivi", batch=3, q_heads=4, kv_heads=1, head_dim=64, max_tokens=300, bits=4,
+             group_k=16, group_v=16, residual=24)
+    g = gen(6)
+    for step in range(90):
+        k, v = p.rand_kv(3, 1, g)
+        p.append(0, k, v, n_valid=[1, step % 2, 1], flags=1)
+        if step % 3 == 2:
+            p.flush(0)
+        if step % 10 == 9:
+            p.assert_same_image()
+            out, ref = p.decode(0, p.rand_q(g))
+            assert_close(out, ref, what="no-autoflush step %d" % step)
+    assert p.status() == 0
+
+
+def test_kivi_ring_full_and_capacity_status():
+    p = Pair("kivi", batch=2, q_heads=4, kv_heads=2, head_dim=64, max_tokens=120, bits=2,
+             group_k=16, group_v=16, residual=16)
+    g = gen(7)
+    k, v = p.rand_kv(2, 32, g)
+    p.append(0, k, v, flags=1)                  # window holds R + G = 32 tokens: full
+    k, v = p.rand_kv(2, 1, g)
+    p.append(0, k, v, flags=1)                  # overflow: skipped, RING_FULL
+    p.assert_same_image()
+    assert p.status() == 2
+    p.flush(0)
+    k, v = p.rand_kv(2, 100, g)
+    p.append(0, k, v, n_valid=[88, 89])         # 32 + 89 > 120: sequence 1 skipped, CAPACITY
+    p.assert_same_image()
+    assert p.status() == 3
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="after skips")
+
+
+def test_kivi_nonfinite_flag():
+    p = Pair("kivi", batch=1, q_heads=4, kv_heads=1, head_dim=64, max_tokens=64, bits=2,
+             group_k=16, group_v=16, residual=8)
+    g = gen(8)
+    k, v = p.rand_kv(1, 20, g)
+    k[0, 19, 0, 5] = float("nan")               # stays in the window: flagged, stored as is
+    p.append(0, k, v)
+    assert p.status() == 4
+    p.assert_same_image()
+
+
+def test_kivi_long_context_split():
+    # many packed chunks per (sequence, kv head): exercises the split context and the merge
+    p = Pair("kivi", batch=1, q_heads=32, kv_heads=8, head_dim=128, max_tokens=20000, bits=4,
+             group_k=128, group_v=128, residual=128)
+    g = gen(9)
+    k, v = p.rand_kv(1, 19000, g)
+    p.append(0, k, v)
+    p.assert_same_image()
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="long context")
+
+
+def test_kivi_peaky_attention_with_value_outliers():
+    # large logits concentrate attention on few tokens, where value-outlier tokens (x8) and
+    # key outlier channels stress the precision of the score and value contractions
+    p = Pair("kivi", batch=2, q_heads=8, kv_heads=2, head_dim=128, max_tokens=1200, bits=2,
+             group_k=32, group_v=32, residual=128)
+    g = gen(10)
+    k, v = p.rand_kv(2, 1100, g, scale=3.0)
+    p.append(0, k, v)
+    out, ref = p.decode(0, p.rand_q(g, scale=3.0), scale=1.0)
+    assert_close(out, ref, what="peaky")
+
+
+# ------------------------------------------------------------------------- INT8 / FP8
+def test_int8_tiny_workload():
+    # 1 layer, batch 1, 4 heads, head_dim 32, 256 fp32 tokens, two key channels x10,
+    # q ~ N(0,1)/sqrt(32), softmax scale 1
+    from quantised_kv_cache_kvq_gb300 import workloads as W
+    w = W.WORKLOADS["int8_tiny"]
+    p = Pair("int8", batch=1, q_heads=4, kv_heads=4, head_dim=32, max_tokens=256, in_dtype="f32")
+    k, v = W.kv_tokens(w, 0, 0, 1, 0, 256)
+    p.append(0, k[:, :200], v[:, :200])
+    for t in range(200, 256, 8):
+        p.append(0, k[:, t:t + 8], v[:, t:t + 8])
+    p.assert_same_image()
+    q = W.queries(w, 0)
+    out, ref = p.decode(0, q, scale=1.0)
+    assert_close(out, ref, what="int8 tiny")
+
+
+@pytest.mark.parametrize("D,gqa,dtype", [(128, 4, "bf16"), (64, 8, "f32"), (256, 1, "bf16"), (32, 2, "f32")])
+def test_int8_and_fp8_ragged(D, gqa, dtype):
+    for scheme in ("int8", "fp8"):
+        p = Pair(scheme, layers=2, batch=3, q_heads=2 * gqa, kv_heads=2, head_dim=D, max_tokens=333,
+                 in_dtype=dtype)
+        g = gen(D + gqa)
+        k, v = p.rand_kv(3, 250, g)
+        sc = None
+        if scheme == "fp8":
+            sc = torch.stack([k.float().abs().amax(dim=(0, 1, 3)), v.float().abs().amax(dim=(0, 1, 3))], 1) / 448
+        p.append(1, k, v, n_valid=[250, 17, 0], fp8_scales=sc)
+        for _ in range(5):
+            k2, v2 = p.rand_kv(3, 1, g)
+            p.append(1, k2, v2, fp8_scales=sc)
+        p.assert_same_image()
+        out, ref = p.decode(1, p.rand_q(g))
+        assert_close(out, ref, what=scheme)
+        k3, v3 = p.rand_kv(3, 100, g)
+        p.append(1, k3, v3, n_valid=[100, 0, 0], fp8_scales=sc)  # 255 + 100 > 333
+        assert p.status() == 1
+        p.assert_same_image()
+
+
+def test_fp8_saturation_and_subnormals():
+    p = Pair("fp8", batch=1, q_heads=4, kv_heads=1, head_dim=128, max_tokens=32)
+    g = gen(12)
+    k, v = p.rand_kv(1, 20, g)
+    k[0, 0, 0, :8] = torch.tensor([1e4, -1e4, 1e-6, -1e-6, 449.0, 447.0, 0.0, -0.0])
+    sc = torch.tensor([[1.0, 0.5]])
+    p.append(0, k, v, fp8_scales=sc)
+    p.assert_same_image()
