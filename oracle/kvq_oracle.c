@@ -493,7 +493,12 @@ uint32_t kvqo_append(const kvqo_config* c, uint8_t* img, int l, int seq_begin, i
         int m = n_valid ? n_valid[bi] : n_new;
         int32_t* s = state_of(c, img, l, b);
         int64_t n = s[0], qn = s[1];
+        /* a sequence that cannot take the tokens is left unchanged */
         if (n + m > c->max_tokens) { st |= ST_CAPACITY; continue; }
+        if (c->scheme == SCHEME_KIVI && (flags & FLAG_NO_AUTOFLUSH) && n + m - qn > L.cap) {
+            st |= ST_RING_FULL;
+            continue;
+        }
         /* non-finite inputs are flagged; the values are still stored */
         for (int h = 0; h < H; h++)
             for (int j = 0; j < m; j++) {
@@ -508,9 +513,6 @@ uint32_t kvqo_append(const kvqo_config* c, uint8_t* img, int l, int seq_begin, i
             if (!(flags & FLAG_NO_AUTOFLUSH)) {
                 int64_t over = n + m - qn - R;
                 if (over >= G) qn2 = qn + G * (over / G);
-            } else if (n + m - qn > cap) {
-                st |= ST_RING_FULL;
-                continue;
             }
             for (int h = 0; h < H; h++) {
                 for (int64_t t0 = qn; t0 < qn2; t0 += G)
