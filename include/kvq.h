@@ -101,7 +101,7 @@ enum kvq_status_bits {
  *   head_dim    channels per head: 64, 128 or 256 (KIVI); 32, 64, 128 or 256 (INT8, FP8)
  *   bits        KIVI: 2, 4 or 8; INT8 and FP8: 8 (the formula mode uses it as the
  *               bits per value, and accepts 16 for an unquantised reference size)
- *   group_k     KIVI G: tokens per key group, a multiple of 16 in [16, 512]
+ *   group_k     KIVI G: tokens per key group, a multiple of 16 in [16, 128]
  *   group_v     KIVI Gv: channels per value group, a multiple of 16 dividing head_dim
  *   residual    KIVI R: newest tokens kept in the bf16 window (>= 0)
  *   max_tokens  per-sequence capacity in tokens (>= 1)

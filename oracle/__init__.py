@@ -149,7 +149,7 @@ class Image:
         return int(self.buf[:4].view(np.uint32)[0])
 
     def state(self, layer, seq):
-        off = 256 + 8 * (layer * self.cfg.batch + seq)
+        off = 256 + 16 * (layer * self.cfg.batch + seq)
         n, qn = self.buf[off:off + 8].view(np.int32)
         return int(n), int(qn)
 

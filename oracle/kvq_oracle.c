@@ -267,12 +267,14 @@ void kvqo_int8_token(const float* x, int n, float* scale_out, int8_t* codes)
  * aligned to 256 bytes, little-endian):
  *   header 256 B: u32 status at byte 0.
  *   state: for (layer l, sequence b): int32 n (tokens cached), int32 qn (tokens held in
- *          packed groups; n for INT8/FP8), at byte 8 * (l * batch + b).
+ *          packed groups; n for INT8/FP8), then two reserved int32 that are zero whenever
+ *          no call is running, at byte 16 * (l * batch + b).
  *   KIVI:  group records, one per (l, b, kv head h, group slot g), NG = (T - R) / G slots:
  *            K codes  G*D*b/8 bytes, token-major: (token t, channel c) at bit (t*D + c)*b
  *            V codes  D*G*b/8 bytes, channel-major: (channel c, token t) at bit (c*G + t)*b
  *            K params 4*D bytes: fp16 scale[D], then fp16 zero[D]
- *            V params 4*G*NGv bytes: fp16 scale[G][NGv], then fp16 zero[G][NGv]
+ *            V params 4*G*NGv bytes: for token t and value group j, fp16 scale then fp16
+ *                     zero at byte 4 * (t*NGv + j)
  *          then the bf16 ring: (l, b, h, slot s) holds K row[D] then V row[D], C = R + G
  *          slots; token t (qn <= t < n) sits in slot t mod C.
  *   INT8:  per (l, b, h) block over T16 = T rounded up to 16:
@@ -297,7 +299,7 @@ static layout_t make_layout(const kvqo_config* c)
     int64_t D = c->head_dim;
     L.header = 0;
     L.state = 256;
-    int64_t pos = L.state + up256((int64_t)c->layers * c->batch * 8);
+    int64_t pos = L.state + up256((int64_t)c->layers * c->batch * 16);
     L.t16 = ((int64_t)c->max_tokens + 15) / 16 * 16;
     if (c->scheme == SCHEME_KIVI) {
         int64_t G = c->group_k, b = c->bits;
@@ -345,7 +347,7 @@ void kvqo_image_regions(const kvqo_config* c, int64_t* out /* [6] */)
 
 static int32_t* state_of(const kvqo_config* c, uint8_t* img, int l, int b)
 {
-    return (int32_t*)(img + 256 + 8 * ((int64_t)l * c->batch + b));
+    return (int32_t*)(img + 256 + 16 * ((int64_t)l * c->batch + b));
 }
 
 static uint8_t* unit_base(const kvqo_config* c, const layout_t* L, uint8_t* img, int l, int b,
@@ -444,8 +446,8 @@ static void kivi_quantise_group(const kvqo_config* c, const layout_t* L, uint8_t
         for (int j = 0; j < ngv; j++) {
             uint16_t s, z;
             kvqo_qb_group(V + (int64_t)i * D + (int64_t)j * Gv, Gv, 1, bits, &s, &z, codes);
-            put_u16(vpar + 2 * (i * ngv + j), s);
-            put_u16(vpar + 2 * (G * ngv) + 2 * (i * ngv + j), z);
+            put_u16(vpar + 4 * (i * ngv + j), s);
+            put_u16(vpar + 4 * (i * ngv + j) + 2, z);
             for (int cc = 0; cc < Gv; cc++) {
                 int ch = j * Gv + cc;
                 put_bits(vcodes, ((int64_t)ch * G + i) * bits, bits, codes[cc]);
@@ -612,8 +614,8 @@ void kvqo_dequant_token(const kvqo_config* c, const uint8_t* img, int l, int b, 
                 kout[ch] = kvqo_qb_dequant(kc, get_u16(kpar + 2 * ch), get_u16(kpar + 2 * D + 2 * ch));
                 int vc = get_bits(rec + L.kc, ((int64_t)ch * G + i) * bits, bits);
                 int j = ch / Gv;
-                vout[ch] = kvqo_qb_dequant(vc, get_u16(vpar + 2 * (i * L.ngv + j)),
-                                           get_u16(vpar + 2 * (G * L.ngv) + 2 * (i * L.ngv + j)));
+                vout[ch] = kvqo_qb_dequant(vc, get_u16(vpar + 4 * (i * L.ngv + j)),
+                                           get_u16(vpar + 4 * (i * L.ngv + j) + 2));
             }
         } else {
             int64_t u = ((int64_t)l * c->batch + b) * c->kv_heads + h;

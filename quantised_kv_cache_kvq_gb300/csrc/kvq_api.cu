@@ -39,11 +39,11 @@ int make_layout(const kvq_config* c, int64_t max_tokens, Layout* out) {
     lo.T16 = static_cast<int32_t>((max_tokens + 15) / 16 * 16);
     const int64_t units = (int64_t)lo.L * lo.B * lo.H;
     lo.state_off = 256;
-    int64_t pos = lo.state_off + align256((int64_t)lo.L * lo.B * 8);
+    int64_t pos = lo.state_off + align256((int64_t)lo.L * lo.B * 16);
     if (c->scheme == KVQ_SCHEME_KIVI) {
         if (!pow2_in(D, 64, 256)) return KVQ_ERR_UNSUPPORTED;
         if (c->bits != 2 && c->bits != 4 && c->bits != 8) return KVQ_ERR_ARG;
-        if (c->group_k < 16 || c->group_k > 512 || c->group_k % 16 != 0) return KVQ_ERR_ARG;
+        if (c->group_k < 16 || c->group_k > 128 || c->group_k % 16 != 0) return KVQ_ERR_ARG;
         if (c->group_v < 16 || c->group_v % 16 != 0 || D % c->group_v != 0) return KVQ_ERR_ARG;
         if (c->residual < 0 || c->residual > (1 << 20)) return KVQ_ERR_ARG;
         if (c->in_dtype != KVQ_DTYPE_BF16) return KVQ_ERR_ARG;
@@ -83,29 +83,32 @@ int make_plan(const Layout& lo, DecodePlan* p) {
     std::memset(p, 0, sizeof *p);
     p->NT = lo.gqa > 4 ? 2 : 1;
     const int64_t units = (int64_t)lo.B * lo.H;
-    const int64_t target_items = 4 * 152;  // a few waves of blocks across the SMs
     if (lo.scheme == KVQ_SCHEME_KIVI) {
         p->CHR = 64;
         p->NRC = (lo.C + p->CHR - 1) / p->CHR;
-        // packed chunk: a whole number of groups and of 64-token warp tiles
-        int unitCH = lo.G;
-        while (unitCH % 64) unitCH += lo.G;
+        // a warp takes W tokens: whole groups, at least 64 tokens; a block takes 4 warps
+        const int W = lo.G >= 64 ? lo.G : lo.G * ((64 + lo.G - 1) / lo.G);
+        p->W = W;
+        p->CH = 4 * W;
+        // chunks per item: about 8 blocks per SM over all units (capacity-based; items
+        // beyond a sequence's length exit at once), at most 32 chunks per item
         const int64_t packed = (int64_t)lo.NG * lo.G;
-        const int64_t per_unit = (target_items + units - 1) / units;
-        int64_t ch = per_unit > 0 ? (packed + per_unit - 1) / per_unit : packed;
-        ch = (ch + unitCH - 1) / unitCH * unitCH;
-        int64_t max_ch = (int64_t)(65536 / lo.rec) * lo.G;  // keep the staged records near 64 KiB
-        max_ch = max_ch / unitCH * unitCH;
-        if (max_ch > 512) max_ch = 512 / unitCH * unitCH;
-        if (max_ch < unitCH) max_ch = unitCH;
-        if (ch > max_ch) ch = max_ch;
-        if (ch < unitCH) ch = unitCH;
-        p->CH = static_cast<int>(ch);
-        p->NQ = static_cast<int>((packed + ch - 1) / ch);
+        const int64_t chunks = (packed + p->CH - 1) / p->CH;
+        const int64_t target = 8 * 152;
+        int64_t cpi = (units * chunks + target - 1) / target;
+        cpi = cpi < 1 ? 1 : (cpi > 32 ? 32 : cpi);
+        p->CPI = static_cast<int>(cpi);
+        // double-buffer the chunks of multi-chunk items when two stages stay within 64 KiB
+        const int64_t stage = (int64_t)(p->CH / lo.G) * lo.rec;
+        p->NSTAGE = (cpi > 1 && 2 * stage <= 65536) ? 2 : 1;
+        p->NQ = static_cast<int>((chunks + cpi - 1) / cpi);
     } else {
         p->CHR = 128;
         p->NRC = (lo.T + p->CHR - 1) / p->CHR;
         p->CH = 0;
+        p->W = 0;
+        p->CPI = 1;
+        p->NSTAGE = 1;
         p->NQ = 0;
     }
     p->S = p->NRC + p->NQ;
@@ -170,7 +173,7 @@ int kvq_cache_init(const kvq_config* cfg, void* cache, kvq_stream_t stream) {
     if (!aligned(cache, 256)) return KVQ_ERR_ALIGN;
     // header, status and the per-sequence counts; the FP8 scale table too (unset scales
     // read as zero until the first append of a layer)
-    const int64_t clear = lo.scheme == KVQ_SCHEME_FP8_E4M3 ? lo.data_off : lo.state_off + kvq::align256((int64_t)lo.L * lo.B * 8);
+    const int64_t clear = lo.scheme == KVQ_SCHEME_FP8_E4M3 ? lo.data_off : lo.state_off + kvq::align256((int64_t)lo.L * lo.B * 16);
     if (cudaMemsetAsync(cache, 0, static_cast<size_t>(clear), reinterpret_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return KVQ_ERR_CUDA;

@@ -94,10 +94,12 @@ struct TokenSource {
 };
 // Quantise the KIVI group of G tokens starting at absolute token t0 of unit (l, b, h)
 // into its record.  Token t < s.n comes from window slot t % C, later tokens from the
-// new input rows.  Cooperative over the whole block; `codes` is G*D bytes of shared
-// memory.  Returns the non-finite flag seen by this thread.
+// new input rows.  Cooperative over the whole block.  The group's bf16 keys and values
+// are first staged into shared memory with 16-byte loads; `smem` holds 5*G*D bytes
+// (keys G*D bf16, values G*D bf16, codes G*D bytes).  Returns the non-finite flag
+// seen by this thread.
 __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int b, int h,
-                                   int64_t t0, const TokenSource& s, uint8_t* codes) {
+                                   int64_t t0, const TokenSource& s, uint8_t* smem) {
     const int D = lo.D, G = lo.G, Gv = lo.Gv, bits = lo.bits;
     const int levels = (1 << bits) - 1;
     const float flevels = static_cast<float>(levels);
@@ -105,28 +107,38 @@ __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int 
     uint8_t* rec = cache + lo.data_off + u * lo.unit + (t0 / G) * (int64_t)lo.rec;
     __half* kpar = reinterpret_cast<__half*>(rec + lo.kc + lo.vc);
     __half* vpar = reinterpret_cast<__half*>(rec + lo.kc + lo.vc + lo.kp);
+    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);
+    uint16_t* vs = ks + G * D;
+    uint8_t* codes = reinterpret_cast<uint8_t*>(vs + G * D);
     uint32_t bad = 0;
-    auto kval = [&](int i, int c) -> float {
-        int64_t t = t0 + i;
-        if (t < s.n)
-            return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(
-                s.ring_unit + (t % lo.C) * (int64_t)(4 * D))[c]);
-        return load_input(s.k_new, input_row(lo, s.n_new, s.bi, t - s.n, h) + c, lo.dtype);
-    };
-    auto vval = [&](int i, int c) -> float {
-        int64_t t = t0 + i;
-        if (t < s.n)
-            return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(
-                s.ring_unit + (t % lo.C) * (int64_t)(4 * D) + 2 * D)[c]);
-        return load_input(s.v_new, input_row(lo, s.n_new, s.bi, t - s.n, h) + c, lo.dtype);
-    };
 
+    // stage the G key and value rows (16-byte pieces; rows are 2*D bytes)
+    {
+        const int cpr = D / 8;
+        for (int idx = threadIdx.x; idx < G * cpr; idx += blockDim.x) {
+            const int i = idx / cpr, piece = idx % cpr;
+            const int64_t t = t0 + i;
+            const uint16_t* kr;
+            const uint16_t* vr;
+            if (t < s.n) {
+                kr = reinterpret_cast<const uint16_t*>(s.ring_unit + (t % lo.C) * (int64_t)(4 * D));
+                vr = kr + D;
+            } else {
+                const int64_t row = input_row(lo, s.n_new, s.bi, t - s.n, h);
+                kr = reinterpret_cast<const uint16_t*>(s.k_new) + row;
+                vr = reinterpret_cast<const uint16_t*>(s.v_new) + row;
+            }
+            reinterpret_cast<uint4*>(ks + i * D)[piece] = reinterpret_cast<const uint4*>(kr)[piece];
+            reinterpret_cast<uint4*>(vs + i * D)[piece] = reinterpret_cast<const uint4*>(vr)[piece];
+        }
+    }
+    __syncthreads();
     // keys: one thread per channel, statistics over the G tokens of the group
     for (int c = threadIdx.x; c < D; c += blockDim.x) {
-        float mn = kval(0, c), mx = mn;
+        float mn = bf16_bits_to_float(ks[c]), mx = mn;
         bad |= nonfinite(mn);
         for (int i = 1; i < G; ++i) {
-            float x = kval(i, c);
+            const float x = bf16_bits_to_float(ks[i * D + c]);
             bad |= nonfinite(x);
             mn = fminf(mn, x);
             mx = fmaxf(mx, x);
@@ -134,7 +146,8 @@ __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int 
         QbParams p = qb_params(mn, mx, flevels);
         kpar[c] = p.s;
         kpar[D + c] = p.z;
-        for (int i = 0; i < G; ++i) codes[i * D + c] = static_cast<uint8_t>(qb_code(kval(i, c), p, levels));
+        for (int i = 0; i < G; ++i)
+            codes[i * D + c] = static_cast<uint8_t>(qb_code(bf16_bits_to_float(ks[i * D + c]), p, levels));
     }
     __syncthreads();
     // pack token-major: code index i*D + c at bit (i*D + c)*bits, 16-byte stores
@@ -159,7 +172,7 @@ __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int 
             float x[8];
             float mn = INFINITY, mx = -INFINITY;
             for (int e = 0; e < cpl; ++e) {
-                x[e] = vval(i, lane * cpl + e);
+                x[e] = bf16_bits_to_float(vs[i * D + lane * cpl + e]);
                 bad |= nonfinite(x[e]);
                 mn = fminf(mn, x[e]);
                 mx = fmaxf(mx, x[e]);
@@ -171,8 +184,8 @@ __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int 
             QbParams p = qb_params(mn, mx, flevels);
             const int gv = (lane * cpl) / Gv;
             if ((lane % lpg) == 0) {
-                vpar[i * lo.NGv + gv] = p.s;
-                vpar[G * lo.NGv + i * lo.NGv + gv] = p.z;
+                vpar[2 * (i * lo.NGv + gv)] = p.s;
+                vpar[2 * (i * lo.NGv + gv) + 1] = p.z;
             }
             // channel-major staging: code of (channel c, token i) at c*G + i
             for (int e = 0; e < cpl; ++e)
@@ -207,11 +220,33 @@ __device__ __forceinline__ uint32_t ring_write_row(const Layout& lo, uint8_t* ca
     const uint16_t* ks = reinterpret_cast<const uint16_t*>(k_new) + src;
     const uint16_t* vs = reinterpret_cast<const uint16_t*>(v_new) + src;
     uint32_t bad = 0;
-    for (int c = lane; c < D; c += 32) {
-        uint16_t kb = ks[c], vb = vs[c];
-        bad |= nonfinite(bf16_bits_to_float(kb)) | nonfinite(bf16_bits_to_float(vb));
-        slot[c] = kb;
-        slot[D + c] = vb;
+    // D/32 consecutive channels per lane (2 to 8 bf16 values): one vector load and store
+    // each for keys and values; input rows are 16-byte aligned (16-byte aligned base, D a
+    // multiple of 64)
+    const int cpl = D / 32;
+    for (int c = lane * cpl; c < D; c += 32 * cpl) {
+        uint32_t kw[4] = {0u, 0u, 0u, 0u}, vw[4] = {0u, 0u, 0u, 0u};
+        if (cpl == 8) {
+            const uint4 k4 = *reinterpret_cast<const uint4*>(ks + c), v4 = *reinterpret_cast<const uint4*>(vs + c);
+            kw[0] = k4.x; kw[1] = k4.y; kw[2] = k4.z; kw[3] = k4.w;
+            vw[0] = v4.x; vw[1] = v4.y; vw[2] = v4.z; vw[3] = v4.w;
+            *reinterpret_cast<uint4*>(slot + c) = k4;
+            *reinterpret_cast<uint4*>(slot + D + c) = v4;
+        } else if (cpl == 4) {
+            const uint2 k2 = *reinterpret_cast<const uint2*>(ks + c), v2 = *reinterpret_cast<const uint2*>(vs + c);
+            kw[0] = k2.x; kw[1] = k2.y; vw[0] = v2.x; vw[1] = v2.y;
+            *reinterpret_cast<uint2*>(slot + c) = k2;
+            *reinterpret_cast<uint2*>(slot + D + c) = v2;
+        } else {
+            kw[0] = *reinterpret_cast<const uint32_t*>(ks + c);
+            vw[0] = *reinterpret_cast<const uint32_t*>(vs + c);
+            *reinterpret_cast<uint32_t*>(slot + c) = kw[0];
+            *reinterpret_cast<uint32_t*>(slot + D + c) = vw[0];
+        }
+        for (int e = 0; e < (cpl + 1) / 2; ++e) {
+            bad |= nonfinite(__uint_as_float(kw[e] << 16)) | nonfinite(__uint_as_float(kw[e] & 0xffff0000u));
+            bad |= nonfinite(__uint_as_float(vw[e] << 16)) | nonfinite(__uint_as_float(vw[e] & 0xffff0000u));
+        }
     }
     return bad;
 }
@@ -279,66 +314,61 @@ __device__ __forceinline__ int new_tokens(const AppendArgs& a, int bi) {
     return a.n_valid ? a.n_valid[bi] : a.n_new;
 }
 
-// Small appends: one block per sequence does everything, so the window reads of a flush
-// are ordered before the window writes of the same append by a block barrier.
+// Small appends: one block per (kv head, sequence).  Each block flushes its head's full
+// groups (reading the window) before writing its head's new window rows, so the reads
+// and writes of the same slots are ordered by a block barrier.  Every block of a
+// sequence reads the old token counts first; the last block of the sequence to finish
+// (an arrival counter in the sequence's state entry, zero at rest) writes the new ones.
 __global__ void __launch_bounds__(kThreads) k_append_small(AppendArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const Layout& lo = a.lo;
-    const int bi = blockIdx.x, b = a.seq_begin + bi;
+    const int h = blockIdx.x, bi = blockIdx.y, b = a.seq_begin + bi;
     int32_t* st = state_ptr(lo, a.cache, a.layer, b);
     const int n = st[0], qn = st[1];
     uint32_t status = 0;
     int m = new_tokens(a, bi);
     m = m < 0 ? 0 : (m > a.n_new ? a.n_new : m);
     if (tokens_taken(lo, n, qn, m, a.flags, &status) < 0) {
-        if (threadIdx.x == 0) atomicOr(reinterpret_cast<uint32_t*>(a.cache), status);
+        if (threadIdx.x == 0 && h == 0) atomicOr(reinterpret_cast<uint32_t*>(a.cache), status);
         return;
     }
     uint32_t bad = 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    int qn2 = n + m;
     if (lo.scheme == KVQ_SCHEME_KIVI) {
-        const int qn2 = qn_after(lo, n, qn, m, a.flags);
-        for (int h = 0; h < lo.H; ++h) {
-            TokenSource s;
-            s.ring_unit = a.cache + lo.ring_off + unit_index(lo, a.layer, b, h) * lo.C * (int64_t)(4 * lo.D);
-            s.k_new = a.k_new;
-            s.v_new = a.v_new;
-            s.n = n;
-            s.n_new = a.n_new;
-            s.bi = bi;
-            for (int64_t t0 = qn; t0 < qn2; t0 += lo.G)
-                bad |= quantise_group(lo, a.cache, a.layer, b, h, t0, s, smem);
-        }
+        qn2 = qn_after(lo, n, qn, m, a.flags);
+        TokenSource s;
+        s.ring_unit = a.cache + lo.ring_off + unit_index(lo, a.layer, b, h) * lo.C * (int64_t)(4 * lo.D);
+        s.k_new = a.k_new;
+        s.v_new = a.v_new;
+        s.n = n;
+        s.n_new = a.n_new;
+        s.bi = bi;
+        for (int64_t t0 = qn; t0 < qn2; t0 += lo.G)
+            bad |= quantise_group(lo, a.cache, a.layer, b, h, t0, s, smem);
         __syncthreads();
         const int64_t first = n > qn2 ? n : qn2;
-        const int64_t rows = (int64_t)n + m - first;
-        for (int64_t r = warp; r < rows * lo.H; r += nwarps) {
-            const int h = static_cast<int>(r % lo.H);
-            const int64_t t = first + r / lo.H;
+        for (int64_t t = first + warp; t < (int64_t)n + m; t += nwarps)
             bad |= ring_write_row(lo, a.cache, a.layer, b, h, t, n, a.k_new, a.v_new, a.n_new, bi, lane);
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            st[0] = n + m;
-            st[1] = qn2;
-        }
     } else {
-        if (lo.scheme == KVQ_SCHEME_FP8_E4M3 && bi == 0)
+        if (lo.scheme == KVQ_SCHEME_FP8_E4M3 && bi == 0 && h == 0)
             for (int i = threadIdx.x; i < 2 * lo.H; i += blockDim.x)
                 reinterpret_cast<float*>(a.cache + lo.scales_off)[(int64_t)a.layer * lo.H * 2 + i] = a.fp8_scales[i];
-        for (int r = warp; r < m * lo.H; r += nwarps) {
-            const int h = r % lo.H, j = r / lo.H;
+        for (int j = warp; j < m; j += nwarps)
             bad |= quantise_row(lo, a.cache, a.layer, b, h, (int64_t)n + j, a.k_new, a.v_new,
                                 input_row(lo, a.n_new, bi, j, h), a.fp8_scales, lane);
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            st[0] = n + m;
-            st[1] = n + m;
-        }
     }
     bad = __syncthreads_or(bad);
-    if (threadIdx.x == 0 && bad) atomicOr(reinterpret_cast<uint32_t*>(a.cache), KVQ_STATUS_NONFINITE);
+    if (threadIdx.x == 0) {
+        if (bad) atomicOr(reinterpret_cast<uint32_t*>(a.cache), KVQ_STATUS_NONFINITE);
+        __threadfence();
+        if (atomicAdd(&st[2], 1) == lo.H - 1) {
+            st[0] = n + m;
+            st[1] = qn2;
+            st[2] = 0;
+            __threadfence();
+        }
+    }
 }
 
 // Bulk appends, step 1 (KIVI): one block per (group to quantise, kv head, sequence).
@@ -455,7 +485,7 @@ __global__ void k_flush_commit(Layout lo, uint8_t* cache, int layer) {
 }  // namespace
 
 static size_t group_smem(const Layout& lo) {
-    return lo.scheme == KVQ_SCHEME_KIVI ? static_cast<size_t>(lo.G) * lo.D : 0;
+    return lo.scheme == KVQ_SCHEME_KIVI ? static_cast<size_t>(5) * lo.G * lo.D : 0;
 }
 
 static int set_smem(const void* fn, size_t bytes) {
@@ -485,7 +515,7 @@ int launch_append(const Layout& lo, uint8_t* cache, int layer, int seq_begin, in
     const size_t smem = group_smem(lo);
     if (n_new <= kSmallAppend) {
         if (set_smem(reinterpret_cast<const void*>(k_append_small), smem)) return KVQ_ERR_CUDA;
-        k_append_small<<<seq_count, kThreads, smem, stream>>>(a);
+        k_append_small<<<dim3(lo.H, seq_count), kThreads, smem, stream>>>(a);
         return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
     }
     if (lo.scheme == KVQ_SCHEME_KIVI) {

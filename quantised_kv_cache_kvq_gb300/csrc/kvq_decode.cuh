@@ -57,8 +57,9 @@ __host__ __device__ inline ItemRange item_range(const Layout& lo, const DecodePl
         r.t0 = base + (int64_t)item * p.CHR;
         r.t1 = r.t0 + p.CHR < n ? r.t0 + p.CHR : n;
     } else {
-        r.t0 = (int64_t)(item - p.NRC) * p.CH;
-        r.t1 = r.t0 + p.CH < qn ? r.t0 + p.CH : qn;
+        const int64_t span = (int64_t)p.CPI * p.CH;
+        r.t0 = (int64_t)(item - p.NRC) * span;
+        r.t1 = r.t0 + span < qn ? r.t0 + span : qn;
     }
     return r;
 }
@@ -66,6 +67,13 @@ __host__ __device__ inline ItemRange item_range(const Layout& lo, const DecodePl
 __device__ __forceinline__ float load_q(const void* q, int64_t idx, int dtype) {
     if (dtype == KVQ_DTYPE_BF16) return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(q)[idx]);
     return reinterpret_cast<const float*>(q)[idx];
+}
+
+// 2^x by the hardware approximation (relative error about 2^-22; flushes subnormals)
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -293,42 +301,56 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, int shift) {
     return h2_as_u32(__hsub2(u32_as_h2(x), __half2(__half(1024.0f), __half(1024.0f))));
 }
 
+// One packed work item: a run of chunks of CH = 4 * W tokens of one (sequence, kv head).
+// Chunks are staged by bulk copies into NSTAGE shared-memory buffers (double-buffered
+// when they fit), each warp takes W tokens of a chunk, and every warp keeps an online
+// softmax (running max, sum and output) across the chunks of the item.
 template <int D, int BITS, int NT>
 __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& so, int b, int h,
                             int item, int64_t t0, int64_t t1) {
-    constexpr int CPW = 32 / BITS;         // key channels per 32-bit word
-    constexpr int HPW = CPW / 2;           // code pairs per word
-    constexpr int NPAIR = D / 8;           // code pairs per thread per token row
+    constexpr int CPW = 32 / BITS;          // key channels per 32-bit word
+    constexpr int HPW = CPW / 2;            // code pairs per word
+    constexpr int NPAIR = D / 8;            // code pairs per thread per token row
     constexpr int KSTEPS = D / 16;
-    constexpr int ROWW = D * BITS / 128;   // words per thread per token row
-    constexpr int MT = D / 64;             // 16-channel tiles per warp in the value pass
-    constexpr int TPW = 32 / BITS;         // value tokens per word
+    constexpr int ROWW = D * BITS / 128;    // words per thread per token row
+    constexpr int MTV = D / 16;             // 16-channel tiles of the value contraction
+    constexpr int TPW = 32 / BITS;          // value tokens per word
     constexpr int HW = TPW / 2;
+    constexpr int MAXT = 8;                 // a warp holds at most 8 tiles (W <= 128 tokens)
     const Layout& lo = a.lo;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
-    const int G = lo.G, CH = a.plan.CH;
-    const int ntok = static_cast<int>(t1 - t0);
-    const int gqa = lo.gqa;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + so.bar);
+    const int G = lo.G, W = a.plan.W, CH = a.plan.CH, gqa = lo.gqa, NGv = lo.NGv;
+    const int nstage = a.plan.NSTAGE;
+    const int64_t stage_bytes = (int64_t)(CH / G) * lo.rec;
+    const int nch = static_cast<int>((t1 - t0 + CH - 1) / CH);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + so.bar);
     float* red = reinterpret_cast<float*>(smem + so.red);
-    float* hstat = reinterpret_cast<float*>(smem + so.hstat);
     float* qs = reinterpret_cast<float*>(smem + so.qs);
     uint32_t* qpa = reinterpret_cast<uint32_t*>(smem + so.qpa);
     uint32_t* qpb = reinterpret_cast<uint32_t*>(smem + so.qpb);
-    float* sc = reinterpret_cast<float*>(smem + so.sc);
-    uint8_t* data = smem + so.data;
+    float* comb = reinterpret_cast<float*>(smem + so.sc);          // [warp][head][D + 2]
     const int64_t u = unit_index(lo, a.layer, b, h);
+    const uint8_t* src_unit = a.cache + lo.data_off + u * lo.unit;
 
-    if (tid == 0) mbar_init(bar, 1);
+    auto issue = [&](int j) {       // stage chunk j (thread 0 only)
+        const int64_t c0 = t0 + (int64_t)j * CH;
+        const int64_t ctok = (t1 - c0) < CH ? (t1 - c0) : CH;
+        const uint32_t bytes = static_cast<uint32_t>(ctok / G) * lo.rec;
+        uint64_t* bar = bars + (j % nstage);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_copy_pieces(smem + so.data + (j % nstage) * stage_bytes, src_unit + (c0 / G) * (int64_t)lo.rec, bytes, bar);
+    };
+    if (tid == 0) {
+        for (int s2 = 0; s2 < nstage; ++s2) mbar_init(bars + s2, 1);
+    }
     __syncthreads();
     if (tid == 0) {
-        const uint32_t bytes = static_cast<uint32_t>(ntok / G) * lo.rec;
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_copy_pieces(data, a.cache + lo.data_off + u * lo.unit + (t0 / G) * (int64_t)lo.rec, bytes, bar);
+        for (int j = 0; j < nstage && j < nch; ++j) issue(j);
     }
-    // query prep while the copy is in flight: scaled query, a power-of-two prescale that
-    // brings max|q| into [0.5, 1) (so fp16 products cannot overflow), and the query in
-    // the thread-pair order of the key fragments as fp16 major + minor parts
+    // query prep (whole block) while the copies are in flight: fp32 scaled query, a
+    // power-of-two prescale bringing max|q| into [0.5, 1) so fp16 products cannot
+    // overflow, and the query in the thread-pair order of the key fragments split into
+    // fp16 major + minor parts
     load_query(a, b, h, qs);
     __syncthreads();
     float qmax = 0.0f;
@@ -351,222 +373,319 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         }
         const __half2 major = __floats2half2_rn(vlo, vhi);
         const float2 mf = __half22float2(major);
-        const __half2 minor = __floats2half2_rn(vlo - mf.x, vhi - mf.y);
         qpa[i] = h2_as_u32(major);
-        qpb[i] = h2_as_u32(minor);
+        qpb[i] = h2_as_u32(__floats2half2_rn(vlo - mf.x, vhi - mf.y));
     }
     __syncthreads();
-    if (!wait_staged(bar, a.ws)) return;
 
-    // ---------------- scores
+    const int part = g & 1;                 // B column g = 2 * head + part
     const int kc_bytes = lo.kc, vc_bytes = lo.vc;
     const int rowbytes = D * BITS / 8;
-    const int tiles_per_warp = CH / 64;
-    const int tile_lo = warp * tiles_per_warp;
-    int tile_hi = tile_lo + tiles_per_warp;
-    if (tile_hi > ntok / 16) tile_hi = ntok / 16;
-    uint32_t bq[NT][NPAIR];
-    float cst[NT];
-    float hmax[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) hmax[nt] = -INFINITY;
-    int cur = -1;
-    for (int mt = tile_lo; mt < tile_hi; ++mt) {
-        const int tok0 = mt * 16, grp = tok0 / G;
-        const uint8_t* rec = data + (int64_t)grp * lo.rec;
-        if (grp != cur) {
-            cur = grp;
-            const __half* sK = reinterpret_cast<const __half*>(rec + kc_bytes + vc_bytes);
-            const __half* zK = sK + D;
-            uint32_t sreg[D / 8];
-            load_words<D / 8>(reinterpret_cast<const uint8_t*>(sK + tig * (D / 4)), sreg);
-            const int part = g & 1;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int hh = 4 * nt + (g >> 1);
-                const uint32_t* pa = qpa + (hh * 4 + tig) * NPAIR;
-                const uint32_t* pb = qpb + (hh * 4 + tig) * NPAIR;
-#pragma unroll
-                for (int m = 0; m < NPAIR; ++m) {
-                    const int wi = m / HPW, j = m % HPW;
-                    const int lo_l = wi * CPW + j, hi_l = lo_l + HPW;
-                    const __half2 s2 = u32_as_h2(prmt(sreg[lo_l / 2], sreg[hi_l / 2], (j & 1) ? 0x7632u : 0x5410u));
-                    const __half2 qa = u32_as_h2(pa[m]), qb = u32_as_h2(pb[m]);
-                    const __half2 major = __hmul2(s2, qa);
-                    __half2 minor = __hfma2(s2, qa, __hneg2(major));
-                    minor = __hfma2(s2, qb, minor);
-                    bq[nt][m] = part ? h2_as_u32(minor) : h2_as_u32(major);
-                }
-                // offset term sum_c qs[hh][c] * zero[c]; the two threads of a (major, minor)
-                // pair split the thread's channel block in halves
-                float zsum = 0.0f;
-                if (hh < gqa) {
-                    const int c0 = tig * (D / 4) + part * (D / 8);
-#pragma unroll 8
-                    for (int c = 0; c < D / 8; ++c) zsum = fmaf(qs[hh * D + c0 + c], __half2float(zK[c0 + c]), zsum);
-                }
-                zsum += __shfl_xor_sync(0xffffffffu, zsum, 4);
-                zsum += __shfl_xor_sync(0xffffffffu, zsum, 1);
-                zsum += __shfl_xor_sync(0xffffffffu, zsum, 2);
-                cst[nt] = __shfl_sync(0xffffffffu, zsum, 8 * tig);
-            }
-        }
-        uint32_t wa[ROWW], wb[ROWW];
-        const int ti = tok0 % G + g;
-        load_words<ROWW>(rec + ti * rowbytes + tig * (ROWW * 4), wa);
-        load_words<ROWW>(rec + (ti + 8) * rowbytes + tig * (ROWW * 4), wb);
-        float acc[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-#pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks) {
-            const int m0 = 2 * ks, m1 = 2 * ks + 1;
-            uint32_t af[4];
-            af[0] = code_pair<BITS>(wa[m0 / HPW], BITS * (m0 % HPW));
-            af[1] = code_pair<BITS>(wb[m0 / HPW], BITS * (m0 % HPW));
-            af[2] = code_pair<BITS>(wa[m1 / HPW], BITS * (m1 % HPW));
-            af[3] = code_pair<BITS>(wb[m1 / HPW], BITS * (m1 % HPW));
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_16816(acc[nt], af, bq[nt][m0], bq[nt][m1]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int head = 4 * nt + tig;
-            if (head < gqa) {
-                const float s0 = fmaf(acc[nt][0] + acc[nt][1], qup, cst[nt]);
-                const float s1 = fmaf(acc[nt][2] + acc[nt][3], qup, cst[nt]);
-                sc[head * CH + tok0 + g] = s0;
-                sc[head * CH + tok0 + g + 8] = s1;
-                hmax[nt] = fmaxf(hmax[nt], fmaxf(s0, s1));
-            }
-        }
-    }
+    // token order of the score tile rows: lane (g, tig) scores tokens rho0 = rho(g) and
+    // rho1 = rho(g + 8) of each 16-token tile, chosen so that the value fragment of lane
+    // (g', t') needs the pairs held by lanes (2t', h') and (2t' + 1, h') (h' = g' / 2)
+    const int rt = g >> 1, re = g & 1;
+    const int rho0 = (2 * rt) / HW * TPW + (2 * rt) % HW + re;
+    const int rho1 = rho0 + HW;
+    // this lane's value-fragment tokens of a tile (k slots 2t, 2t+1, 2t+8, 2t+9)
+    const int vwi = (2 * tig) / HW, vj0 = (2 * tig) % HW;
+    const int tA = vwi * TPW + vj0, tB = tA + HW, tC = tA + 1, tD = tB + 1;
+    const int src1 = (2 * tig) * 4 + (g >> 1), src2 = (2 * tig + 1) * 4 + (g >> 1);
+    // value groups are powers of two (multiples of 16 dividing head_dim): tile q of 16
+    // channels lies in value group q >> gvs
+    const int gvs = __ffs(lo.Gv) - 5;
+    const int wpc = G * BITS / 32;          // 32-bit words of one channel's value codes
+
+    float mrun[NT], lrun[NT];
+    float oacc[MTV][NT][4];
+    float ozacc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        float m = hmax[nt];
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-        if (g == 0) red[warp * 32 + 4 * nt + tig] = m;
+        mrun[nt] = -INFINITY;
+        lrun[nt] = 0.0f;
+        ozacc[nt][0] = ozacc[nt][1] = ozacc[nt][2] = ozacc[nt][3] = 0.0f;
+#pragma unroll
+        for (int mt = 0; mt < MTV; ++mt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.0f;
     }
-    __syncthreads();
-    chunk_softmax(lo, sc, ntok, CH, red, hstat);
-
-    // ---------------- values
-    const int wi = (2 * tig) / HW, j0 = (2 * tig) % HW;
-    const int tA = wi * TPW + j0, tB = tA + HW, tC = tA + 1, tD = tB + 1;
-    const int cw0 = warp * (D / 4);
-    float oacc[MT][NT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.0f;
-    const int part = g & 1;
-    for (int ks = 0; ks < ntok / 16; ++ks) {
-        const int tokbase = ks * 16, grp = tokbase / G, tb = tokbase % G;
-        const uint8_t* rec = data + (int64_t)grp * lo.rec;
-        const uint32_t* vcw = reinterpret_cast<const uint32_t*>(rec + kc_bytes);
-        const __half* sV = reinterpret_cast<const __half*>(rec + kc_bytes + vc_bytes + lo.kp);
-        // p of this thread's four tokens, split into fp16 major + minor parts
-        __half2 pa01[NT], pb01[NT], pa23[NT], pb23[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int hp = 4 * nt + (g >> 1);
-            float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
-            if (hp < gqa) {
-                const float* ps = sc + hp * CH + tokbase;
-                p0 = ps[tA]; p1 = ps[tB]; p2 = ps[tC]; p3 = ps[tD];
-            }
-            pa01[nt] = __floats2half2_rn(p0, p1);
-            pa23[nt] = __floats2half2_rn(p2, p3);
-            const float2 f01 = __half22float2(pa01[nt]), f23 = __half22float2(pa23[nt]);
-            pb01[nt] = __floats2half2_rn(p0 - f01.x, p1 - f01.y);
-            pb23[nt] = __floats2half2_rn(p2 - f23.x, p3 - f23.y);
+    bool live = true;
+    for (int j = 0; j < nch; ++j) {
+        bool ok = mbar_wait_bounded(bars + (j % nstage), (j / nstage) & 1, kWaitLimit);
+        ok = __syncthreads_and(ok);
+        if (!ok) {
+            if (tid == 0) atomicOr(reinterpret_cast<uint32_t*>(a.ws), KVQ_STATUS_TIMEOUT);
+            mbar_wait_bounded(bars + (j % nstage), (j / nstage) & 1, kWaitLimit);
+            live = false;
+            break;
         }
-        uint32_t bp[NT][2];
-        int gv_cur = -1;
+        const int64_t c0 = t0 + (int64_t)j * CH;
+        const int ctok = static_cast<int>((t1 - c0) < CH ? (t1 - c0) : CH);
+        const int wtok = ctok - warp * W < 0 ? 0 : (ctok - warp * W > W ? W : ctok - warp * W);   // whole groups
+        const uint8_t* stage = smem + so.data + (j % nstage) * stage_bytes + (int64_t)warp * (W / G) * lo.rec;
+        if (wtok > 0) {
+            const int ntl = wtok / 16;
+            // offset term of every group of the warp: cst[group][head] = sum_c q_c zero_c,
+            // as one small tensor-core product (rows = groups, k = channels in pair order)
+            float cstf[NT][4];
+            {
+                const int ngrp = wtok / G;
+                uint32_t zreg[D / 8];
+                if (g < ngrp) {
+                    const __half* zK = reinterpret_cast<const __half*>(stage + (int64_t)g * lo.rec + kc_bytes + vc_bytes) + D;
+                    load_words<D / 8>(reinterpret_cast<const uint8_t*>(zK + tig * (D / 4)), zreg);
+                } else {
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            const int c0 = cw0 + mt * 16 + g;
-            const int gv = (cw0 + mt * 16) / lo.Gv;
-            if (gv != gv_cur) {
-                gv_cur = gv;
-                const __half2 s01 = __halves2half2(sV[(tb + tA) * lo.NGv + gv], sV[(tb + tB) * lo.NGv + gv]);
-                const __half2 s23 = __halves2half2(sV[(tb + tC) * lo.NGv + gv], sV[(tb + tD) * lo.NGv + gv]);
+                    for (int i = 0; i < D / 8; ++i) zreg[i] = 0u;
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const __half2 M01 = __hmul2(s01, pa01[nt]);
-                    __half2 m01 = __hfma2(s01, pa01[nt], __hneg2(M01));
-                    m01 = __hfma2(s01, pb01[nt], m01);
-                    const __half2 M23 = __hmul2(s23, pa23[nt]);
-                    __half2 m23 = __hfma2(s23, pa23[nt], __hneg2(M23));
-                    m23 = __hfma2(s23, pb23[nt], m23);
-                    bp[nt][0] = part ? h2_as_u32(m01) : h2_as_u32(M01);
-                    bp[nt][1] = part ? h2_as_u32(m23) : h2_as_u32(M23);
+                    cstf[nt][0] = cstf[nt][1] = cstf[nt][2] = cstf[nt][3] = 0.0f;
+                    const int hh = 4 * nt + (g >> 1);
+                    uint32_t qt[NPAIR];
+                    load_words<NPAIR>(reinterpret_cast<const uint8_t*>((part ? qpb : qpa) + (hh * 4 + tig) * NPAIR), qt);
+#pragma unroll
+                    for (int ks = 0; ks < KSTEPS; ++ks) {
+                        uint32_t af[4];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int m = 2 * ks + e, wi = m / HPW, jj = m % HPW;
+                            const int lo_l = wi * CPW + jj, hi_l = lo_l + HPW;
+                            af[2 * e] = prmt(zreg[lo_l / 2], zreg[hi_l / 2], (jj & 1) ? 0x7632u : 0x5410u);
+                            af[2 * e + 1] = 0u;
+                        }
+                        mma_16816(cstf[nt], af, qt[2 * ks], qt[2 * ks + 1]);
+                    }
                 }
             }
-            const uint32_t w0 = vcw[(c0 * G + tb) * BITS / 32 + wi];
-            const uint32_t w1 = vcw[((c0 + 8) * G + tb) * BITS / 32 + wi];
-            uint32_t af[4];
-            af[0] = code_pair<BITS>(w0, BITS * j0);
-            af[1] = code_pair<BITS>(w1, BITS * j0);
-            af[2] = code_pair<BITS>(w0, BITS * (j0 + 1));
-            af[3] = code_pair<BITS>(w1, BITS * (j0 + 1));
+            // ---- pass 1: scores of the warp's tiles, kept in registers
+            float sc2[MAXT][NT][2];
+            float cmax[NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_16816(oacc[mt][nt], af, bp[nt][0], bp[nt][1]);
-        }
-    }
-    // offset term of the values: oz[head][gv] = sum_t p[head][t] * zero[t][gv]
-    float oz[MT][NT];
+            for (int nt = 0; nt < NT; ++nt) cmax[nt] = -INFINITY;
+            {
+                uint32_t bq[NT][NPAIR];
+                float cst[NT];
+                int grp = 0, ti = 0;            // group and offset of the tile in the group
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-        const int gv = (cw0 + mt * 16) / lo.Gv;
-        float zs[8];
+                for (int i = 0; i < MAXT; ++i) {
+                    if (i >= ntl) break;
+                    if (i > 0) {
+                        ti += 16;
+                        if (ti == G) { ti = 0; ++grp; }
+                    }
+                    const uint8_t* rec = stage + (int64_t)grp * lo.rec;
+                    if (ti == 0) {
+                        // key-score operand of the group: (q * key scale) as fp16 major + minor
+                        const __half* sK = reinterpret_cast<const __half*>(rec + kc_bytes + vc_bytes);
+                        uint32_t sreg[D / 8];
+                        load_words<D / 8>(reinterpret_cast<const uint8_t*>(sK + tig * (D / 4)), sreg);
 #pragma unroll
-        for (int hh = 0; hh < 8; ++hh) zs[hh] = 0.0f;
-        for (int t = lane; t < ntok; t += 32) {
-            const uint8_t* rec = data + (int64_t)(t / G) * lo.rec;
-            const __half* zV = reinterpret_cast<const __half*>(rec + kc_bytes + vc_bytes + lo.kp) + G * lo.NGv;
-            const float z = __half2float(zV[(t % G) * lo.NGv + gv]);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const int hh = 4 * nt + (g >> 1);
+                            uint32_t qa[NPAIR], qb[NPAIR];
+                            load_words<NPAIR>(reinterpret_cast<const uint8_t*>(qpa + (hh * 4 + tig) * NPAIR), qa);
+                            load_words<NPAIR>(reinterpret_cast<const uint8_t*>(qpb + (hh * 4 + tig) * NPAIR), qb);
 #pragma unroll
-            for (int hh = 0; hh < 8; ++hh)
-                if (hh < gqa) zs[hh] = fmaf(sc[hh * CH + t], z, zs[hh]);
-        }
+                            for (int m = 0; m < NPAIR; ++m) {
+                                const int wi = m / HPW, jj = m % HPW;
+                                const int lo_l = wi * CPW + jj, hi_l = lo_l + HPW;
+                                const __half2 s2 = u32_as_h2(prmt(sreg[lo_l / 2], sreg[hi_l / 2], (jj & 1) ? 0x7632u : 0x5410u));
+                                const __half2 major = __hmul2(s2, u32_as_h2(qa[m]));
+                                __half2 minor = __hfma2(s2, u32_as_h2(qa[m]), __hneg2(major));
+                                minor = __hfma2(s2, u32_as_h2(qb[m]), minor);
+                                bq[nt][m] = part ? h2_as_u32(minor) : h2_as_u32(major);
+                            }
+                            const float c = (grp < 8 ? cstf[nt][0] + cstf[nt][1] : cstf[nt][2] + cstf[nt][3]);
+                            cst[nt] = __shfl_sync(0xffffffffu, c, (grp & 7) * 4 + tig) * qup;
+                        }
+                    }
+                    uint32_t wa[ROWW], wb[ROWW];
+                    load_words<ROWW>(rec + (ti + rho0) * rowbytes + tig * (ROWW * 4), wa);
+                    load_words<ROWW>(rec + (ti + rho1) * rowbytes + tig * (ROWW * 4), wb);
+                    float acc[NT][4];
 #pragma unroll
-        for (int hh = 0; hh < 8; ++hh)
-            if (hh < gqa) zs[hh] = warp_sum(zs[hh]);
+                    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float v = 0.0f;
+                    for (int ks = 0; ks < KSTEPS; ++ks) {
+                        const int m0 = 2 * ks, m1 = 2 * ks + 1;
+                        uint32_t af[4];
+                        af[0] = code_pair<BITS>(wa[m0 / HPW], BITS * (m0 % HPW));
+                        af[1] = code_pair<BITS>(wb[m0 / HPW], BITS * (m0 % HPW));
+                        af[2] = code_pair<BITS>(wa[m1 / HPW], BITS * (m1 % HPW));
+                        af[3] = code_pair<BITS>(wb[m1 / HPW], BITS * (m1 % HPW));
 #pragma unroll
-            for (int hh = 0; hh < 8; ++hh)
-                if (hh == 4 * nt + tig) v = zs[hh];
-            oz[mt][nt] = v;
-        }
-    }
-    float* wso = reinterpret_cast<float*>(a.ws + a.plan.ws_o_off);
+                        for (int nt = 0; nt < NT; ++nt) mma_16816(acc[nt], af, bq[nt][m0], bq[nt][m1]);
+                    }
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+                    for (int nt = 0; nt < NT; ++nt) {
+                        sc2[i][nt][0] = fmaf(acc[nt][0] + acc[nt][1], qup, cst[nt]);
+                        sc2[i][nt][1] = fmaf(acc[nt][2] + acc[nt][3], qup, cst[nt]);
+                        cmax[nt] = fmaxf(cmax[nt], fmaxf(sc2[i][nt][0], sc2[i][nt][1]));
+                    }
+                }
+            }
+            // running maximum per head (lanes of a head share tig); rescale what the warp
+            // accumulated over earlier chunks when it grows
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int head = 4 * nt + tig;
-            if (head < gqa) {
-                const int c0 = cw0 + mt * 16 + g;
-                float* o = wso + slot_index(a, b, h, item, head) * D;
-                o[c0] = (oacc[mt][nt][0] + oacc[mt][nt][1]) + oz[mt][nt];
-                o[c0 + 8] = (oacc[mt][nt][2] + oacc[mt][nt][3]) + oz[mt][nt];
+            for (int nt = 0; nt < NT; ++nt) {
+                float m = cmax[nt];
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                const float mnew = fmaxf(mrun[nt], m);
+                if (mnew > mrun[nt] && mrun[nt] > -INFINITY) {
+                    const float alpha = fast_exp2(mrun[nt] - mnew);
+                    lrun[nt] *= alpha;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) ozacc[nt][e] *= alpha;
+#pragma unroll
+                    for (int mt = 0; mt < MTV; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) oacc[mt][nt][e] *= alpha;
+                }
+                mrun[nt] = mnew;
+            }
+            // ---- pass 2: p = 2^(s - max) and the value contraction, tile by tile
+            int grp = 0, ti = 0;
+#pragma unroll
+            for (int i = 0; i < MAXT; ++i) {
+                if (i >= ntl) break;
+                if (i > 0) {
+                    ti += 16;
+                    if (ti == G) { ti = 0; ++grp; }
+                }
+                const uint8_t* rec = stage + (int64_t)grp * lo.rec;
+                uint32_t pa1[NT], pb1[NT], pa2[NT], pb2[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float p0 = fast_exp2(sc2[i][nt][0] - mrun[nt]);
+                    const float p1 = fast_exp2(sc2[i][nt][1] - mrun[nt]);
+                    lrun[nt] += p0 + p1;
+                    // p as fp16 major + minor, moved to the lanes of the value fragment
+                    const __half2 pa = __floats2half2_rn(p0, p1);
+                    const float2 pf = __half22float2(pa);
+                    const __half2 pb = __floats2half2_rn(p0 - pf.x, p1 - pf.y);
+                    const uint32_t ua = h2_as_u32(pa), ub = h2_as_u32(pb);
+                    uint32_t x1 = __shfl_sync(0xffffffffu, ua, src1);
+                    uint32_t y1 = __shfl_sync(0xffffffffu, ub, src1);
+                    uint32_t x2 = __shfl_sync(0xffffffffu, ua, src2);
+                    uint32_t y2 = __shfl_sync(0xffffffffu, ub, src2);
+                    if (4 * nt + (g >> 1) >= gqa) x1 = y1 = x2 = y2 = 0u;
+                    pa1[nt] = x1; pb1[nt] = y1; pa2[nt] = x2; pb2[nt] = y2;
+                }
+                // values: O[c][col] += sum_t code[t][c] * (p_t * scale[t][gv(c)]); the offset
+                // term OZ[gv][col] += sum_t zero[t][gv] * p_t
+                const uint8_t* vpar = rec + kc_bytes + vc_bytes + lo.kp;
+                const uint32_t* vcw = reinterpret_cast<const uint32_t*>(rec + kc_bytes);
+                const uint32_t* pA = reinterpret_cast<const uint32_t*>(vpar + 4 * (ti + tA) * NGv);
+                const uint32_t* pB = reinterpret_cast<const uint32_t*>(vpar + 4 * (ti + tB) * NGv);
+                const uint32_t* pC = reinterpret_cast<const uint32_t*>(vpar + 4 * (ti + tC) * NGv);
+                const uint32_t* pD = reinterpret_cast<const uint32_t*>(vpar + 4 * (ti + tD) * NGv);
+                uint32_t zA = 0u, zC = 0u, zA8 = 0u, zC8 = 0u;   // zero pairs of value groups g, g + 8
+                if (g < NGv) { zA = prmt(pA[g], pB[g], 0x7632u); zC = prmt(pC[g], pD[g], 0x7632u); }
+                if (g + 8 < NGv) { zA8 = prmt(pA[g + 8], pB[g + 8], 0x7632u); zC8 = prmt(pC[g + 8], pD[g + 8], 0x7632u); }
+                uint32_t bp[NT][2];
+                const uint32_t* vct = vcw + (ti * BITS / 32 + vwi);
+#pragma unroll
+                for (int q = 0; q < MTV; ++q) {
+                    const int gv = q >> gvs;
+                    if (q == 0 || gv != ((q - 1) >> gvs)) {
+                        const __half2 s01 = u32_as_h2(prmt(pA[gv], pB[gv], 0x5410u));
+                        const __half2 s23 = u32_as_h2(prmt(pC[gv], pD[gv], 0x5410u));
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const __half2 M01 = __hmul2(s01, u32_as_h2(pa1[nt]));
+                            __half2 m01 = __hfma2(s01, u32_as_h2(pa1[nt]), __hneg2(M01));
+                            m01 = __hfma2(s01, u32_as_h2(pb1[nt]), m01);
+                            const __half2 M23 = __hmul2(s23, u32_as_h2(pa2[nt]));
+                            __half2 m23 = __hfma2(s23, u32_as_h2(pa2[nt]), __hneg2(M23));
+                            m23 = __hfma2(s23, u32_as_h2(pb2[nt]), m23);
+                            bp[nt][0] = part ? h2_as_u32(m01) : h2_as_u32(M01);
+                            bp[nt][1] = part ? h2_as_u32(m23) : h2_as_u32(M23);
+                        }
+                    }
+                    const int c0 = 16 * q + g;
+                    const uint32_t w0 = vct[c0 * wpc];
+                    const uint32_t w1 = vct[(c0 + 8) * wpc];
+                    uint32_t af[4];
+                    af[0] = code_pair<BITS>(w0, BITS * vj0);
+                    af[1] = code_pair<BITS>(w1, BITS * vj0);
+                    af[2] = code_pair<BITS>(w0, BITS * (vj0 + 1));
+                    af[3] = code_pair<BITS>(w1, BITS * (vj0 + 1));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma_16816(oacc[q][nt], af, bp[nt][0], bp[nt][1]);
+                }
+                {
+                    uint32_t af[4] = {zA, zA8, zC, zC8};
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_16816(ozacc[nt], af, part ? pb1[nt] : pa1[nt], part ? pb2[nt] : pa2[nt]);
+                }
             }
         }
+        __syncthreads();            // every warp is done with this stage
+        if (tid == 0 && j + nstage < nch) issue(j + nstage);
+    }
+    // ---- warp partial: reduce l over the lanes of a head, add the value offset term,
+    // combine the 4 warps in shared memory
+    float* cw = comb + (int64_t)warp * gqa * (D + 2);
+    const bool wlive = live && mrun[0] > -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int head = 4 * nt + tig;
+        float l = lrun[nt];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        const float oz01 = ozacc[nt][0] + ozacc[nt][1], oz23 = ozacc[nt][2] + ozacc[nt][3];
+#pragma unroll
+        for (int mt = 0; mt < MTV; ++mt) {
+            const int gv = mt >> gvs;
+            const float zsrc = gv < 8 ? oz01 : oz23;
+            const float oz = __shfl_sync(0xffffffffu, zsrc, (gv & 7) * 4 + tig);
+            if (head < gqa && wlive) {
+                const int c0 = 16 * mt + g;
+                cw[head * (D + 2) + c0] = (oacc[mt][nt][0] + oacc[mt][nt][1]) + oz;
+                cw[head * (D + 2) + c0 + 8] = (oacc[mt][nt][2] + oacc[mt][nt][3]) + oz;
+            }
+        }
+        if (g == 0 && head < gqa) {
+            cw[head * (D + 2) + D] = wlive ? mrun[nt] : -INFINITY;
+            cw[head * (D + 2) + D + 1] = wlive ? l : 0.0f;
+        }
+    }
+    __syncthreads();
+    // per (warp, head) weight 2^(m_w - M) and the combined max and sum, once per head
+    float* wgt = red;   // [head][4 warps] (red is free again)
     if (tid < gqa) {
+        float M = -INFINITY, l = 0.0f;
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, comb[(w * gqa + tid) * (D + 2) + D]);
+        for (int w = 0; w < 4; ++w) {
+            const float* cwp = comb + (w * gqa + tid) * (D + 2);
+            const float wt = cwp[D + 1] > 0.0f ? fast_exp2(cwp[D] - M) : 0.0f;
+            wgt[tid * 4 + w] = wt;
+            l = fmaf(cwp[D + 1], wt, l);
+        }
         float* ml = reinterpret_cast<float*>(a.ws + a.plan.ws_ml_off) + 2 * slot_index(a, b, h, item, tid);
-        ml[0] = hstat[tid];
-        ml[1] = hstat[32 + tid];
+        ml[0] = M;
+        ml[1] = l;
+    }
+    __syncthreads();
+    float* wso = reinterpret_cast<float*>(a.ws + a.plan.ws_o_off);
+    for (int i = tid; i < gqa * D; i += blockDim.x) {
+        const int head = i / D, c = i % D;
+        float o = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float wt = wgt[head * 4 + w];
+            if (wt != 0.0f) o = fmaf(comb[(w * gqa + head) * (D + 2) + c], wt, o);
+        }
+        wso[slot_index(a, b, h, item, head) * D + c] = o;
     }
 }
 
 // One block per (item, kv head, sequence).  BITS == 0: no packed path (INT8 / FP8).
 template <int D, int BITS, int NT>
-__global__ void __launch_bounds__(kDecodeThreads) k_decode(DecodeArgs a) {
+__global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2) k_decode(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int item = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int32_t* st = state_ptr(a.lo, a.cache, a.layer, b);

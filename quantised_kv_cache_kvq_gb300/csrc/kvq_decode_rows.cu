@@ -7,11 +7,14 @@ namespace {
 
 // Combine the chunks of one (sequence, query head): with chunk i holding m_i (max score,
 // base 2), l_i = sum 2^(s - m_i) and o_i = sum 2^(s - m_i) v, the output is
-// sum_i o_i 2^(m_i - M) / sum_i l_i 2^(m_i - M), M = max_i m_i.
+// sum_i o_i 2^(m_i - M) / sum_i l_i 2^(m_i - M), M = max_i m_i.  Warps take chunks in turn,
+// lanes hold D/32 channels each, four chunks in flight per warp.
+template <int D>
 __global__ void __launch_bounds__(128) k_merge(DecodeArgs a) {
-    extern __shared__ float wts[];
+    constexpr int CPL = D / 32;
     __shared__ float red[4];
-    __shared__ float bc;
+    __shared__ float part_o[4][D];
+    __shared__ float part_l[4];
     const Layout& lo = a.lo;
     const int hq = blockIdx.x, b = blockIdx.y;
     const int h = hq / lo.gqa, head = hq % lo.gqa;
@@ -21,41 +24,55 @@ __global__ void __launch_bounds__(128) k_merge(DecodeArgs a) {
     const int S = a.plan.S;
     const float* ml = reinterpret_cast<const float*>(a.ws + a.plan.ws_ml_off);
     const float* o = reinterpret_cast<const float*>(a.ws + a.plan.ws_o_off);
-    auto slot = [&](int item) { return (((int64_t)b * lo.H + h) * S + item) * lo.gqa + head; };
+    const int64_t slot0 = (((int64_t)b * lo.H + h) * S) * lo.gqa + head;   // + item * gqa
     float mx = -INFINITY;
     for (int it = tid; it < S; it += blockDim.x) {
         const ItemRange r = item_range(lo, a.plan, it, n, qn);
-        if (r.t0 < r.t1) mx = fmaxf(mx, ml[2 * slot(it)]);
+        if (r.t0 < r.t1) mx = fmaxf(mx, ml[2 * (slot0 + (int64_t)it * lo.gqa)]);
     }
     mx = warp_max(mx);
     if (lane == 0) red[warp] = mx;
     __syncthreads();
-    if (tid == 0) bc = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    __syncthreads();
-    const float M = bc;
+    const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    float acc[CPL];
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) acc[e] = 0.0f;
     float l = 0.0f;
-    for (int it = tid; it < S; it += blockDim.x) {
-        const ItemRange r = item_range(lo, a.plan, it, n, qn);
-        float w = 0.0f;
-        if (r.t0 < r.t1) {
-            w = exp2f(ml[2 * slot(it)] - M);
-            l += ml[2 * slot(it) + 1] * w;
+    for (int it0 = warp; it0 < S; it0 += 16) {
+        float w4[4];
+        float v4[4][CPL];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int it = it0 + 4 * k;
+            w4[k] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) v4[k][e] = 0.0f;
+            if (it < S) {
+                const ItemRange r = item_range(lo, a.plan, it, n, qn);
+                if (r.t0 < r.t1) {
+                    const int64_t sl = slot0 + (int64_t)it * lo.gqa;
+                    const float2 mlv = *reinterpret_cast<const float2*>(ml + 2 * sl);
+                    w4[k] = fast_exp2(mlv.x - M);
+                    if (lane == 0) l = fmaf(mlv.y, w4[k], l);
+#pragma unroll
+                    for (int e = 0; e < CPL; ++e) v4[k][e] = o[sl * D + lane + 32 * e];
+                }
+            }
         }
-        wts[it] = w;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) acc[e] = fmaf(v4[k][e], w4[k], acc[e]);
     }
-    l = warp_sum(l);
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) part_o[warp][lane + 32 * e] = acc[e];
+    if (lane == 0) part_l[warp] = l;
     __syncthreads();
-    if (lane == 0) red[warp] = l;
-    __syncthreads();
-    const float L = red[0] + red[1] + red[2] + red[3];
-    float* out = a.out + ((int64_t)b * lo.Hq + hq) * lo.D;
-    for (int d = tid; d < lo.D; d += blockDim.x) {
-        float acc = 0.0f;
-        for (int it = 0; it < S; ++it) {
-            const float w = wts[it];
-            if (w != 0.0f) acc = fmaf(o[slot(it) * lo.D + d], w, acc);
-        }
-        out[d] = L > 0.0f ? acc / L : 0.0f;
+    const float L = part_l[0] + part_l[1] + part_l[2] + part_l[3];
+    float* out = a.out + ((int64_t)b * lo.Hq + hq) * D;
+    for (int d = tid; d < D; d += blockDim.x) {
+        const float v = part_o[0][d] + part_o[1][d] + part_o[2][d] + part_o[3][d];
+        out[d] = L > 0.0f ? v / L : 0.0f;
     }
 }
 
@@ -91,12 +108,13 @@ int launch_decode(const Layout& lo, const DecodePlan& plan, const uint8_t* cache
         rc = launch_decode_rows(a, stream);
     }
     if (rc != KVQ_OK) return rc;
-    const size_t msmem = static_cast<size_t>(plan.S) * sizeof(float);
-    if (msmem > 48 * 1024 &&
-        cudaFuncSetAttribute(k_merge, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(msmem)) !=
-            cudaSuccess)
-        return KVQ_ERR_CUDA;
-    k_merge<<<dim3(lo.Hq, lo.B), 128, msmem, stream>>>(a);
+    const dim3 mgrid(lo.Hq, lo.B);
+    switch (lo.D) {
+        case 32: k_merge<32><<<mgrid, 128, 0, stream>>>(a); break;
+        case 64: k_merge<64><<<mgrid, 128, 0, stream>>>(a); break;
+        case 128: k_merge<128><<<mgrid, 128, 0, stream>>>(a); break;
+        default: k_merge<256><<<mgrid, 128, 0, stream>>>(a); break;
+    }
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

@@ -3,8 +3,9 @@
 //
 // Cache image (little-endian, every region starts on a 256-byte boundary):
 //   header   256 B; u32 status word at byte 0.
-//   state    int32 pairs (n, qn) per (layer, sequence): n tokens cached, the first qn of
-//            them in packed groups (KIVI) -- qn == n for INT8 and FP8.
+//   state    16 B per (layer, sequence): int32 n tokens cached, int32 qn of them in packed
+//            groups (KIVI; qn == n for INT8 and FP8), an int32 arrival counter of the
+//            one-kernel append (zero whenever no call runs) and a reserved zero word.
 //   KIVI     "group records", one per (layer, sequence, kv head, group slot), NG =
 //            (max_tokens - R) / G slots per (layer, sequence, kv head).  A record holds
 //            everything a decode block needs for G tokens, so a run of groups is one
@@ -12,7 +13,8 @@
 //              K codes  G*D*b/8 B, token-major: (token t, channel c) at bit (t*D + c)*b
 //              V codes  D*G*b/8 B, channel-major: (channel c, token t) at bit (c*G + t)*b
 //              K params 4*D B: fp16 scale[D] then fp16 zero[D] (per channel, "min")
-//              V params 4*G*(D/Gv) B: fp16 scale[G][D/Gv] then fp16 zero[G][D/Gv]
+//              V params 4*G*(D/Gv) B: for token t and value group j, fp16 scale then fp16
+//                       zero at byte 4*(t*(D/Gv) + j)
 //            then the bf16 window ("ring"): per (layer, sequence, kv head) C = R + G slots
 //            of [K row bf16[D], V row bf16[D]]; token t (qn <= t < n) lives in slot t % C.
 //   INT8     per (layer, sequence, kv head), T16 = max_tokens rounded up to 16:
@@ -43,10 +45,12 @@ inline int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 
 // How one decode step is split: every (sequence, kv head) "unit" gets NRC row chunks of
 // CHR tokens (the bf16 window for KIVI, all tokens for INT8/FP8) and NQ packed chunks of
-// CH tokens (KIVI groups), S = NRC + NQ work items in all.  Each item leaves a partial
-// softmax result (m, l, o[D]) per query head in the workspace.
+// CH tokens (KIVI groups), S = NRC + NQ work items in all.  A packed chunk is split among
+// the block's 4 warps, W = CH / 4 tokens (whole groups) each; a packed item covers CPI
+// consecutive chunks, staged through NSTAGE shared-memory buffers.  Each item leaves a
+// partial softmax result (m, l, o[D]) per query head in the workspace.
 struct DecodePlan {
-    int CH, NQ, CHR, NRC, S, NT;
+    int CH, W, CPI, NSTAGE, NQ, CHR, NRC, S, NT;
     int64_t ws_o_off, ws_ml_off, ws_total;
     int64_t smem;
 };
@@ -58,19 +62,24 @@ struct SmemOffsets {
 __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const DecodePlan& p) {
     SmemOffsets o;
     int64_t off = 0;
-    o.bar = off;   off += 64;
+    o.bar = off;   off += 64;                         // one mbarrier per warp
     o.red = off;   off += 4 * 32 * 4;                 // [warp][32] floats
     o.hstat = off; off += 2 * 32 * 4;                 // per-head max and sum
     o.qs = off;    off += (int64_t)lo.gqa * lo.D * 4; // scaled query, fp32
     o.qpa = off;   off += (int64_t)4 * p.NT * 4 * (lo.D / 8) * 4;
     o.qpb = off;   off += (int64_t)4 * p.NT * 4 * (lo.D / 8) * 4;
-    o.sc = off;    off += (int64_t)lo.gqa * (p.CH > p.CHR ? p.CH : p.CHR) * 4;
+    o.sc = off;
+    {
+        const int64_t rows_sc = (int64_t)lo.gqa * p.CHR;                // row path scores
+        const int64_t comb = (int64_t)4 * lo.gqa * (lo.D + 2);           // per-warp partials
+        off += 4 * (rows_sc > comb ? rows_sc : comb);
+    }
     off = (off + 127) / 128 * 128;
     o.data = off;
     int64_t rows = 0, packed = 0;
     if (lo.scheme == KVQ_SCHEME_KIVI) {
         rows = (int64_t)p.CHR * 4 * lo.D;
-        packed = (int64_t)(p.CH / lo.G) * lo.rec;
+        packed = (int64_t)p.NSTAGE * (p.CH / lo.G) * lo.rec;
     } else if (lo.scheme == KVQ_SCHEME_INT8) {
         rows = (int64_t)p.CHR * (2 * lo.D + 8);
     } else {
@@ -87,11 +96,11 @@ int make_layout(const kvq_config* cfg, int64_t max_tokens, Layout* out);
 
 // ---------------------------------------------------------------------------- device helpers
 __device__ __forceinline__ int32_t* state_ptr(const Layout& lo, uint8_t* cache, int l, int b) {
-    return reinterpret_cast<int32_t*>(cache + lo.state_off) + 2 * ((int64_t)l * lo.B + b);
+    return reinterpret_cast<int32_t*>(cache + lo.state_off) + 4 * ((int64_t)l * lo.B + b);
 }
 __device__ __forceinline__ const int32_t* state_ptr(const Layout& lo, const uint8_t* cache, int l,
                                                     int b) {
-    return reinterpret_cast<const int32_t*>(cache + lo.state_off) + 2 * ((int64_t)l * lo.B + b);
+    return reinterpret_cast<const int32_t*>(cache + lo.state_off) + 4 * ((int64_t)l * lo.B + b);
 }
 __device__ __forceinline__ int64_t unit_index(const Layout& lo, int l, int b, int h) {
     return ((int64_t)l * lo.B + b) * lo.H + h;

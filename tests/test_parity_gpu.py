@@ -91,7 +91,10 @@ def test_kivi_no_autoflush_and_explicit_flush():
             p.assert_same_image()
             out, ref = p.decode(0, p.rand_q(g))
             assert_close(out, ref, what="no-autoflush step %d" % step)
-    assert p.status() == 0
+    # flushing only every third step lets the R + G window overflow now and then; the
+    # skipped appends are flagged identically on both sides (the status word is part of
+    # the compared image)
+    assert p.status() == p.img.status == 2
 
 
 def test_kivi_ring_full_and_capacity_status():
