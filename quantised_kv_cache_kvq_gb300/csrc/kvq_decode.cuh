@@ -274,6 +274,181 @@ __device__ void rows_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets&
     }
 }
 
+// Combine the 4 warps' partials (comb[warp][head][D + 2] = o[D], m, l) of one work item
+// into the item's workspace slot.  Called by the whole block after a barrier.
+template <int D>
+__device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* comb, float* red, int b,
+                                              int h, int item) {
+    const int tid = threadIdx.x;
+    const int gqa = a.lo.gqa;
+    float* wgt = red;   // [head][4 warps]
+    if (tid < gqa) {
+        float M = -INFINITY, l = 0.0f;
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, comb[(w * gqa + tid) * (D + 2) + D]);
+        for (int w = 0; w < 4; ++w) {
+            const float* cwp = comb + (w * gqa + tid) * (D + 2);
+            const float wt = cwp[D + 1] > 0.0f ? fast_exp2(cwp[D] - M) : 0.0f;
+            wgt[tid * 4 + w] = wt;
+            l = fmaf(cwp[D + 1], wt, l);
+        }
+        float* ml = reinterpret_cast<float*>(a.ws + a.plan.ws_ml_off) + 2 * slot_index(a, b, h, item, tid);
+        ml[0] = M;
+        ml[1] = l;
+    }
+    __syncthreads();
+    float* wso = reinterpret_cast<float*>(a.ws + a.plan.ws_o_off);
+    for (int i = tid; i < gqa * D; i += blockDim.x) {
+        const int head = i / D, c = i % D;
+        float o = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float wt = wgt[head * 4 + w];
+            if (wt != 0.0f) o = fmaf(comb[(w * gqa + head) * (D + 2) + c], wt, o);
+        }
+        wso[slot_index(a, b, h, item, head) * D + c] = o;
+    }
+}
+
+// ------------------------------------------------------------------------ window path
+// The bf16 window of a KIVI cache.  Keys and queries are exact bf16 values, so the scores
+// go straight to the tensor cores (no conversion, no operand split): rows = 16 tokens,
+// columns = up to 8 query heads.  Each warp takes one 16-token tile, keeps its own
+// softmax partial, and accumulates P.V on CUDA cores with every lane owning D/32
+// consecutive channels; the block then combines its 4 warps.
+template <int D>
+__device__ void window_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& so, int b, int h,
+                            int item, int64_t t0, int64_t t1) {
+    constexpr int KSTEPS = D / 16;
+    constexpr int CPL = D / 32;
+    const Layout& lo = a.lo;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+    const int cnt = static_cast<int>(t1 - t0);
+    const int gqa = lo.gqa;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + so.bar);
+    float* red = reinterpret_cast<float*>(smem + so.red);
+    float* comb = reinterpret_cast<float*>(smem + so.sc);       // [warp][head][D + 2]
+    float* pw = reinterpret_cast<float*>(smem + so.pw);         // [warp][16 tokens][8 heads]
+    uint8_t* data = smem + so.data;
+    const int64_t u = unit_index(lo, a.layer, b, h);
+
+    if (tid == 0) mbar_init(bar, 1);
+    __syncthreads();
+    if (tid == 0) {
+        const uint8_t* ring = a.cache + lo.ring_off + u * lo.C * (int64_t)(4 * D);
+        const int s0 = static_cast<int>(t0 % lo.C);
+        const int first = cnt < lo.C - s0 ? cnt : lo.C - s0;
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * 4 * D);
+        bulk_copy_pieces(data, ring + (int64_t)s0 * 4 * D, static_cast<uint32_t>(first) * 4 * D, bar);
+        if (cnt > first)
+            bulk_copy_pieces(data + (int64_t)first * 4 * D, ring, static_cast<uint32_t>(cnt - first) * 4 * D, bar);
+    }
+    // query operand: column g = head g (zero beyond gqa), k = channel pairs (2t, 2t+1) and
+    // (2t+8, 2t+9) of each 16-channel step, straight from the caller's bf16 query
+    uint32_t bq[KSTEPS][2];
+    {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            reinterpret_cast<const uint16_t*>(a.q) + ((int64_t)b * lo.Hq + (int64_t)h * gqa + g) * D);
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+            bq[ks][0] = g < gqa ? qrow[(16 * ks + 2 * tig) / 2] : 0u;
+            bq[ks][1] = g < gqa ? qrow[(16 * ks + 8 + 2 * tig) / 2] : 0u;
+        }
+    }
+    const bool ok = wait_staged(bar, a.ws);
+    const int tok0 = 16 * warp;
+    const int ntok = cnt - tok0 < 0 ? 0 : (cnt - tok0 > 16 ? 16 : cnt - tok0);
+    float o[8][CPL];
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh)
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) o[hh][e] = 0.0f;
+    float mh = -INFINITY, lh = 0.0f;      // this lane's head (lane < gqa): max and sum
+    if (ok && ntok > 0) {
+        // scores: rows g, g + 8 of the tile (tokens beyond the window read as zero rows)
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const uint8_t* r0 = data + (int64_t)(tok0 + g) * 4 * D;
+        const uint8_t* r1 = data + (int64_t)(tok0 + g + 8) * 4 * D;
+        const bool v0 = g < ntok, v1 = g + 8 < ntok;
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+            uint32_t af[4];
+            af[0] = v0 ? *reinterpret_cast<const uint32_t*>(r0 + 2 * (16 * ks + 2 * tig)) : 0u;
+            af[1] = v1 ? *reinterpret_cast<const uint32_t*>(r1 + 2 * (16 * ks + 2 * tig)) : 0u;
+            af[2] = v0 ? *reinterpret_cast<const uint32_t*>(r0 + 2 * (16 * ks + 8 + 2 * tig)) : 0u;
+            af[3] = v1 ? *reinterpret_cast<const uint32_t*>(r1 + 2 * (16 * ks + 8 + 2 * tig)) : 0u;
+            mma_16816_bf16(acc, af, bq[ks][0], bq[ks][1]);
+        }
+        // lane (g, t) holds heads 2t, 2t+1 for tokens g and g + 8
+        float sc[2][2];
+        sc[0][0] = v0 ? acc[0] * a.qscale : -INFINITY;
+        sc[0][1] = v0 ? acc[1] * a.qscale : -INFINITY;
+        sc[1][0] = v1 ? acc[2] * a.qscale : -INFINITY;
+        sc[1][1] = v1 ? acc[3] * a.qscale : -INFINITY;
+        float m0 = fmaxf(sc[0][0], sc[1][0]), m1 = fmaxf(sc[0][1], sc[1][1]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+        }
+        float* pt = pw + warp * 16 * 8;
+        const float p00 = v0 ? fast_exp2(sc[0][0] - m0) : 0.0f, p01 = v0 ? fast_exp2(sc[0][1] - m1) : 0.0f;
+        const float p10 = v1 ? fast_exp2(sc[1][0] - m0) : 0.0f, p11 = v1 ? fast_exp2(sc[1][1] - m1) : 0.0f;
+        pt[g * 8 + 2 * tig] = p00;
+        pt[g * 8 + 2 * tig + 1] = p01;
+        pt[(g + 8) * 8 + 2 * tig] = p10;
+        pt[(g + 8) * 8 + 2 * tig + 1] = p11;
+        float l0 = p00 + p10, l1 = p01 + p11;
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        // lane hh (< gqa) keeps head hh's max and sum: heads 2t, 2t+1 live in lanes t
+        const int src = (lane < 8 ? lane : 0) >> 1;
+        const float mm0 = __shfl_sync(0xffffffffu, m0, src), mm1 = __shfl_sync(0xffffffffu, m1, src);
+        const float ll0 = __shfl_sync(0xffffffffu, l0, src), ll1 = __shfl_sync(0xffffffffu, l1, src);
+        mh = (lane & 1) ? mm1 : mm0;
+        lh = (lane & 1) ? ll1 : ll0;
+        __syncwarp();
+        // values: lane owns channels [lane * CPL, lane * CPL + CPL)
+        for (int i = 0; i < ntok; ++i) {
+            const uint16_t* vr = reinterpret_cast<const uint16_t*>(data + (int64_t)(tok0 + i) * 4 * D + 2 * D) + lane * CPL;
+            float v[CPL];
+#pragma unroll
+            for (int e = 0; e < CPL; e += 2) {
+                const uint32_t two = *reinterpret_cast<const uint32_t*>(vr + e);
+                v[e] = __uint_as_float(two << 16);
+                v[e + 1] = __uint_as_float(two & 0xffff0000u);
+            }
+            const float4 pa = *reinterpret_cast<const float4*>(pt + i * 8);
+            const float4 pb = *reinterpret_cast<const float4*>(pt + i * 8 + 4);
+            const float pp[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+            for (int hh = 0; hh < 8; ++hh) {
+                if (hh >= gqa) break;
+#pragma unroll
+                for (int e = 0; e < CPL; ++e) o[hh][e] = fmaf(pp[hh], v[e], o[hh][e]);
+            }
+        }
+    }
+    // warp partial into shared memory, then the 4 warps combined
+    float* cw = comb + (int64_t)warp * gqa * (D + 2);
+    const bool wlive = ok && ntok > 0;
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh) {
+        if (hh >= gqa) break;
+        if (wlive)
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) cw[hh * (D + 2) + lane * CPL + e] = o[hh][e];
+    }
+    if (lane < gqa) {
+        cw[lane * (D + 2) + D] = wlive ? mh : -INFINITY;
+        cw[lane * (D + 2) + D + 1] = wlive ? lh : 0.0f;
+    }
+    __syncthreads();
+    combine_warps<D>(a, comb, red, b, h, item);
+}
+
 // ------------------------------------------------------------------------ packed path
 template <int N>
 __device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[N]) {
@@ -456,8 +631,9 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                     }
                 }
             }
-            // ---- pass 1: scores of the warp's tiles, kept in registers
-            float sc2[MAXT][NT][2];
+            // ---- pass 1: scores of the warp's tiles, parked in the warp's shared scratch
+            // (rolled loops keep the kernel within the instruction cache)
+            float2* wsc = reinterpret_cast<float2*>(smem + so.sc) + (int64_t)warp * MAXT * NT * 32 + lane;
             float cmax[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) cmax[nt] = -INFINITY;
@@ -465,9 +641,8 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                 uint32_t bq[NT][NPAIR];
                 float cst[NT];
                 int grp = 0, ti = 0;            // group and offset of the tile in the group
-#pragma unroll
-                for (int i = 0; i < MAXT; ++i) {
-                    if (i >= ntl) break;
+#pragma unroll 1
+                for (int i = 0; i < ntl; ++i) {
                     if (i > 0) {
                         ti += 16;
                         if (ti == G) { ti = 0; ++grp; }
@@ -501,9 +676,13 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                     uint32_t wa[ROWW], wb[ROWW];
                     load_words<ROWW>(rec + (ti + rho0) * rowbytes + tig * (ROWW * 4), wa);
                     load_words<ROWW>(rec + (ti + rho1) * rowbytes + tig * (ROWW * 4), wb);
-                    float acc[NT][4];
+                    // two accumulator chains (even and odd k steps) for instruction-level
+                    // parallelism between the dependent tensor-core operations
+                    float acc[2][NT][4];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+                    for (int e = 0; e < 2; ++e)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) acc[e][nt][0] = acc[e][nt][1] = acc[e][nt][2] = acc[e][nt][3] = 0.0f;
 #pragma unroll
                     for (int ks = 0; ks < KSTEPS; ++ks) {
                         const int m0 = 2 * ks, m1 = 2 * ks + 1;
@@ -513,13 +692,14 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                         af[2] = code_pair<BITS>(wa[m1 / HPW], BITS * (m1 % HPW));
                         af[3] = code_pair<BITS>(wb[m1 / HPW], BITS * (m1 % HPW));
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) mma_16816(acc[nt], af, bq[nt][m0], bq[nt][m1]);
+                        for (int nt = 0; nt < NT; ++nt) mma_16816(acc[ks & 1][nt], af, bq[nt][m0], bq[nt][m1]);
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        sc2[i][nt][0] = fmaf(acc[nt][0] + acc[nt][1], qup, cst[nt]);
-                        sc2[i][nt][1] = fmaf(acc[nt][2] + acc[nt][3], qup, cst[nt]);
-                        cmax[nt] = fmaxf(cmax[nt], fmaxf(sc2[i][nt][0], sc2[i][nt][1]));
+                        const float s0 = fmaf((acc[0][nt][0] + acc[1][nt][0]) + (acc[0][nt][1] + acc[1][nt][1]), qup, cst[nt]);
+                        const float s1 = fmaf((acc[0][nt][2] + acc[1][nt][2]) + (acc[0][nt][3] + acc[1][nt][3]), qup, cst[nt]);
+                        wsc[(i * NT + nt) * 32] = make_float2(s0, s1);
+                        cmax[nt] = fmaxf(cmax[nt], fmaxf(s0, s1));
                     }
                 }
             }
@@ -546,9 +726,8 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
             }
             // ---- pass 2: p = 2^(s - max) and the value contraction, tile by tile
             int grp = 0, ti = 0;
-#pragma unroll
-            for (int i = 0; i < MAXT; ++i) {
-                if (i >= ntl) break;
+#pragma unroll 1
+            for (int i = 0; i < ntl; ++i) {
                 if (i > 0) {
                     ti += 16;
                     if (ti == G) { ti = 0; ++grp; }
@@ -557,8 +736,9 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                 uint32_t pa1[NT], pb1[NT], pa2[NT], pb2[NT];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const float p0 = fast_exp2(sc2[i][nt][0] - mrun[nt]);
-                    const float p1 = fast_exp2(sc2[i][nt][1] - mrun[nt]);
+                    const float2 sv = wsc[(i * NT + nt) * 32];
+                    const float p0 = fast_exp2(sv.x - mrun[nt]);
+                    const float p1 = fast_exp2(sv.y - mrun[nt]);
                     lrun[nt] += p0 + p1;
                     // p as fp16 major + minor, moved to the lanes of the value fragment
                     const __half2 pa = __floats2half2_rn(p0, p1);
@@ -654,33 +834,7 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         }
     }
     __syncthreads();
-    // per (warp, head) weight 2^(m_w - M) and the combined max and sum, once per head
-    float* wgt = red;   // [head][4 warps] (red is free again)
-    if (tid < gqa) {
-        float M = -INFINITY, l = 0.0f;
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, comb[(w * gqa + tid) * (D + 2) + D]);
-        for (int w = 0; w < 4; ++w) {
-            const float* cwp = comb + (w * gqa + tid) * (D + 2);
-            const float wt = cwp[D + 1] > 0.0f ? fast_exp2(cwp[D] - M) : 0.0f;
-            wgt[tid * 4 + w] = wt;
-            l = fmaf(cwp[D + 1], wt, l);
-        }
-        float* ml = reinterpret_cast<float*>(a.ws + a.plan.ws_ml_off) + 2 * slot_index(a, b, h, item, tid);
-        ml[0] = M;
-        ml[1] = l;
-    }
-    __syncthreads();
-    float* wso = reinterpret_cast<float*>(a.ws + a.plan.ws_o_off);
-    for (int i = tid; i < gqa * D; i += blockDim.x) {
-        const int head = i / D, c = i % D;
-        float o = 0.0f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float wt = wgt[head * 4 + w];
-            if (wt != 0.0f) o = fmaf(comb[(w * gqa + head) * (D + 2) + c], wt, o);
-        }
-        wso[slot_index(a, b, h, item, head) * D + c] = o;
-    }
+    combine_warps<D>(a, comb, red, b, h, item);
 }
 
 // One block per (item, kv head, sequence).  BITS == 0: no packed path (INT8 / FP8).
@@ -694,10 +848,11 @@ __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
     if (r.t0 >= r.t1) return;
     const SmemOffsets so = decode_smem(a.lo, a.plan);
     if constexpr (BITS != 0) {
-        if (item >= a.plan.NRC) {
+        if (item >= a.plan.NRC)
             packed_item<D, BITS, NT>(a, smem, so, b, h, item, r.t0, r.t1);
-            return;
-        }
+        else
+            window_item<D>(a, smem, so, b, h, item, r.t0, r.t1);
+        return;
     }
     rows_item<D>(a, smem, so, b, h, item, r.t0, r.t1);
 }

@@ -57,7 +57,7 @@ struct DecodePlan {
 
 // Shared-memory carve of the decode block, identical on host and device.
 struct SmemOffsets {
-    int64_t bar, red, hstat, qs, qpa, qpb, sc, data, total;
+    int64_t bar, red, hstat, qs, qpa, qpb, pw, sc, data, total;
 };
 __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const DecodePlan& p) {
     SmemOffsets o;
@@ -68,11 +68,15 @@ __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const Decod
     o.qs = off;    off += (int64_t)lo.gqa * lo.D * 4; // scaled query, fp32
     o.qpa = off;   off += (int64_t)4 * p.NT * 4 * (lo.D / 8) * 4;
     o.qpb = off;   off += (int64_t)4 * p.NT * 4 * (lo.D / 8) * 4;
+    o.pw = off;    off += 4 * 16 * 8 * 4;                // window path: [warp][token][head] p
     o.sc = off;
     {
         const int64_t rows_sc = (int64_t)lo.gqa * p.CHR;                // row path scores
         const int64_t comb = (int64_t)4 * lo.gqa * (lo.D + 2);           // per-warp partials
-        off += 4 * (rows_sc > comb ? rows_sc : comb);
+        const int64_t wsc = (int64_t)4 * 8 * p.NT * 32 * 2;              // per-warp tile scores
+        int64_t big = rows_sc > comb ? rows_sc : comb;
+        big = big > wsc ? big : wsc;
+        off += 4 * big;
     }
     off = (off + 127) / 128 * 128;
     o.data = off;
@@ -157,6 +161,16 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
                                           uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D(16x8 f32) += A(16x16 bf16, row) * B(16x8 bf16, col)
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
