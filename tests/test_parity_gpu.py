@@ -199,3 +199,16 @@ def test_fp8_saturation_and_subnormals():
     sc = torch.tensor([[1.0, 0.5]])
     p.append(0, k, v, fp8_scales=sc)
     p.assert_same_image()
+
+
+def test_fp8_long_context_separate_merge():
+    # enough row chunks that the per-chunk merge weights exceed the decode block's scratch, so
+    # the split context is merged by the separate merge kernel
+    p = Pair("fp8", batch=1, q_heads=4, kv_heads=1, head_dim=128, max_tokens=80000)
+    g = gen(13)
+    k, v = p.rand_kv(1, 79000, g)
+    sc = torch.stack([k.float().abs().amax(dim=(0, 1, 3)), v.float().abs().amax(dim=(0, 1, 3))], 1) / 448
+    p.append(0, k, v, fp8_scales=sc)
+    p.assert_same_image()
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="fp8 long")
