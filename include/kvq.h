@@ -204,6 +204,28 @@ int kvq_decode_attention(const kvq_config* cfg, const void* cache, int32_t layer
                          uint64_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * kvq_decode_attention_noalloc -- the same decode as kvq_decode_attention for callers that
+ * cannot allocate device memory for a workspace: code running where cudaMalloc is not
+ * allowed or not wanted (an allocator or memory-pool callback, a plugin whose host owns all
+ * device memory, a path that must not synchronise the device the way an allocation can).
+ * The pages have no counterpart: this is an interface convenience of this library.
+ *   The split-context scratch lives in a fixed array of KVQ_NOALLOC_SCRATCH_BYTES that the
+ *   library holds in device memory on every GPU that loads it, until the process exits.
+ *   Configurations whose kvq_workspace_bytes exceeds it are rejected with
+ *   KVQ_ERR_WORKSPACE before anything is enqueued.  The call allocates nothing.
+ *   The first call on a device looks the array's device address up (once per device, with
+ *   that device current); make that first call before any stream capture.
+ *   Every call on a device shares the one array and it keeps the previous call's
+ *   contents: calls that overlap on the GPU (different streams, or threads) race and
+ *   corrupt each other's results; serialise them.  Each call clears the array's status
+ *   word; a device-side status (a bounded wait that gave up) is not reported by this
+ *   variant.  Arguments, layouts and the output are those of kvq_decode_attention.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+int kvq_decode_attention_noalloc(const kvq_config* cfg, const void* cache, int32_t layer, const void* q,
+                                 float softmax_scale, float* out, kvq_stream_t stream);
+
+/*
  * kvq_read_status -- OR of the status words of `cache` and `workspace` (either may be
  * NULL) into *out (host).  Synchronises `stream` to read them.
  */

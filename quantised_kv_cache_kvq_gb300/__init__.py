@@ -12,6 +12,7 @@ from ._native import (  # noqa: F401
     KVQ_NO_AUTOFLUSH, KVQ_SCHEME_FP8_E4M3, KVQ_SCHEME_INT8, KVQ_SCHEME_KIVI,
     KVQ_STATUS_CAPACITY, KVQ_STATUS_NONFINITE, KVQ_STATUS_RING_FULL, KVQ_STATUS_TIMEOUT,
     KvqConfig, KvqError, kvq_cache_bytes, kvq_cache_init, kvq_decode_attention,
+    kvq_decode_attention_noalloc,
     kvq_flush_group, kvq_quantize_append, kvq_read_status, kvq_sequence_lengths,
     kvq_workspace_bytes, library_path, load, status_string,
 )

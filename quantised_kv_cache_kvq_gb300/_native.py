@@ -17,9 +17,10 @@ KVQ_STATUS_CAPACITY, KVQ_STATUS_RING_FULL, KVQ_STATUS_NONFINITE, KVQ_STATUS_TIME
 # every symbol include/kvq.h declares
 EXPORTS = (
     "kvq_cache_bytes", "kvq_cache_init", "kvq_quantize_append", "kvq_flush_group",
-    "kvq_workspace_bytes", "kvq_decode_attention", "kvq_read_status", "kvq_sequence_lengths",
-    "kvq_status_string",
+    "kvq_workspace_bytes", "kvq_decode_attention", "kvq_decode_attention_noalloc", "kvq_read_status",
+    "kvq_sequence_lengths", "kvq_status_string",
 )
+KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class KvqConfig(C.Structure):
@@ -64,6 +65,7 @@ def load():
         "kvq_flush_group": [cfgp, P, i32, P],
         "kvq_workspace_bytes": [cfgp, C.POINTER(u64)],
         "kvq_decode_attention": [cfgp, P, i32, P, C.c_float, P, P, u64, P],
+        "kvq_decode_attention_noalloc": [cfgp, P, i32, P, C.c_float, P, P],
         "kvq_read_status": [P, P, C.POINTER(u32), P],
         "kvq_sequence_lengths": [cfgp, P, i32, P, P, P],
     }
@@ -139,6 +141,12 @@ def kvq_decode_attention(cfg, cache, layer, q, softmax_scale, out, workspace, wo
     _check("kvq_decode_attention", load().kvq_decode_attention(
         C.byref(cfg), _ptr(cache), int(layer), _ptr(q), float(softmax_scale), _ptr(out),
         _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def kvq_decode_attention_noalloc(cfg, cache, layer, q, softmax_scale, out, stream=None):
+    """Decode with the library's own fixed scratch (no workspace argument; see kvq.h)."""
+    _check("kvq_decode_attention_noalloc", load().kvq_decode_attention_noalloc(
+        C.byref(cfg), _ptr(cache), int(layer), _ptr(q), float(softmax_scale), _ptr(out), _stream(stream)))
 
 
 def kvq_read_status(cache=None, workspace=None, stream=None):
