@@ -86,8 +86,12 @@ int make_plan(const Layout& lo, DecodePlan* p) {
     if (lo.scheme == KVQ_SCHEME_KIVI) {
         p->CHR = 64;
         p->NRC = (lo.C + p->CHR - 1) / p->CHR;
-        // a warp takes W tokens: whole groups, at least 64 tokens; a block takes 4 warps
-        const int W = lo.G >= 64 ? lo.G : lo.G * ((64 + lo.G - 1) / lo.G);
+        // a warp takes W tokens (a multiple of 16, at least 64) and a block 4 warps, with 4 * W
+        // a whole number of groups: W = 16 * (G / gcd(G, 64)) scaled up to 64 or more
+        int gg = lo.G, hh = 64;
+        while (hh) { const int t = gg % hh; gg = hh; hh = t; }
+        const int wstep = 16 * (lo.G / gg);
+        const int W = wstep * ((64 + wstep - 1) / wstep);
         p->W = W;
         p->CH = 4 * W;
         // chunks per item: about 8 blocks per SM over all units (capacity-based; items

@@ -595,14 +595,17 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         const int64_t c0 = t0 + (int64_t)j * CH;
         const int ctok = static_cast<int>((t1 - c0) < CH ? (t1 - c0) : CH);
         const int wtok = ctok - warp * W < 0 ? 0 : (ctok - warp * W > W ? W : ctok - warp * W);   // whole groups
-        const uint8_t* stage = smem + so.data + (j % nstage) * stage_bytes + (int64_t)warp * (W / G) * lo.rec;
+        // the warp's tokens start W * warp tokens into the chunk: group g0 of the chunk's
+        // records, offset ti0 in it (a group may be shared by two warps)
+        const int g0 = (warp * W) / G, ti0 = (warp * W) % G;
+        const uint8_t* stage = smem + so.data + (j % nstage) * stage_bytes + (int64_t)g0 * lo.rec;
         if (wtok > 0) {
             const int ntl = wtok / 16;
             // offset term of every group of the warp: cst[group][head] = sum_c q_c zero_c,
             // as one small tensor-core product (rows = groups, k = channels in pair order)
             float cstf[NT][4];
             {
-                const int ngrp = wtok / G;
+                const int ngrp = (ti0 + wtok + G - 1) / G;   // groups the warp's tokens touch
                 uint32_t zreg[D / 8];
                 if (g < ngrp) {
                     const __half* zK = reinterpret_cast<const __half*>(stage + (int64_t)g * lo.rec + kc_bytes + vc_bytes) + D;
@@ -640,7 +643,7 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
             {
                 uint32_t bq[NT][NPAIR];
                 float cst[NT];
-                int grp = 0, ti = 0;            // group and offset of the tile in the group
+                int grp = 0, ti = ti0;          // group (from g0) and offset of the tile in it
 #pragma unroll 1
                 for (int i = 0; i < ntl; ++i) {
                     if (i > 0) {
@@ -648,7 +651,7 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                         if (ti == G) { ti = 0; ++grp; }
                     }
                     const uint8_t* rec = stage + (int64_t)grp * lo.rec;
-                    if (ti == 0) {
+                    if (i == 0 || ti == 0) {
                         // key-score operand of the group: (q * key scale) as fp16 major + minor
                         const __half* sK = reinterpret_cast<const __half*>(rec + kc_bytes + vc_bytes);
                         uint32_t sreg[D / 8];
@@ -725,7 +728,7 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                 mrun[nt] = mnew;
             }
             // ---- pass 2: p = 2^(s - max) and the value contraction, tile by tile
-            int grp = 0, ti = 0;
+            int grp = 0, ti = ti0;
 #pragma unroll 1
             for (int i = 0; i < ntl; ++i) {
                 if (i > 0) {
