@@ -79,6 +79,14 @@ int make_layout(const kvq_config* c, int64_t max_tokens, Layout* out) {
     return KVQ_OK;
 }
 
+// Decode blocks resident per SM for `smem` bytes of dynamic shared memory: 4 by the
+// kernel's register bound, fewer when 228 KiB of shared memory per SM (1 KiB of it
+// reserved per block) does not hold 4.
+static int resident_blocks(int64_t smem) {
+    const int64_t r = (228 * 1024) / (smem + 1024);
+    return r < 4 ? static_cast<int>(r) : 4;
+}
+
 int make_plan(const Layout& lo, DecodePlan* p) {
     std::memset(p, 0, sizeof *p);
     p->NT = lo.gqa > 4 ? 2 : 1;
@@ -94,17 +102,24 @@ int make_plan(const Layout& lo, DecodePlan* p) {
         const int W = wstep * ((64 + wstep - 1) / wstep);
         p->W = W;
         p->CH = 4 * W;
-        // chunks per item: about 8 blocks per SM over all units (capacity-based; items
-        // beyond a sequence's length exit at once), at most 32 chunks per item
+        // chunks per item (capacity-based; items beyond a sequence's length exit at once):
+        // as many as make the items fit one wave of resident blocks, so the per-block setup
+        // and combine are paid once per block of a wave and no wave runs part-empty.  At
+        // most 32 chunks per item.
         const int64_t packed = (int64_t)lo.NG * lo.G;
         const int64_t chunks = (packed + p->CH - 1) / p->CH;
-        const int64_t target = 8 * 152;
-        int64_t cpi = (units * chunks + target - 1) / target;
+        p->CPI = 1;
+        p->NSTAGE = 1;
+        const int res1 = resident_blocks(decode_smem(lo, *p).total);
+        const int64_t slots = (int64_t)kNumSMs * res1;
+        int64_t cpi = (units * chunks + slots - 1) / slots;
         cpi = cpi < 1 ? 1 : (cpi > 32 ? 32 : cpi);
         p->CPI = static_cast<int>(cpi);
-        // double-buffer the chunks of multi-chunk items when two stages stay within 64 KiB
-        const int64_t stage = (int64_t)(p->CH / lo.G) * lo.rec;
-        p->NSTAGE = (cpi > 1 && 2 * stage <= 65536) ? 2 : 1;
+        // double-buffer the chunks of multi-chunk items when that costs no resident block
+        if (cpi > 1) {
+            p->NSTAGE = 2;
+            if (resident_blocks(decode_smem(lo, *p).total) < res1) p->NSTAGE = 1;
+        }
         p->NQ = static_cast<int>((chunks + cpi - 1) / cpi);
     } else {
         p->CHR = 128;

@@ -26,6 +26,8 @@
 
 #include <cuda_fp8.h>
 
+#include <type_traits>
+
 #include "kvq_internal.cuh"
 #include "kvq_launch.h"
 
@@ -274,38 +276,48 @@ __device__ void rows_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets&
     }
 }
 
-// Combine the 4 warps' partials (comb[warp][head][D + 2] = o[D], m, l) of one work item
-// into the item's workspace slot.  Called by the whole block after a barrier.
+// Combine the 4 warps' partials of one work item (comb[warp][head][D] = o, cml[warp][head]
+// = (m, l)) into the item's workspace slots.  Called by the whole block after a barrier.
+// A warp without tokens leaves m = -inf, l = 0 and its o unwritten; it gets weight 0 and
+// its o is never read.
 template <int D>
-__device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* comb, float* red, int b,
-                                              int h, int item) {
+__device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* comb, const float* cml,
+                                              float* red, int b, int h, int item) {
     const int tid = threadIdx.x;
     const int gqa = a.lo.gqa;
     float* wgt = red;   // [head][4 warps]
     if (tid < gqa) {
         float M = -INFINITY, l = 0.0f;
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, comb[(w * gqa + tid) * (D + 2) + D]);
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, cml[2 * (w * gqa + tid)]);
         for (int w = 0; w < 4; ++w) {
-            const float* cwp = comb + (w * gqa + tid) * (D + 2);
-            const float wt = cwp[D + 1] > 0.0f ? fast_exp2(cwp[D] - M) : 0.0f;
+            const float* mlw = cml + 2 * (w * gqa + tid);
+            const float wt = mlw[1] > 0.0f ? fast_exp2(mlw[0] - M) : 0.0f;
             wgt[tid * 4 + w] = wt;
-            l = fmaf(cwp[D + 1], wt, l);
+            l = fmaf(mlw[1], wt, l);
         }
         float* ml = reinterpret_cast<float*>(a.ws + a.plan.ws_ml_off) + 2 * slot_index(a, b, h, item, tid);
         ml[0] = M;
         ml[1] = l;
     }
     __syncthreads();
-    float* wso = reinterpret_cast<float*>(a.ws + a.plan.ws_o_off);
-    for (int i = tid; i < gqa * D; i += blockDim.x) {
-        const int head = i / D, c = i % D;
-        float o = 0.0f;
+    // the item's gqa slots are consecutive: gqa * D floats, four per thread and step
+    float4* wso = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.ws + a.plan.ws_o_off) +
+                                            slot_index(a, b, h, item, 0) * D);
+    for (int i = tid; i < gqa * D / 4; i += blockDim.x) {
+        const int head = (4 * i) / D;
+        float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             const float wt = wgt[head * 4 + w];
-            if (wt != 0.0f) o = fmaf(comb[(w * gqa + head) * (D + 2) + c], wt, o);
+            if (wt != 0.0f) {
+                const float4 v = reinterpret_cast<const float4*>(comb + w * gqa * D)[i];
+                o.x = fmaf(v.x, wt, o.x);
+                o.y = fmaf(v.y, wt, o.y);
+                o.z = fmaf(v.z, wt, o.z);
+                o.w = fmaf(v.w, wt, o.w);
+            }
         }
-        wso[slot_index(a, b, h, item, head) * D + c] = o;
+        wso[i] = o;
     }
 }
 
@@ -326,7 +338,8 @@ __device__ void window_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     const int gqa = lo.gqa;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + so.bar);
     float* red = reinterpret_cast<float*>(smem + so.red);
-    float* comb = reinterpret_cast<float*>(smem + so.sc);       // [warp][head][D + 2]
+    float* comb = reinterpret_cast<float*>(smem + so.sc);       // [warp][head][D]
+    float* cml = comb + 4 * gqa * D;                            // [warp][head][m, l]
     float* pw = reinterpret_cast<float*>(smem + so.pw);         // [warp][16 tokens][8 heads]
     uint8_t* data = smem + so.data;
     const int64_t u = unit_index(lo, a.layer, b, h);
@@ -432,54 +445,99 @@ __device__ void window_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         }
     }
     // warp partial into shared memory, then the 4 warps combined
-    float* cw = comb + (int64_t)warp * gqa * (D + 2);
+    float* cw = comb + warp * gqa * D;
     const bool wlive = ok && ntok > 0;
 #pragma unroll
     for (int hh = 0; hh < 8; ++hh) {
         if (hh >= gqa) break;
         if (wlive)
 #pragma unroll
-            for (int e = 0; e < CPL; ++e) cw[hh * (D + 2) + lane * CPL + e] = o[hh][e];
+            for (int e = 0; e < CPL; ++e) cw[hh * D + lane * CPL + e] = o[hh][e];
     }
     if (lane < gqa) {
-        cw[lane * (D + 2) + D] = wlive ? mh : -INFINITY;
-        cw[lane * (D + 2) + D + 1] = wlive ? lh : 0.0f;
+        cml[2 * (warp * gqa + lane)] = wlive ? mh : -INFINITY;
+        cml[2 * (warp * gqa + lane) + 1] = wlive ? lh : 0.0f;
     }
     __syncthreads();
-    combine_warps<D>(a, comb, red, b, h, item);
+    combine_warps<D>(a, comb, cml, red, b, h, item);
 }
 
 // ------------------------------------------------------------------------ packed path
+// Loads from the staged chunk by 32-bit shared-window address.  They are volatile so the
+// compiler keeps them after the barrier waits (volatile asm with a memory clobber) that
+// make the bulk copies visible, and before the barrier that frees the stage.
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
 template <int N>
-__device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[N]) {
+__device__ __forceinline__ void lds_words(uint32_t a, uint32_t (&w)[N]) {
     if constexpr (N % 4 == 0) {
 #pragma unroll
         for (int i = 0; i < N; i += 4) {
-            const uint4 v = *reinterpret_cast<const uint4*>(p + 4 * i);
+            const uint4 v = lds128(a + 4 * i);
             w[i] = v.x; w[i + 1] = v.y; w[i + 2] = v.z; w[i + 3] = v.w;
         }
     } else if constexpr (N == 2) {
-        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        const uint2 v = lds64(a);
         w[0] = v.x; w[1] = v.y;
     } else {
 #pragma unroll
-        for (int i = 0; i < N; ++i) w[i] = reinterpret_cast<const uint32_t*>(p)[i];
+        for (int i = 0; i < N; ++i) w[i] = lds32(a + 4 * i);
     }
 }
 
-// Two codes of a 32-bit word (the one at bit `shift` and the one 16 bits above it) as an
-// exact fp16 pair: OR the code into the mantissa of 1024.0 and subtract 1024.
+// 2^k as a float for -126 <= k <= 127 (exact).
+__device__ __forceinline__ float exp2i(int k) { return __int_as_float((127 + k) << 23); }
+// 2^k as an fp16 pair for -14 <= k <= 15 (exact).
+__device__ __forceinline__ uint32_t exp2i_h2(int k) { return static_cast<uint32_t>((15 + k) << 10) * 0x00010001u; }
+
+// Code extraction.  A b-bit code c at bit p of a 16-bit half, with every other bit of the
+// half cleared, is the fp16 subnormal c * 2^(p - 24) -- exact, and made for the code pair
+// of both halves of a 32-bit word by one AND, as long as p + b <= 10 (the code stays in
+// the mantissa).  The factor 2^(p - 24) is undone exactly: 2^-p goes into the other MMA
+// operand as a power-of-two scale, 2^24 onto the fp32 result.
 template <int BITS>
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, int shift) {
-    constexpr uint32_t mask = ((1u << BITS) - 1u) * 0x00010001u;
-    const uint32_t x = ((w >> shift) & mask) | 0x64006400u;
-    return h2_as_u32(__hsub2(u32_as_h2(x), __half2(__half(1024.0f), __half(1024.0f))));
+__device__ __forceinline__ uint32_t code_bits(uint32_t w, int p) {
+    return w & ((((1u << BITS) - 1u) << p) * 0x00010001u);
+}
+// Key pair jj of a word (codes at bits BITS*jj and 16 + BITS*jj): the 2-bit codes above
+// bit 8 are first shifted down by 6 (one shift per word), everything else stays in place.
+template <int BITS> constexpr int key_shift(int jj) { return BITS * jj + BITS > 10 ? 6 : 0; }
+template <int BITS> constexpr int key_pos(int jj) { return BITS * jj - key_shift<BITS>(jj); }
+
+// (s * x) of fp16 pairs split in two fp16 parts by an error-free product: with x = (0,
+// major) -> the rounded product of s and `major`; with x = (major, minor) -> the rounding
+// error of s * major plus s * minor.  The lanes holding B column 2h take the first form,
+// the lanes of column 2h + 1 the second, so no lane selects between results.
+__device__ __forceinline__ uint32_t split_mul(__half2 s, uint32_t x, uint32_t y) {
+    const __half2 t = __hmul2(s, u32_as_h2(x));
+    const __half2 e = __hfma2(s, u32_as_h2(x), __hneg2(t));
+    return h2_as_u32(__hfma2(s, u32_as_h2(y), e));
 }
 
 // One packed work item: a run of chunks of CH = 4 * W tokens of one (sequence, kv head).
 // Chunks are staged by bulk copies into NSTAGE shared-memory buffers (double-buffered
 // when they fit), each warp takes W tokens of a chunk, and every warp keeps an online
 // softmax (running max, sum and output) across the chunks of the item.
+//
+// Scales.  Scores: A = key codes c * 2^(p - 24), B = q * s_c * 2^(E - p) with E per group
+// such that the largest key scale of the group times 2^E is below 2^15, so the product
+// is c * q * s_c * 2^(E - 24) and the score is the fp32 sum times 2^(24 - E).  Values:
+// A = value codes c * 2^(p - 24), B = P * s_t * 2^(Ev - p) with Ev per warp such that the
+// largest value scale seen so far times 2^Ev is below 2^15 (lowered, and what was
+// accumulated rescaled by the exact power of two, when a larger scale arrives).
 template <int D, int BITS, int NT>
 __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& so, int b, int h,
                             int item, int64_t t0, int64_t t1) {
@@ -487,33 +545,38 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     constexpr int HPW = CPW / 2;            // code pairs per word
     constexpr int NPAIR = D / 8;            // code pairs per thread per token row
     constexpr int KSTEPS = D / 16;
-    constexpr int ROWW = D * BITS / 128;    // words per thread per token row
+    constexpr int ROWW = D * BITS / 128;    // words per thread per key row
+    constexpr int ROWB = D * BITS / 8;      // bytes per key row
     constexpr int MTV = D / 16;             // 16-channel tiles of the value contraction
     constexpr int TPW = 32 / BITS;          // value tokens per word
     constexpr int HW = TPW / 2;
+    constexpr int VP1 = 2 * BITS <= 10 ? BITS : 0;   // position of the second value pair
     constexpr int MAXT = 8;                 // a warp holds at most 8 tiles (W <= 128 tokens)
+    constexpr int QROW = NPAIR + 4;         // words per row of the query tables (padded)
     const Layout& lo = a.lo;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
     const int G = lo.G, W = a.plan.W, CH = a.plan.CH, gqa = lo.gqa, NGv = lo.NGv;
     const int nstage = a.plan.NSTAGE;
-    const int64_t stage_bytes = (int64_t)(CH / G) * lo.rec;
+    const uint32_t rec = static_cast<uint32_t>(lo.rec);
+    const uint32_t stage_bytes = static_cast<uint32_t>(CH / G) * rec;
     const int nch = static_cast<int>((t1 - t0 + CH - 1) / CH);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + so.bar);
     float* red = reinterpret_cast<float*>(smem + so.red);
     float* qs = reinterpret_cast<float*>(smem + so.qs);
-    uint32_t* qpa = reinterpret_cast<uint32_t*>(smem + so.qpa);
-    uint32_t* qpb = reinterpret_cast<uint32_t*>(smem + so.qpb);
-    float* comb = reinterpret_cast<float*>(smem + so.sc);          // [warp][head][D + 2]
+    uint32_t* qx = reinterpret_cast<uint32_t*>(smem + so.qpa);
+    uint32_t* qy = reinterpret_cast<uint32_t*>(smem + so.qpb);
+    float* comb = reinterpret_cast<float*>(smem + so.sc);          // [warp][head][D]
+    float* cml = comb + 4 * gqa * D;                               // [warp][head][m, l]
     const int64_t u = unit_index(lo, a.layer, b, h);
     const uint8_t* src_unit = a.cache + lo.data_off + u * lo.unit;
 
     auto issue = [&](int j) {       // stage chunk j (thread 0 only)
         const int64_t c0 = t0 + (int64_t)j * CH;
         const int64_t ctok = (t1 - c0) < CH ? (t1 - c0) : CH;
-        const uint32_t bytes = static_cast<uint32_t>(ctok / G) * lo.rec;
+        const uint32_t bytes = static_cast<uint32_t>(ctok / G) * rec;
         uint64_t* bar = bars + (j % nstage);
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_copy_pieces(smem + so.data + (j % nstage) * stage_bytes, src_unit + (c0 / G) * (int64_t)lo.rec, bytes, bar);
+        bulk_copy_pieces(smem + so.data + (j % nstage) * stage_bytes, src_unit + (c0 / G) * (int64_t)rec, bytes, bar);
     };
     if (tid == 0) {
         for (int s2 = 0; s2 < nstage; ++s2) mbar_init(bars + s2, 1);
@@ -524,8 +587,9 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     }
     // query prep (whole block) while the copies are in flight: fp32 scaled query, a
     // power-of-two prescale bringing max|q| into [0.5, 1) so fp16 products cannot
-    // overflow, and the query in the thread-pair order of the key fragments split into
-    // fp16 major + minor parts
+    // overflow, and per-lane tables of the query in the lanes' key-pair order split into
+    // fp16 major + minor parts: row 32 * nt + lane holds x = (0 | major) and y = (major |
+    // minor) for B column g = 2 * head + part of that lane (split_mul)
     load_query(a, b, h, qs);
     __syncthreads();
     float qmax = 0.0f;
@@ -537,10 +601,11 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     int qexp = 0;
     if (qmax > 0.0f) frexpf(qmax, &qexp);
     const float qdown = ldexpf(1.0f, -qexp), qup = ldexpf(1.0f, qexp);
-    for (int i = tid; i < 4 * NT * 4 * NPAIR; i += blockDim.x) {
-        const int m = i % NPAIR, tg = (i / NPAIR) % 4, hh = i / (NPAIR * 4);
-        const int wi = m / HPW, j = m % HPW;
-        const int clo = tg * (D / 4) + wi * CPW + j, chi = clo + HPW;
+    for (int i = tid; i < 32 * NT * NPAIR; i += blockDim.x) {
+        const int m = i % NPAIR, row = i / NPAIR;
+        const int ln = row & 31, hh = 4 * (row >> 5) + (ln >> 3), pt = (ln >> 2) & 1, tg = ln & 3;
+        const int wi = m / HPW, jj = m % HPW;
+        const int clo = tg * (D / 4) + wi * CPW + jj, chi = clo + HPW;
         float vlo = 0.0f, vhi = 0.0f;
         if (hh < gqa) {
             vlo = qs[hh * D + clo] * qdown;
@@ -548,28 +613,42 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         }
         const __half2 major = __floats2half2_rn(vlo, vhi);
         const float2 mf = __half22float2(major);
-        qpa[i] = h2_as_u32(major);
-        qpb[i] = h2_as_u32(__floats2half2_rn(vlo - mf.x, vhi - mf.y));
+        const uint32_t mj = h2_as_u32(major), mn = h2_as_u32(__floats2half2_rn(vlo - mf.x, vhi - mf.y));
+        qx[row * QROW + m] = pt ? mj : 0u;
+        qy[row * QROW + m] = pt ? mn : mj;
     }
     __syncthreads();
 
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t qx_lane = sbase + static_cast<uint32_t>(so.qpa) + lane * QROW * 4;
+    const uint32_t qy_lane = sbase + static_cast<uint32_t>(so.qpb) + lane * QROW * 4;
     const int part = g & 1;                 // B column g = 2 * head + part
-    const int kc_bytes = lo.kc, vc_bytes = lo.vc;
-    const int rowbytes = D * BITS / 8;
+    const int re = g & 1;                   // score rows of this lane: odd token slots when 1
+    const uint32_t kpar = lo.kc + lo.vc;                    // key params in a record
+    const uint32_t vpar = kpar + lo.kp;                     // value params in a record
+    const uint32_t kscale_lane = kpar + tig * (D / 2);      // the lane's quarter of the key scales
+    const uint32_t kzero_lane = kscale_lane + 2 * D;
     // token order of the score tile rows: lane (g, tig) scores tokens rho0 = rho(g) and
     // rho1 = rho(g + 8) of each 16-token tile, chosen so that the value fragment of lane
     // (g', t') needs the pairs held by lanes (2t', h') and (2t' + 1, h') (h' = g' / 2)
-    const int rt = g >> 1, re = g & 1;
+    const int rt = g >> 1;
     const int rho0 = (2 * rt) / HW * TPW + (2 * rt) % HW + re;
     const int rho1 = rho0 + HW;
-    // this lane's value-fragment tokens of a tile (k slots 2t, 2t+1, 2t+8, 2t+9)
+    const uint32_t krow0 = rho0 * ROWB + tig * (ROWW * 4), krow1 = rho1 * ROWB + tig * (ROWW * 4);
+    // this lane's value-fragment tokens of a tile (k slots 2t, 2t+1, 2t+8, 2t+9): tA, tB
+    // at value-word position vj0 (low, high half), tC, tD at vj0 + 1; the lane shifts its
+    // value words right by BITS * vj0 so the pairs sit at bits 0 and BITS
     const int vwi = (2 * tig) / HW, vj0 = (2 * tig) % HW;
     const int tA = vwi * TPW + vj0, tB = tA + HW, tC = tA + 1, tD = tB + 1;
+    const uint32_t vsh = BITS * vj0;
+    const uint32_t cstride = static_cast<uint32_t>(G * BITS / 8);     // bytes of one channel's value codes
+    const uint32_t vcode_lane = lo.kc + g * cstride + vwi * 4;
+    const uint32_t oA = 4 * tA * NGv, oB = 4 * tB * NGv, oC = 4 * tC * NGv, oD = 4 * tD * NGv;
     const int src1 = (2 * tig) * 4 + (g >> 1), src2 = (2 * tig + 1) * 4 + (g >> 1);
-    // value groups are powers of two (multiples of 16 dividing head_dim): tile q of 16
-    // channels lies in value group q >> gvs
-    const int gvs = __ffs(lo.Gv) - 5;
-    const int wpc = G * BITS / 32;          // 32-bit words of one channel's value codes
+    const uint32_t pmask = part ? 0xffffffffu : 0u;
+    const uint32_t zg = g < NGv ? 4 * g : 0u, zmask = g < NGv ? 0xffffffffu : 0u;
+    const uint32_t zg8 = g + 8 < NGv ? 4 * (g + 8) : 0u, zmask8 = g + 8 < NGv ? 0xffffffffu : 0u;
+    const int gvs = __ffs(lo.Gv) - 5;       // value groups are powers of two >= 16
 
     float mrun[NT], lrun[NT];
     float oacc[MTV][NT][4];
@@ -582,6 +661,7 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
 #pragma unroll
         for (int mt = 0; mt < MTV; ++mt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.0f;
     }
+    int Ev = 15;
     bool live = true;
     for (int j = 0; j < nch; ++j) {
         bool ok = mbar_wait_bounded(bars + (j % nstage), (j / nstage) & 1, kWaitLimit);
@@ -594,22 +674,21 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         }
         const int64_t c0 = t0 + (int64_t)j * CH;
         const int ctok = static_cast<int>((t1 - c0) < CH ? (t1 - c0) : CH);
-        const int wtok = ctok - warp * W < 0 ? 0 : (ctok - warp * W > W ? W : ctok - warp * W);   // whole groups
+        const int wtok = ctok - warp * W < 0 ? 0 : (ctok - warp * W > W ? W : ctok - warp * W);   // multiple of 16
         // the warp's tokens start W * warp tokens into the chunk: group g0 of the chunk's
         // records, offset ti0 in it (a group may be shared by two warps)
         const int g0 = (warp * W) / G, ti0 = (warp * W) % G;
-        const uint8_t* stage = smem + so.data + (j % nstage) * stage_bytes + (int64_t)g0 * lo.rec;
+        const uint32_t st0 = sbase + static_cast<uint32_t>(so.data) + (j % nstage) * stage_bytes + g0 * rec;
         if (wtok > 0) {
-            const int ntl = wtok / 16;
+            const int ntl = wtok >> 4;
             // offset term of every group of the warp: cst[group][head] = sum_c q_c zero_c,
             // as one small tensor-core product (rows = groups, k = channels in pair order)
             float cstf[NT][4];
             {
-                const int ngrp = (ti0 + wtok + G - 1) / G;   // groups the warp's tokens touch
+                const int ngrp = (ti0 + wtok + G - 1) / G;   // groups the warp's tokens touch (<= 8)
                 uint32_t zreg[D / 8];
                 if (g < ngrp) {
-                    const __half* zK = reinterpret_cast<const __half*>(stage + (int64_t)g * lo.rec + kc_bytes + vc_bytes) + D;
-                    load_words<D / 8>(reinterpret_cast<const uint8_t*>(zK + tig * (D / 4)), zreg);
+                    lds_words<D / 8>(st0 + g * rec + kzero_lane, zreg);
                 } else {
 #pragma unroll
                     for (int i = 0; i < D / 8; ++i) zreg[i] = 0u;
@@ -617,9 +696,8 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     cstf[nt][0] = cstf[nt][1] = cstf[nt][2] = cstf[nt][3] = 0.0f;
-                    const int hh = 4 * nt + (g >> 1);
                     uint32_t qt[NPAIR];
-                    load_words<NPAIR>(reinterpret_cast<const uint8_t*>((part ? qpb : qpa) + (hh * 4 + tig) * NPAIR), qt);
+                    lds_words<NPAIR>(qy_lane + nt * 32 * QROW * 4, qt);
 #pragma unroll
                     for (int ks = 0; ks < KSTEPS; ++ks) {
                         uint32_t af[4];
@@ -641,73 +719,126 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) cmax[nt] = -INFINITY;
             {
-                uint32_t bq[NT][NPAIR];
-                float cst[NT];
-                int grp = 0, ti = ti0;          // group (from g0) and offset of the tile in it
+                int i = 0, grp = 0, ti = ti0;
+                uint32_t ro = st0;
 #pragma unroll 1
-                for (int i = 0; i < ntl; ++i) {
-                    if (i > 0) {
-                        ti += 16;
-                        if (ti == G) { ti = 0; ++grp; }
-                    }
-                    const uint8_t* rec = stage + (int64_t)grp * lo.rec;
-                    if (i == 0 || ti == 0) {
-                        // key-score operand of the group: (q * key scale) as fp16 major + minor
-                        const __half* sK = reinterpret_cast<const __half*>(rec + kc_bytes + vc_bytes);
+                while (i < ntl) {
+                    // key-score operand of the group: (q * key scale * 2^(E - p)) as fp16
+                    // major + minor, E from the group's largest key scale
+                    uint32_t bq[NT][NPAIR];
+                    float kf, cst[NT];
+                    {
                         uint32_t sreg[D / 8];
-                        load_words<D / 8>(reinterpret_cast<const uint8_t*>(sK + tig * (D / 4)), sreg);
+                        lds_words<D / 8>(ro + kscale_lane, sreg);
+                        __half2 mx = u32_as_h2(sreg[0]);
+#pragma unroll
+                        for (int k = 1; k < D / 8; ++k) mx = __hmax2(mx, u32_as_h2(sreg[k]));
+                        uint32_t mb = h2_as_u32(mx);
+                        mb = max(mb & 0xffffu, mb >> 16);
+                        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+                        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+                        const int E = min(15, 29 - static_cast<int>((mb >> 10) & 31u));
+                        kf = exp2i(24 - E) * qup;
+                        __half2 sp[NPAIR];
+#pragma unroll
+                        for (int m = 0; m < NPAIR; ++m) {
+                            const int wi = m / HPW, jj = m % HPW;
+                            const int lo_l = wi * CPW + jj, hi_l = lo_l + HPW;
+                            sp[m] = __hmul2(u32_as_h2(prmt(sreg[lo_l / 2], sreg[hi_l / 2], (jj & 1) ? 0x7632u : 0x5410u)),
+                                            u32_as_h2(exp2i_h2(E - key_pos<BITS>(jj))));
+                        }
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const int hh = 4 * nt + (g >> 1);
-                            uint32_t qa[NPAIR], qb[NPAIR];
-                            load_words<NPAIR>(reinterpret_cast<const uint8_t*>(qpa + (hh * 4 + tig) * NPAIR), qa);
-                            load_words<NPAIR>(reinterpret_cast<const uint8_t*>(qpb + (hh * 4 + tig) * NPAIR), qb);
+                            uint32_t xq[NPAIR], yq[NPAIR];
+                            lds_words<NPAIR>(qx_lane + nt * 32 * QROW * 4, xq);
+                            lds_words<NPAIR>(qy_lane + nt * 32 * QROW * 4, yq);
 #pragma unroll
-                            for (int m = 0; m < NPAIR; ++m) {
-                                const int wi = m / HPW, jj = m % HPW;
-                                const int lo_l = wi * CPW + jj, hi_l = lo_l + HPW;
-                                const __half2 s2 = u32_as_h2(prmt(sreg[lo_l / 2], sreg[hi_l / 2], (jj & 1) ? 0x7632u : 0x5410u));
-                                const __half2 major = __hmul2(s2, u32_as_h2(qa[m]));
-                                __half2 minor = __hfma2(s2, u32_as_h2(qa[m]), __hneg2(major));
-                                minor = __hfma2(s2, u32_as_h2(qb[m]), minor);
-                                bq[nt][m] = part ? h2_as_u32(minor) : h2_as_u32(major);
-                            }
-                            const float c = (grp < 8 ? cstf[nt][0] + cstf[nt][1] : cstf[nt][2] + cstf[nt][3]);
-                            cst[nt] = __shfl_sync(0xffffffffu, c, (grp & 7) * 4 + tig) * qup;
+                            for (int m = 0; m < NPAIR; ++m) bq[nt][m] = split_mul(sp[m], xq[m], yq[m]);
+                            const float c = __shfl_sync(0xffffffffu, cstf[nt][0] + cstf[nt][1], grp * 4 + tig);
+                            cst[nt] = c * qup;
                         }
                     }
-                    uint32_t wa[ROWW], wb[ROWW];
-                    load_words<ROWW>(rec + (ti + rho0) * rowbytes + tig * (ROWW * 4), wa);
-                    load_words<ROWW>(rec + (ti + rho1) * rowbytes + tig * (ROWW * 4), wb);
-                    // two accumulator chains (even and odd k steps) for instruction-level
-                    // parallelism between the dependent tensor-core operations
-                    float acc[2][NT][4];
+                    const int nseg = min(ntl - i, (G - ti) >> 4);
+                    uint32_t kro = ro + ti * ROWB;
+#pragma unroll 1
+                    for (int k = 0; k < nseg; ++k, ++i, kro += 16 * ROWB) {
+                        uint32_t wa[ROWW], wb[ROWW];
+                        lds_words<ROWW>(kro + krow0, wa);
+                        lds_words<ROWW>(kro + krow1, wb);
+                        // two accumulator chains (even and odd k steps) for instruction-level
+                        // parallelism between the dependent tensor-core operations
+                        float acc[2][NT][4];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e)
+                        for (int e = 0; e < 2; ++e)
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) acc[e][nt][0] = acc[e][nt][1] = acc[e][nt][2] = acc[e][nt][3] = 0.0f;
+                            for (int nt = 0; nt < NT; ++nt) acc[e][nt][0] = acc[e][nt][1] = acc[e][nt][2] = acc[e][nt][3] = 0.0f;
 #pragma unroll
-                    for (int ks = 0; ks < KSTEPS; ++ks) {
-                        const int m0 = 2 * ks, m1 = 2 * ks + 1;
-                        uint32_t af[4];
-                        af[0] = code_pair<BITS>(wa[m0 / HPW], BITS * (m0 % HPW));
-                        af[1] = code_pair<BITS>(wb[m0 / HPW], BITS * (m0 % HPW));
-                        af[2] = code_pair<BITS>(wa[m1 / HPW], BITS * (m1 % HPW));
-                        af[3] = code_pair<BITS>(wb[m1 / HPW], BITS * (m1 % HPW));
+                        for (int ks = 0; ks < KSTEPS; ++ks) {
+                            const int m0 = 2 * ks, m1 = 2 * ks + 1;
+                            const int j0 = m0 % HPW, j1 = m1 % HPW;
+                            uint32_t af[4];
+                            af[0] = code_bits<BITS>(wa[m0 / HPW] >> key_shift<BITS>(j0), key_pos<BITS>(j0));
+                            af[1] = code_bits<BITS>(wb[m0 / HPW] >> key_shift<BITS>(j0), key_pos<BITS>(j0));
+                            af[2] = code_bits<BITS>(wa[m1 / HPW] >> key_shift<BITS>(j1), key_pos<BITS>(j1));
+                            af[3] = code_bits<BITS>(wb[m1 / HPW] >> key_shift<BITS>(j1), key_pos<BITS>(j1));
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) mma_16816(acc[ks & 1][nt], af, bq[nt][m0], bq[nt][m1]);
+                            for (int nt = 0; nt < NT; ++nt) mma_16816(acc[ks & 1][nt], af, bq[nt][m0], bq[nt][m1]);
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const float s0 = fmaf((acc[0][nt][0] + acc[1][nt][0]) + (acc[0][nt][1] + acc[1][nt][1]), kf, cst[nt]);
+                            const float s1 = fmaf((acc[0][nt][2] + acc[1][nt][2]) + (acc[0][nt][3] + acc[1][nt][3]), kf, cst[nt]);
+                            wsc[(i * NT + nt) * 32] = make_float2(s0, s1);
+                            cmax[nt] = fmaxf(cmax[nt], fmaxf(s0, s1));
+                        }
                     }
+                    ro += rec;
+                    ti = 0;
+                    ++grp;
+                }
+            }
+            // value-scale exponent: the largest value scale of the warp's tokens in this
+            // chunk must stay below 2^(15 - Ev); lower Ev (and rescale) when it does not
+            {
+                // (the warp's tokens are a multiple of 16 per record: whole 16-byte runs of
+                // (scale, zero) pairs; the scale is the low half of each word)
+                uint32_t smx = 0;
+                int t = ti0, rem = wtok;
+                uint32_t r = st0;
+#pragma unroll 1
+                while (rem > 0) {
+                    const int n = min(rem, G - t);
+                    const uint32_t base = r + vpar + 4 * t * NGv;
+#pragma unroll 1
+                    for (int k = 4 * lane; k < n * NGv; k += 128) {
+                        const uint4 v = lds128(base + 4 * k);
+                        smx = max(smx, max(max(v.x & 0xffffu, v.y & 0xffffu), max(v.z & 0xffffu, v.w & 0xffffu)));
+                    }
+                    rem -= n;
+                    t = 0;
+                    r += rec;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) smx = max(smx, __shfl_xor_sync(0xffffffffu, smx, o));
+                const int en = min(15, 29 - static_cast<int>((smx >> 10) & 31u));
+                if (en < Ev) {
+                    const float f = exp2i(en - Ev);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const float s0 = fmaf((acc[0][nt][0] + acc[1][nt][0]) + (acc[0][nt][1] + acc[1][nt][1]), qup, cst[nt]);
-                        const float s1 = fmaf((acc[0][nt][2] + acc[1][nt][2]) + (acc[0][nt][3] + acc[1][nt][3]), qup, cst[nt]);
-                        wsc[(i * NT + nt) * 32] = make_float2(s0, s1);
-                        cmax[nt] = fmaxf(cmax[nt], fmaxf(s0, s1));
+                        lrun[nt] *= f;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) ozacc[nt][e] *= f;
+#pragma unroll
+                        for (int mt = 0; mt < MTV; ++mt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) oacc[mt][nt][e] *= f;
                     }
+                    Ev = en;
                 }
             }
             // running maximum per head (lanes of a head share tig); rescale what the warp
             // accumulated over earlier chunks when it grows
+            float mE[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 float m = cmax[nt];
@@ -726,96 +857,112 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                         for (int e = 0; e < 4; ++e) oacc[mt][nt][e] *= alpha;
                 }
                 mrun[nt] = mnew;
+                // p' = 2^(s - max + Ev - re * VP1): the value operand's power-of-two scale
+                // for this lane's token slots, applied in the exponent
+                mE[nt] = mnew - static_cast<float>(Ev - re * VP1);
             }
-            // ---- pass 2: p = 2^(s - max) and the value contraction, tile by tile
-            int grp = 0, ti = ti0;
+            // ---- pass 2: p' and the value contraction, tile by tile; the value-group
+            // size is a template parameter so the per-group operand rebuilds unroll
+            auto pass2 = [&](auto gvs_c) {
+                constexpr int GVS = decltype(gvs_c)::value;
+                constexpr int QM = (1 << GVS) - 1;
+                int i = 0, ti = ti0;
+                uint32_t ro = st0;
 #pragma unroll 1
-            for (int i = 0; i < ntl; ++i) {
-                if (i > 0) {
-                    ti += 16;
-                    if (ti == G) { ti = 0; ++grp; }
-                }
-                const uint8_t* rec = stage + (int64_t)grp * lo.rec;
-                uint32_t pa1[NT], pb1[NT], pa2[NT], pb2[NT];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float2 sv = wsc[(i * NT + nt) * 32];
-                    const float p0 = fast_exp2(sv.x - mrun[nt]);
-                    const float p1 = fast_exp2(sv.y - mrun[nt]);
-                    lrun[nt] += p0 + p1;
-                    // p as fp16 major + minor, moved to the lanes of the value fragment
-                    const __half2 pa = __floats2half2_rn(p0, p1);
-                    const float2 pf = __half22float2(pa);
-                    const __half2 pb = __floats2half2_rn(p0 - pf.x, p1 - pf.y);
-                    const uint32_t ua = h2_as_u32(pa), ub = h2_as_u32(pb);
-                    uint32_t x1 = __shfl_sync(0xffffffffu, ua, src1);
-                    uint32_t y1 = __shfl_sync(0xffffffffu, ub, src1);
-                    uint32_t x2 = __shfl_sync(0xffffffffu, ua, src2);
-                    uint32_t y2 = __shfl_sync(0xffffffffu, ub, src2);
-                    if (4 * nt + (g >> 1) >= gqa) x1 = y1 = x2 = y2 = 0u;
-                    pa1[nt] = x1; pb1[nt] = y1; pa2[nt] = x2; pb2[nt] = y2;
-                }
-                // values: O[c][col] += sum_t code[t][c] * (p_t * scale[t][gv(c)]); the offset
-                // term OZ[gv][col] += sum_t zero[t][gv] * p_t
-                const uint8_t* vpar = rec + kc_bytes + vc_bytes + lo.kp;
-                const uint32_t* vcw = reinterpret_cast<const uint32_t*>(rec + kc_bytes);
-                const uint32_t* pA = reinterpret_cast<const uint32_t*>(vpar + 4 * (ti + tA) * NGv);
-                const uint32_t* pB = reinterpret_cast<const uint32_t*>(vpar + 4 * (ti + tB) * NGv);
-                const uint32_t* pC = reinterpret_cast<const uint32_t*>(vpar + 4 * (ti + tC) * NGv);
-                const uint32_t* pD = reinterpret_cast<const uint32_t*>(vpar + 4 * (ti + tD) * NGv);
-                uint32_t zA = 0u, zC = 0u, zA8 = 0u, zC8 = 0u;   // zero pairs of value groups g, g + 8
-                if (g < NGv) { zA = prmt(pA[g], pB[g], 0x7632u); zC = prmt(pC[g], pD[g], 0x7632u); }
-                if (g + 8 < NGv) { zA8 = prmt(pA[g + 8], pB[g + 8], 0x7632u); zC8 = prmt(pC[g + 8], pD[g + 8], 0x7632u); }
-                uint32_t bp[NT][2];
-                const uint32_t* vct = vcw + (ti * BITS / 32 + vwi);
-#pragma unroll
-                for (int q = 0; q < MTV; ++q) {
-                    const int gv = q >> gvs;
-                    if (q == 0 || gv != ((q - 1) >> gvs)) {
-                        const __half2 s01 = u32_as_h2(prmt(pA[gv], pB[gv], 0x5410u));
-                        const __half2 s23 = u32_as_h2(prmt(pC[gv], pD[gv], 0x5410u));
+                while (i < ntl) {
+                    const int nseg = min(ntl - i, (G - ti) >> 4);
+#pragma unroll 1
+                    for (int k = 0; k < nseg; ++k, ++i, ti += 16) {
+                        uint32_t px1[NT], py1[NT], px2[NT], py2[NT];
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const __half2 M01 = __hmul2(s01, u32_as_h2(pa1[nt]));
-                            __half2 m01 = __hfma2(s01, u32_as_h2(pa1[nt]), __hneg2(M01));
-                            m01 = __hfma2(s01, u32_as_h2(pb1[nt]), m01);
-                            const __half2 M23 = __hmul2(s23, u32_as_h2(pa2[nt]));
-                            __half2 m23 = __hfma2(s23, u32_as_h2(pa2[nt]), __hneg2(M23));
-                            m23 = __hfma2(s23, u32_as_h2(pb2[nt]), m23);
-                            bp[nt][0] = part ? h2_as_u32(m01) : h2_as_u32(M01);
-                            bp[nt][1] = part ? h2_as_u32(m23) : h2_as_u32(M23);
+                            const float2 sv = wsc[(i * NT + nt) * 32];
+                            const float p0 = fast_exp2(sv.x - mE[nt]);
+                            const float p1 = fast_exp2(sv.y - mE[nt]);
+                            lrun[nt] += p0 + p1;
+                            // p' as fp16 major + minor, moved to the lanes of the value fragment
+                            const __half2 pa = __floats2half2_rn(p0, p1);
+                            const float2 pf = __half22float2(pa);
+                            const __half2 pb = __floats2half2_rn(p0 - pf.x, p1 - pf.y);
+                            const uint32_t ua = h2_as_u32(pa), ub = h2_as_u32(pb);
+                            const uint32_t x1 = __shfl_sync(0xffffffffu, ua, src1);
+                            const uint32_t y1 = __shfl_sync(0xffffffffu, ub, src1);
+                            const uint32_t x2 = __shfl_sync(0xffffffffu, ua, src2);
+                            const uint32_t y2 = __shfl_sync(0xffffffffu, ub, src2);
+                            px1[nt] = x1 & pmask;
+                            py1[nt] = part ? y1 : x1;
+                            px2[nt] = x2 & pmask;
+                            py2[nt] = part ? y2 : x2;
+                        }
+                        // values: O[c][col] += sum_t code[t][c] * (p'_t * scale[t][gv(c)]); the
+                        // offset term OZ[gv][col] += sum_t zero[t][gv] * p_t
+                        const uint32_t vpt = ro + vpar + 4 * ti * NGv;
+                        // zero pairs of value groups g and g + 8 (rows of the offset product);
+                        // lanes past the last group read group 0 and mask it out
+                        const uint32_t zA = prmt(lds32(vpt + oA + zg), lds32(vpt + oB + zg), 0x7632u) & zmask;
+                        const uint32_t zC = prmt(lds32(vpt + oC + zg), lds32(vpt + oD + zg), 0x7632u) & zmask;
+                        uint32_t zA8 = 0u, zC8 = 0u;
+                        if constexpr (D > 128) {
+                            zA8 = prmt(lds32(vpt + oA + zg8), lds32(vpt + oB + zg8), 0x7632u) & zmask8;
+                            zC8 = prmt(lds32(vpt + oC + zg8), lds32(vpt + oD + zg8), 0x7632u) & zmask8;
+                        }
+                        const uint32_t vct = ro + vcode_lane + ti * BITS / 8;
+                        uint32_t bv[NT][2];
+#pragma unroll
+                        for (int q = 0; q < MTV; ++q) {
+                            if ((q & QM) == 0) {
+                                const int gv = q >> GVS;
+                                const __half2 s01 = u32_as_h2(prmt(lds32(vpt + oA + 4 * gv), lds32(vpt + oB + 4 * gv), 0x5410u));
+                                const __half2 s23 = u32_as_h2(prmt(lds32(vpt + oC + 4 * gv), lds32(vpt + oD + 4 * gv), 0x5410u));
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    bv[nt][0] = split_mul(s01, px1[nt], py1[nt]);
+                                    bv[nt][1] = split_mul(s23, px2[nt], py2[nt]);
+                                }
+                            }
+                            const uint32_t w0 = lds32(vct + (16 * q) * cstride) >> vsh;
+                            const uint32_t w1 = lds32(vct + (16 * q + 8) * cstride) >> vsh;
+                            uint32_t af[4];
+                            af[0] = code_bits<BITS>(w0, 0);
+                            af[1] = code_bits<BITS>(w1, 0);
+                            af[2] = code_bits<BITS>(VP1 ? w0 : (w0 >> BITS), VP1);
+                            af[3] = code_bits<BITS>(VP1 ? w1 : (w1 >> BITS), VP1);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) mma_16816(oacc[q][nt], af, bv[nt][0], bv[nt][1]);
+                        }
+                        {
+                            // the second k-slot pair carries 2^-VP1 in p': undo it (exactly)
+                            uint32_t af[4] = {zA, zA8, zC, zC8};
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                mma_16816(ozacc[nt], af, py1[nt],
+                                          h2_as_u32(__hmul2(u32_as_h2(py2[nt]), u32_as_h2(exp2i_h2(VP1)))));
                         }
                     }
-                    const int c0 = 16 * q + g;
-                    const uint32_t w0 = vct[c0 * wpc];
-                    const uint32_t w1 = vct[(c0 + 8) * wpc];
-                    uint32_t af[4];
-                    af[0] = code_pair<BITS>(w0, BITS * vj0);
-                    af[1] = code_pair<BITS>(w1, BITS * vj0);
-                    af[2] = code_pair<BITS>(w0, BITS * (vj0 + 1));
-                    af[3] = code_pair<BITS>(w1, BITS * (vj0 + 1));
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) mma_16816(oacc[q][nt], af, bp[nt][0], bp[nt][1]);
+                    ro += rec;
+                    ti = 0;
                 }
-                {
-                    uint32_t af[4] = {zA, zA8, zC, zC8};
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        mma_16816(ozacc[nt], af, part ? pb1[nt] : pa1[nt], part ? pb2[nt] : pa2[nt]);
-                }
+            };
+            switch (gvs) {
+                case 0: pass2(std::integral_constant<int, 0>{}); break;
+                case 1: if constexpr (MTV > 1) pass2(std::integral_constant<int, 1>{}); break;
+                case 2: if constexpr (MTV > 2) pass2(std::integral_constant<int, 2>{}); break;
+                case 3: if constexpr (MTV > 4) pass2(std::integral_constant<int, 3>{}); break;
+                default: if constexpr (MTV > 8) pass2(std::integral_constant<int, 4>{}); break;
             }
         }
         __syncthreads();            // every warp is done with this stage
         if (tid == 0 && j + nstage < nch) issue(j + nstage);
     }
-    // ---- warp partial: reduce l over the lanes of a head, add the value offset term,
-    // combine the 4 warps in shared memory
-    float* cw = comb + (int64_t)warp * gqa * (D + 2);
+    // ---- warp partial: undo the power-of-two scales, reduce l over the lanes of a head,
+    // add the value offset term, combine the 4 warps in shared memory
+    float* cw = comb + warp * gqa * D;
     const bool wlive = live && mrun[0] > -INFINITY;
+    const float ofac = exp2i(24 - Ev), zfac = exp2i(-Ev), lfac = exp2i(re * VP1 - Ev);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int head = 4 * nt + tig;
-        float l = lrun[nt];
+        float l = lrun[nt] * lfac;
         l += __shfl_xor_sync(0xffffffffu, l, 4);
         l += __shfl_xor_sync(0xffffffffu, l, 8);
         l += __shfl_xor_sync(0xffffffffu, l, 16);
@@ -824,20 +971,20 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         for (int mt = 0; mt < MTV; ++mt) {
             const int gv = mt >> gvs;
             const float zsrc = gv < 8 ? oz01 : oz23;
-            const float oz = __shfl_sync(0xffffffffu, zsrc, (gv & 7) * 4 + tig);
+            const float oz = __shfl_sync(0xffffffffu, zsrc, (gv & 7) * 4 + tig) * zfac;
             if (head < gqa && wlive) {
                 const int c0 = 16 * mt + g;
-                cw[head * (D + 2) + c0] = (oacc[mt][nt][0] + oacc[mt][nt][1]) + oz;
-                cw[head * (D + 2) + c0 + 8] = (oacc[mt][nt][2] + oacc[mt][nt][3]) + oz;
+                cw[head * D + c0] = fmaf(oacc[mt][nt][0] + oacc[mt][nt][1], ofac, oz);
+                cw[head * D + c0 + 8] = fmaf(oacc[mt][nt][2] + oacc[mt][nt][3], ofac, oz);
             }
         }
         if (g == 0 && head < gqa) {
-            cw[head * (D + 2) + D] = wlive ? mrun[nt] : -INFINITY;
-            cw[head * (D + 2) + D + 1] = wlive ? l : 0.0f;
+            cml[2 * (warp * gqa + head)] = wlive ? mrun[nt] : -INFINITY;
+            cml[2 * (warp * gqa + head) + 1] = wlive ? l : 0.0f;
         }
     }
     __syncthreads();
-    combine_warps<D>(a, comb, red, b, h, item);
+    combine_warps<D>(a, comb, cml, red, b, h, item);
 }
 
 // One block per (item, kv head, sequence).  BITS == 0: no packed path (INT8 / FP8).

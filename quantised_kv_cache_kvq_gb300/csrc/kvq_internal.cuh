@@ -43,6 +43,9 @@ struct Layout {
 
 inline int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 
+// Streaming multiprocessors of the GB300 the decode work is sized for.
+constexpr int kNumSMs = 152;
+
 // How one decode step is split: every (sequence, kv head) "unit" gets NRC row chunks of
 // CHR tokens (the bf16 window for KIVI, all tokens for INT8/FP8) and NQ packed chunks of
 // CH tokens (KIVI groups), S = NRC + NQ work items in all.  A packed chunk is split among
@@ -66,13 +69,13 @@ __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const Decod
     o.red = off;   off += 4 * 32 * 4;                 // [warp][32] floats
     o.hstat = off; off += 2 * 32 * 4;                 // per-head max and sum
     o.qs = off;    off += (int64_t)lo.gqa * lo.D * 4; // scaled query, fp32
-    o.qpa = off;   off += (int64_t)4 * p.NT * 4 * (lo.D / 8) * 4;
-    o.qpb = off;   off += (int64_t)4 * p.NT * 4 * (lo.D / 8) * 4;
+    o.qpa = off;   off += (int64_t)32 * p.NT * (lo.D / 8 + 4) * 4;   // query tables: [32 NT][D/8 + 4]
+    o.qpb = off;   off += (int64_t)32 * p.NT * (lo.D / 8 + 4) * 4;
     o.pw = off;    off += 4 * 16 * 8 * 4;                // window path: [warp][token][head] p
     o.sc = off;
     {
         const int64_t rows_sc = (int64_t)lo.gqa * p.CHR;                // row path scores
-        const int64_t comb = (int64_t)4 * lo.gqa * (lo.D + 2);           // per-warp partials
+        const int64_t comb = (int64_t)4 * lo.gqa * (lo.D + 2);           // per-warp o and (m, l)
         const int64_t wsc = (int64_t)4 * 8 * p.NT * 32 * 2;              // per-warp tile scores
         int64_t big = rows_sc > comb ? rows_sc : comb;
         big = big > wsc ? big : wsc;
