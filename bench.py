@@ -113,6 +113,34 @@ def decode_bytes(w, n_tokens):
     return w.batch * H * (cache + qbytes)
 
 
+def sources_sha256():
+    """Digest of the CUDA sources (file names and contents) the library is built from."""
+    import hashlib
+    d = os.path.join(ROOT, "quantised_kv_cache_kvq_gb300", "csrc")
+    h = hashlib.sha256()
+    for n in sorted(os.listdir(d)):
+        h.update(n.encode())
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per decode launch (both kernels) from the committed ncu summary of this
+    workload; None without one, or when the kernels' sources changed since its capture."""
+    import re
+    try:
+        with open(os.path.join(ROOT, "profiles", "k_decode_%s.md" % workload)) as f:
+            text = f.read()
+    except OSError:
+        return None
+    t = re.search(r"^traffic_bytes_per_launch: (\d+)$", text, re.M)
+    h = re.search(r"^sources_sha256: ([0-9a-f]+)$", text, re.M)
+    if not (t and h) or h.group(1) != sources_sha256():
+        return None
+    return int(t.group(1))
+
+
 def max_over_ranks(values, world, device="cpu"):
     """Element-wise maximum of per-rank timings (the job is as slow as its slowest rank)."""
     if world <= 1:
@@ -404,7 +432,7 @@ def main():
         "hbm_gbs": step_gbs, "hbm_pct_of_peak": 100.0 * step_gbs / peak,
         "roofline": {"kernel": "kvq decode attention (split-context kernel + merge)", "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": None,
+                     "peak_kind": peak_kind, "traffic": profiled_traffic(w.name),
                      "avg_launch_us": 1e3 * dec_avg_ms,
                      "bytes_per_launch": r["bytes_decode"] / args.steps},
         "cpu_baseline": cpu,

@@ -139,6 +139,23 @@ def test_kivi_long_context_split():
     assert_close(out, ref, what="long context")
 
 
+@pytest.mark.parametrize("bits,D,G,Gv,batch,tokens", [
+    (2, 128, 32, 32, 2, 12200),    # several chunks per item, one stage
+    (2, 64, 16, 16, 8, 3000),      # several chunks per item, double-buffered stages
+    (4, 128, 128, 128, 1, 60000),  # long items (several chunks), warps sharing a group
+])
+def test_kivi_multi_chunk_items(bits, D, G, Gv, batch, tokens):
+    # enough packed chunks over all (sequence, kv head) units that the decode gives every
+    # block a run of chunks, with the online softmax carried across them
+    p = Pair("kivi", batch=batch, q_heads=32, kv_heads=8, head_dim=D, max_tokens=tokens + 100, bits=bits,
+             group_k=G, group_v=Gv, residual=128)
+    g = gen(bits * 7 + D + G)
+    k, v = p.rand_kv(batch, tokens, g)
+    p.append(0, k, v, n_valid=[tokens - 37 * i for i in range(batch)])
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="multi-chunk items")
+
+
 def test_kivi_peaky_attention_with_value_outliers():
     # large logits concentrate attention on few tokens, where value-outlier tokens (x8) and
     # key outlier channels stress the precision of the score and value contractions
