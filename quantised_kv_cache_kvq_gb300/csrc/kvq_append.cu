@@ -321,6 +321,7 @@ __device__ __forceinline__ int new_tokens(const AppendArgs& a, int bi) {
 // (an arrival counter in the sequence's state entry, zero at rest) writes the new ones.
 __global__ void __launch_bounds__(kThreads) k_append_small(AppendArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
+    grid_launch_dependents();   // a decode launched next may start launching (it waits for us)
     const Layout& lo = a.lo;
     const int h = blockIdx.x, bi = blockIdx.y, b = a.seq_begin + bi;
     int32_t* st = state_ptr(lo, a.cache, a.layer, b);

@@ -984,6 +984,7 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         }
     }
     __syncthreads();
+    grid_launch_dependents();   // the merge may start launching; it waits for this grid
     combine_warps<D>(a, comb, cml, red, b, h, item);
 }
 
@@ -991,6 +992,7 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
 template <int D, int BITS, int NT>
 __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2) k_decode(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
+    grid_dependency_wait();
     const int item = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int32_t* st = state_ptr(a.lo, a.cache, a.layer, b);
     const int64_t n = st[0], qn = st[1];
@@ -1015,8 +1017,9 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
             cudaSuccess)
         return KVQ_ERR_CUDA;
     dim3 grid(a.plan.S, a.lo.H, a.lo.B);
-    fn<<<grid, kDecodeThreads, a.plan.smem, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+    return launch_dependent(fn, grid, kDecodeThreads, static_cast<size_t>(a.plan.smem), stream, a) == cudaSuccess
+               ? KVQ_OK
+               : KVQ_ERR_CUDA;
 }
 
 // Dispatchers, one per translation unit.

@@ -5,74 +5,87 @@
 namespace kvq {
 namespace {
 
+constexpr int kMergeThreads = 256;
+
 // Combine the chunks of one (sequence, query head): with chunk i holding m_i (max score,
 // base 2), l_i = sum 2^(s - m_i) and o_i = sum 2^(s - m_i) v, the output is
-// sum_i o_i 2^(m_i - M) / sum_i l_i 2^(m_i - M), M = max_i m_i.  Warps take chunks in turn,
-// lanes hold D/32 channels each, four chunks in flight per warp.
+// sum_i o_i 2^(m_i - M) / sum_i l_i 2^(m_i - M), M = max_i m_i.  A block of 8 warps takes
+// 32 * nwc channels of one (sequence, query head): warp w holds channels 32 (w % nwc) + lane
+// and the chunks w / nwc + nwi * k, twelve per round, every load of a round issued before
+// any is used.  The host picks nwi (and nwc = 8 / nwi) so that most merges take one round.
 template <int D>
-__global__ void __launch_bounds__(128) k_merge(DecodeArgs a) {
-    constexpr int CPL = D / 32;
-    __shared__ float red[4];
-    __shared__ float part_o[4][D];
-    __shared__ float part_l[4];
+__global__ void __launch_bounds__(kMergeThreads) k_merge(DecodeArgs a, int nwc) {
+    constexpr int NW = kMergeThreads / 32, R = 12;
+    __shared__ float red_m[2][NW];
+    __shared__ float part_o[NW][32];
+    __shared__ float part_l[NW];
+    grid_dependency_wait();
     const Layout& lo = a.lo;
-    const int hq = blockIdx.x, b = blockIdx.y;
+    const int hq = blockIdx.y, b = blockIdx.z;
     const int h = hq / lo.gqa, head = hq % lo.gqa;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwi = NW / nwc, wc = warp % nwc, wi = warp / nwc;
     const int32_t* st = state_ptr(lo, a.cache, a.layer, b);
     const int64_t n = st[0], qn = st[1];
     const int S = a.plan.S;
     const float* ml = reinterpret_cast<const float*>(a.ws + a.plan.ws_ml_off);
     const float* o = reinterpret_cast<const float*>(a.ws + a.plan.ws_o_off);
     const int64_t slot0 = (((int64_t)b * lo.H + h) * S) * lo.gqa + head;   // + item * gqa
-    float mx = -INFINITY;
-    for (int it = tid; it < S; it += blockDim.x) {
-        const ItemRange r = item_range(lo, a.plan, it, n, qn);
-        if (r.t0 < r.t1) mx = fmaxf(mx, ml[2 * (slot0 + (int64_t)it * lo.gqa)]);
-    }
-    mx = warp_max(mx);
-    if (lane == 0) red[warp] = mx;
-    __syncthreads();
-    const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    float acc[CPL];
+    const int c = 32 * (blockIdx.x * nwc + wc) + lane;
+    float M = -INFINITY, acc = 0.0f, l = 0.0f;
+    const int rounds = (S + nwi * R - 1) / (nwi * R);     // the same in every warp (barriers inside)
+    for (int round = 0; round < rounds; ++round) {
+        const int it0 = wi + round * nwi * R;
+        float mv[R], lv[R], ov[R];
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) acc[e] = 0.0f;
-    float l = 0.0f;
-    for (int it0 = warp; it0 < S; it0 += 16) {
-        float w4[4];
-        float v4[4][CPL];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int it = it0 + 4 * k;
-            w4[k] = 0.0f;
-#pragma unroll
-            for (int e = 0; e < CPL; ++e) v4[k][e] = 0.0f;
+        for (int k = 0; k < R; ++k) {
+            const int it = it0 + nwi * k;
+            mv[k] = -INFINITY;
+            lv[k] = 0.0f;
+            ov[k] = 0.0f;
             if (it < S) {
                 const ItemRange r = item_range(lo, a.plan, it, n, qn);
                 if (r.t0 < r.t1) {
                     const int64_t sl = slot0 + (int64_t)it * lo.gqa;
                     const float2 mlv = *reinterpret_cast<const float2*>(ml + 2 * sl);
-                    w4[k] = fast_exp2(mlv.x - M);
-                    if (lane == 0) l = fmaf(mlv.y, w4[k], l);
-#pragma unroll
-                    for (int e = 0; e < CPL; ++e) v4[k][e] = o[sl * D + lane + 32 * e];
+                    mv[k] = mlv.y > 0.0f ? mlv.x : -INFINITY;
+                    lv[k] = mlv.y;
+                    ov[k] = o[sl * D + c];
                 }
             }
         }
+        // the round's maximum over the block (the same in every lane of a warp)
+        float mr = mv[0];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 1; k < R; ++k) mr = fmaxf(mr, mv[k]);
+        if (lane == 0) red_m[round & 1][warp] = mr;
+        __syncthreads();
 #pragma unroll
-            for (int e = 0; e < CPL; ++e) acc[e] = fmaf(v4[k][e], w4[k], acc[e]);
+        for (int w = 0; w < NW; ++w) mr = fmaxf(mr, red_m[round & 1][w]);
+        const float mnew = fmaxf(M, mr);
+        if (mnew > M && M > -INFINITY) {
+            const float f = fast_exp2(M - mnew);
+            acc *= f;
+            l *= f;
+        }
+        M = mnew;
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            const float w = lv[k] > 0.0f ? fast_exp2(mv[k] - M) : 0.0f;
+            acc = fmaf(ov[k], w, acc);
+            l = fmaf(lv[k], w, l);
+        }
     }
-#pragma unroll
-    for (int e = 0; e < CPL; ++e) part_o[warp][lane + 32 * e] = acc[e];
+    part_o[warp][lane] = acc;
     if (lane == 0) part_l[warp] = l;
     __syncthreads();
-    const float L = part_l[0] + part_l[1] + part_l[2] + part_l[3];
-    float* out = a.out + ((int64_t)b * lo.Hq + hq) * D;
-    for (int d = tid; d < D; d += blockDim.x) {
-        const float v = part_o[0][d] + part_o[1][d] + part_o[2][d] + part_o[3][d];
-        out[d] = L > 0.0f ? v / L : 0.0f;
+    if (wi == 0) {
+        float L = 0.0f, v = 0.0f;
+        for (int j = 0; j < nwi; ++j) {
+            L += part_l[j * nwc + wc];
+            v += part_o[j * nwc + wc][lane];
+        }
+        a.out[((int64_t)b * lo.Hq + hq) * D + c] = L > 0.0f ? v / L : 0.0f;
     }
 }
 
@@ -108,14 +121,24 @@ int launch_decode(const Layout& lo, const DecodePlan& plan, const uint8_t* cache
         rc = launch_decode_rows(a, stream);
     }
     if (rc != KVQ_OK) return rc;
-    const dim3 mgrid(lo.Hq, lo.B);
-    switch (lo.D) {
-        case 32: k_merge<32><<<mgrid, 128, 0, stream>>>(a); break;
-        case 64: k_merge<64><<<mgrid, 128, 0, stream>>>(a); break;
-        case 128: k_merge<128><<<mgrid, 128, 0, stream>>>(a); break;
-        default: k_merge<256><<<mgrid, 128, 0, stream>>>(a); break;
+    // warps over chunks: enough for one round of 12 chunks each (at most all 8), the rest
+    // of the block's warps over channels (at most D / 32)
+    int nwi = 1;
+    while (nwi < kMergeThreads / 32 && nwi * 12 < plan.S) nwi *= 2;
+    int nwc = kMergeThreads / 32 / nwi;
+    if (nwc > lo.D / 32) {
+        nwc = lo.D / 32;
+        nwi = kMergeThreads / 32 / nwc;
     }
-    return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+    const dim3 mgrid(lo.D / (32 * nwc), lo.Hq, lo.B);
+    cudaError_t e;
+    switch (lo.D) {
+        case 32: e = launch_dependent(k_merge<32>, mgrid, kMergeThreads, 0, stream, a, nwc); break;
+        case 64: e = launch_dependent(k_merge<64>, mgrid, kMergeThreads, 0, stream, a, nwc); break;
+        case 128: e = launch_dependent(k_merge<128>, mgrid, kMergeThreads, 0, stream, a, nwc); break;
+        default: e = launch_dependent(k_merge<256>, mgrid, kMergeThreads, 0, stream, a, nwc); break;
+    }
+    return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 }  // namespace kvq
