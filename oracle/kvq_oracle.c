@@ -271,10 +271,12 @@ void kvqo_int8_token(const float* x, int n, float* scale_out, int8_t* codes)
  *          no call is running, at byte 16 * (l * batch + b).
  *   KIVI:  group records, one per (l, b, kv head h, group slot g), NG = (T - R) / G slots:
  *            K codes  G*D*b/8 bytes, token-major: (token t, channel c) at bit (t*D + c)*b
- *            V codes  D*G*b/8 bytes, channel-major: (channel c, token t) at bit (c*G + t)*b
+ *            V codes  D*G*b/8 bytes of 32-bit words [token word][channel column] (see
+ *                     vcode_bit: each 16-token tile is laid out so that the two halves of
+ *                     a word hold tokens tt and tt + 8 of the tile)
  *            K params 4*D bytes: fp16 scale[D], then fp16 zero[D]
- *            V params 4*G*NGv bytes: for token t and value group j, fp16 scale then fp16
- *                     zero at byte 4 * (t*NGv + j)
+ *            V params 4*G*NGv bytes: fp16 scale[NGv][G], then fp16 zero[NGv][G], the G
+ *                     tokens of a value group in tile order (see vparam_byte)
  *          then the bf16 ring: (l, b, h, slot s) holds K row[D] then V row[D], C = R + G
  *          slots; token t (qn <= t < n) sits in slot t mod C.
  *   INT8:  per (l, b, h) block over T16 = T rounded up to 16:
@@ -290,6 +292,32 @@ typedef struct {
 } layout_t;
 
 static int64_t up256(int64_t x) { return (x + 255) / 256 * 256; }
+
+/* Bit index, within a record's value codes, of the code of token t (0 <= t < G) and
+ * channel ch.  Codes sit in 32-bit words, tpw = 32 / bits tokens per word, hw = tpw / 2 per
+ * 16-bit half, bits / 2 words per 16-token tile.  Token tt of a tile lies in half tt / 8
+ * (so a word's halves hold tokens tt and tt + 8), word (tt mod 8) / hw of the tile, at bit
+ * bits * ((tt mod 8) mod hw) of the half.  Words are stored [token word tw][column], D
+ * columns per token word; for bits >= 4 odd token words store channel ch in column
+ * ch XOR 8 (tiles then span several words). */
+static int64_t vcode_bit(int64_t D, int bits, int64_t t, int64_t ch)
+{
+    int64_t hw = 16 / bits, wpt = bits / 2;
+    int64_t tile = t / 16, tt = t % 16, half = tt / 8, w = (tt % 8) / hw, i = (tt % 8) % hw;
+    int64_t tw = tile * wpt + w;
+    int64_t col = bits >= 4 && (tw & 1) ? (ch ^ 8) : ch;
+    return (tw * D + col) * 32 + 16 * half + bits * i;
+}
+
+/* Byte offset, within a record's value parameters, of the fp16 scale of token t
+ * (0 <= t < G) and value group j; the zero is 2 * G * NGv bytes further.  Within each
+ * 16-token tile token tt sits at position 2 * (tt mod 8) + tt / 8, so tokens tt and tt + 8
+ * are neighbours. */
+static int64_t vparam_byte(int64_t G, int64_t j, int64_t t)
+{
+    int64_t tt = t % 16;
+    return 2 * (j * G + (t - tt) + 2 * (tt % 8) + tt / 8);
+}
 
 static layout_t make_layout(const kvqo_config* c)
 {
@@ -446,11 +474,11 @@ static void kivi_quantise_group(const kvqo_config* c, const layout_t* L, uint8_t
         for (int j = 0; j < ngv; j++) {
             uint16_t s, z;
             kvqo_qb_group(V + (int64_t)i * D + (int64_t)j * Gv, Gv, 1, bits, &s, &z, codes);
-            put_u16(vpar + 4 * (i * ngv + j), s);
-            put_u16(vpar + 4 * (i * ngv + j) + 2, z);
+            put_u16(vpar + vparam_byte(G, j, i), s);
+            put_u16(vpar + 2 * (int64_t)G * ngv + vparam_byte(G, j, i), z);
             for (int cc = 0; cc < Gv; cc++) {
                 int ch = j * Gv + cc;
-                put_bits(vcodes, ((int64_t)ch * G + i) * bits, bits, codes[cc]);
+                put_bits(vcodes, vcode_bit(D, bits, i, ch), bits, codes[cc]);
             }
         }
     }
@@ -612,10 +640,10 @@ void kvqo_dequant_token(const kvqo_config* c, const uint8_t* img, int l, int b, 
             for (int ch = 0; ch < D; ch++) {
                 int kc = get_bits(rec, ((int64_t)i * D + ch) * bits, bits);
                 kout[ch] = kvqo_qb_dequant(kc, get_u16(kpar + 2 * ch), get_u16(kpar + 2 * D + 2 * ch));
-                int vc = get_bits(rec + L.kc, ((int64_t)ch * G + i) * bits, bits);
+                int vc = get_bits(rec + L.kc, vcode_bit(D, bits, i, ch), bits);
                 int j = ch / Gv;
-                vout[ch] = kvqo_qb_dequant(vc, get_u16(vpar + 4 * (i * L.ngv + j)),
-                                           get_u16(vpar + 4 * (i * L.ngv + j) + 2));
+                vout[ch] = kvqo_qb_dequant(vc, get_u16(vpar + vparam_byte(G, j, i)),
+                                           get_u16(vpar + 2 * (int64_t)G * L.ngv + vparam_byte(G, j, i)));
             }
         } else {
             int64_t u = ((int64_t)l * c->batch + b) * c->kv_heads + h;

@@ -184,8 +184,11 @@ __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int 
             QbParams p = qb_params(mn, mx, flevels);
             const int gv = (lane * cpl) / Gv;
             if ((lane % lpg) == 0) {
-                vpar[2 * (i * lo.NGv + gv)] = p.s;
-                vpar[2 * (i * lo.NGv + gv) + 1] = p.z;
+                // scale[gv][G] then zero[gv][G], tokens of a 16-token tile in the order
+                // 0, 8, 1, 9, ...
+                const int tt = i % 16, pos = gv * G + (i - tt) + 2 * (tt % 8) + tt / 8;
+                vpar[pos] = p.s;
+                vpar[G * lo.NGv + pos] = p.z;
             }
             // channel-major staging: code of (channel c, token i) at c*G + i
             for (int e = 0; e < cpl; ++e)
@@ -193,15 +196,25 @@ __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int 
         }
     }
     __syncthreads();
+    // value codes: 32-bit words [token word][column], D columns per token word.  A word's
+    // 16-bit halves hold tokens tt and tt + 8 of a 16-token tile, hw = 16 / bits codes per
+    // half; bits / 2 words per tile; for bits >= 4 odd token words keep channel c in column
+    // c ^ 8 (the decode's lanes then read distinct shared-memory banks)
     {
-        uint8_t* vrec = rec + lo.kc;
-        const int per16 = 128 / bits;
-        const int chunks = G * D / per16;
-        for (int k = threadIdx.x; k < chunks; k += blockDim.x) {
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
-            const uint8_t* src = codes + k * per16;
-            for (int e = 0; e < per16; ++e) w[(e * bits) >> 5] |= static_cast<uint32_t>(src[e]) << ((e * bits) & 31);
-            reinterpret_cast<uint4*>(vrec)[k] = make_uint4(w[0], w[1], w[2], w[3]);
+        uint32_t* vrec = reinterpret_cast<uint32_t*>(rec + lo.kc);
+        const int hw = 16 / bits, wpt = bits / 2;
+        const int words = (G / 16) * wpt * D;
+        for (int k = threadIdx.x; k < words; k += blockDim.x) {
+            const int tw = k / D, col = k % D;
+            const int ch = (bits >= 4 && (tw & 1)) ? (col ^ 8) : col;
+            const int t0w = (tw / wpt) * 16 + (tw % wpt) * hw;   // first token of the low half
+            const uint8_t* src = codes + ch * G;
+            uint32_t w = 0u;
+            for (int e = 0; e < hw; ++e) {
+                w |= static_cast<uint32_t>(src[t0w + e]) << (bits * e);
+                w |= static_cast<uint32_t>(src[t0w + 8 + e]) << (16 + bits * e);
+            }
+            vrec[k] = w;
         }
     }
     __syncthreads();

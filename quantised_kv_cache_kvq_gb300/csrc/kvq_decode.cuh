@@ -13,14 +13,15 @@
 // asynchronous copy, then both contractions run on the tensor cores with operands built
 // in registers:
 //   scores  S[token][col] = sum_c code[token][c] * Bq[c][col], A = 2/4/8-bit key codes
-//           turned into exact fp16 integers, Bq = (query * per-channel key scale) split
+//           turned into exact fp16 subnormals (code * 2^(p - 24), powers of two undone
+//           exactly on the other operand and the result), Bq = (query * per-channel key scale) split
 //           into an fp16 major part and an fp16 minor part (cols 2h, 2h+1), so the fp32
 //           accumulator sees the product to ~22 bits; the per-group offset term
 //           sum_c q_c * zero_c is added in fp32.  (Q_b equation: xhat = code*s + min.)
-//   values  O[c][col] = sum_t code[t][c] * Bp[t][col], A = value codes (stored
-//           channel-major so one 32-bit word holds a channel's consecutive tokens),
-//           Bp = p_t * value scale split into major/minor parts; the offset term
-//           sum_t p_t * zero_t is added in fp32.
+//   values  O[c][col] = sum_t code[t][c] * Bp[t][col], A = value codes (stored as
+//           32-bit words [token word][channel], the halves of a word holding tokens tt
+//           and tt + 8 of a tile), Bp = p_t * value scale split into major/minor parts;
+//           the offset term sum_t p_t * zero_t is one more small product.
 // The bf16 window (KIVI), INT8 rows and FP8 rows go through a CUDA-core row path.
 #pragma once
 
@@ -628,26 +629,28 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     const uint32_t vpar = kpar + lo.kp;                     // value params in a record
     const uint32_t kscale_lane = kpar + tig * (D / 2);      // the lane's quarter of the key scales
     const uint32_t kzero_lane = kscale_lane + 2 * D;
-    // token order of the score tile rows: lane (g, tig) scores tokens rho0 = rho(g) and
-    // rho1 = rho(g + 8) of each 16-token tile, chosen so that the value fragment of lane
-    // (g', t') needs the pairs held by lanes (2t', h') and (2t' + 1, h') (h' = g' / 2)
-    const int rt = g >> 1;
-    const int rho0 = (2 * rt) / HW * TPW + (2 * rt) % HW + re;
-    const int rho1 = rho0 + HW;
-    const uint32_t krow0 = rho0 * ROWB + tig * (ROWW * 4), krow1 = rho1 * ROWB + tig * (ROWW * 4);
-    // this lane's value-fragment tokens of a tile (k slots 2t, 2t+1, 2t+8, 2t+9): tA, tB
-    // at value-word position vj0 (low, high half), tC, tD at vj0 + 1; the lane shifts its
-    // value words right by BITS * vj0 so the pairs sit at bits 0 and BITS
-    const int vwi = (2 * tig) / HW, vj0 = (2 * tig) % HW;
-    const int tA = vwi * TPW + vj0, tB = tA + HW, tC = tA + 1, tD = tB + 1;
-    const uint32_t vsh = BITS * vj0;
-    const uint32_t cstride = static_cast<uint32_t>(G * BITS / 8);     // bytes of one channel's value codes
-    const uint32_t vcode_lane = lo.kc + g * cstride + vwi * 4;
-    const uint32_t oA = 4 * tA * NGv, oB = 4 * tB * NGv, oC = 4 * tC * NGv, oD = 4 * tD * NGv;
+    // score tile rows: lane (g, tig) scores tokens g and g + 8 of each 16-token tile, so the
+    // lane pair (2t', h') and (2t' + 1, h') holds the tokens of the value fragment of lane
+    // (g', t') (h' = g' / 2): 2t' and 2t' + 8 (k slots 2t', 2t' + 1), 2t' + 1 and 2t' + 9
+    // (k slots 2t' + 8, 2t' + 9)
+    const uint32_t krow0 = g * ROWB + tig * (ROWW * 4), krow1 = (g + 8) * ROWB + tig * (ROWW * 4);
+    // value codes of a tile: BITS / 2 token words, each with the tile's tokens tt and tt + 8
+    // in its two halves; this lane's tokens 2t, 2t + 8 and 2t + 1, 2t + 9 sit in word vwi at
+    // bits BITS * i0 and BITS * (i0 + 1) of each half: a right shift by BITS * i0 brings
+    // them to bits 0 and BITS.  Odd token words (BITS >= 4) keep channel c in column c ^ 8.
+    const int vwi = (2 * tig) / HW, i0 = (2 * tig) % HW;
+    const uint32_t vsh = BITS * i0;
+    const uint32_t vswz = (BITS >= 4 && (vwi & 1)) ? 8u : 0u;
+    const uint32_t vcol0 = 4 * (g ^ vswz), vcol1 = 4 * ((g + 8) ^ vswz);
+    const uint32_t vword_lane = lo.kc + vwi * 4 * D;
+    // value scales and zeros: [group][G] fp16 with tile token tt at position 2 (tt mod 8) +
+    // tt / 8, so this lane's four tokens are the 8 bytes at tile position 4t
+    const uint32_t vscale_lane = vpar + 8 * tig;
+    const uint32_t vzero_lane = vpar + 2 * G * NGv + 8 * tig;
     const int src1 = (2 * tig) * 4 + (g >> 1), src2 = (2 * tig + 1) * 4 + (g >> 1);
     const uint32_t pmask = part ? 0xffffffffu : 0u;
-    const uint32_t zg = g < NGv ? 4 * g : 0u, zmask = g < NGv ? 0xffffffffu : 0u;
-    const uint32_t zg8 = g + 8 < NGv ? 4 * (g + 8) : 0u, zmask8 = g + 8 < NGv ? 0xffffffffu : 0u;
+    const uint32_t zg = g < NGv ? 2 * G * g : 0u, zmask = g < NGv ? 0xffffffffu : 0u;
+    const uint32_t zg8 = g + 8 < NGv ? 2 * G * (g + 8) : 0u, zmask8 = g + 8 < NGv ? 0xffffffffu : 0u;
     const int gvs = __ffs(lo.Gv) - 5;       // value groups are powers of two >= 16
 
     float mrun[NT], lrun[NT];
@@ -730,13 +733,20 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                     {
                         uint32_t sreg[D / 8];
                         lds_words<D / 8>(ro + kscale_lane, sreg);
-                        __half2 mx = u32_as_h2(sreg[0]);
+                        // the group's largest key scale (scales are >= 0, so fp16 bit patterns
+                        // order as integers): each lane takes D / 32 of the D scales
+                        uint32_t mb;
+                        {
+                            uint32_t part_w[D / 64];
+                            lds_words<D / 64>(ro + kpar + lane * (D / 16), part_w);
+                            __half2 mx = u32_as_h2(part_w[0]);
 #pragma unroll
-                        for (int k = 1; k < D / 8; ++k) mx = __hmax2(mx, u32_as_h2(sreg[k]));
-                        uint32_t mb = h2_as_u32(mx);
-                        mb = max(mb & 0xffffu, mb >> 16);
-                        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-                        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+                            for (int k = 1; k < D / 64; ++k) mx = __hmax2(mx, u32_as_h2(part_w[k]));
+                            mb = h2_as_u32(mx);
+                            mb = max(mb & 0xffffu, mb >> 16);
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+                        }
                         const int E = min(15, 29 - static_cast<int>((mb >> 10) & 31u));
                         kf = exp2i(24 - E) * qup;
                         __half2 sp[NPAIR];
@@ -797,26 +807,20 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                     ++grp;
                 }
             }
-            // value-scale exponent: the largest value scale of the warp's tokens in this
-            // chunk must stay below 2^(15 - Ev); lower Ev (and rescale) when it does not
+            // value-scale exponent: the largest value scale of the records the warp's tokens
+            // lie in must stay below 2^(15 - Ev); lower Ev (and rescale) when it does not
             {
-                // (the warp's tokens are a multiple of 16 per record: whole 16-byte runs of
-                // (scale, zero) pairs; the scale is the low half of each word)
                 uint32_t smx = 0;
-                int t = ti0, rem = wtok;
-                uint32_t r = st0;
+                const int nrec = (ti0 + wtok + G - 1) / G;
+                const int nv = NGv * G / 8;      // 16-byte runs of value scales per record
 #pragma unroll 1
-                while (rem > 0) {
-                    const int n = min(rem, G - t);
-                    const uint32_t base = r + vpar + 4 * t * NGv;
-#pragma unroll 1
-                    for (int k = 4 * lane; k < n * NGv; k += 128) {
-                        const uint4 v = lds128(base + 4 * k);
-                        smx = max(smx, max(max(v.x & 0xffffu, v.y & 0xffffu), max(v.z & 0xffffu, v.w & 0xffffu)));
-                    }
-                    rem -= n;
-                    t = 0;
-                    r += rec;
+                for (int k = lane; k < nrec * nv; k += 32) {
+                    const int r = k / nv, o = k - r * nv;
+                    const uint4 v = lds128(st0 + r * rec + vpar + 16 * o);
+                    const __half2 m2 = __hmax2(__hmax2(u32_as_h2(v.x), u32_as_h2(v.y)),
+                                               __hmax2(u32_as_h2(v.z), u32_as_h2(v.w)));
+                    const uint32_t mb = h2_as_u32(m2);
+                    smx = max(smx, max(mb & 0xffffu, mb >> 16));
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) smx = max(smx, __shfl_xor_sync(0xffffffffu, smx, o));
@@ -895,33 +899,33 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                             py2[nt] = part ? y2 : x2;
                         }
                         // values: O[c][col] += sum_t code[t][c] * (p'_t * scale[t][gv(c)]); the
-                        // offset term OZ[gv][col] += sum_t zero[t][gv] * p_t
-                        const uint32_t vpt = ro + vpar + 4 * ti * NGv;
-                        // zero pairs of value groups g and g + 8 (rows of the offset product);
-                        // lanes past the last group read group 0 and mask it out
-                        const uint32_t zA = prmt(lds32(vpt + oA + zg), lds32(vpt + oB + zg), 0x7632u) & zmask;
-                        const uint32_t zC = prmt(lds32(vpt + oC + zg), lds32(vpt + oD + zg), 0x7632u) & zmask;
+                        // offset term OZ[gv][col] += sum_t zero[t][gv] * p_t.  Zero pairs of value
+                        // groups g and g + 8 (rows of the offset product); lanes past the last
+                        // group read group 0 and mask it out.
+                        const uint2 z2 = lds64(ro + vzero_lane + 2 * ti + zg);
+                        const uint32_t zA = z2.x & zmask, zC = z2.y & zmask;
                         uint32_t zA8 = 0u, zC8 = 0u;
                         if constexpr (D > 128) {
-                            zA8 = prmt(lds32(vpt + oA + zg8), lds32(vpt + oB + zg8), 0x7632u) & zmask8;
-                            zC8 = prmt(lds32(vpt + oC + zg8), lds32(vpt + oD + zg8), 0x7632u) & zmask8;
+                            const uint2 z8 = lds64(ro + vzero_lane + 2 * ti + zg8);
+                            zA8 = z8.x & zmask8;
+                            zC8 = z8.y & zmask8;
                         }
-                        const uint32_t vct = ro + vcode_lane + ti * BITS / 8;
+                        const uint32_t vsc = ro + vscale_lane + 2 * ti;
+                        const uint32_t vrow = ro + vword_lane + (ti / 16) * (BITS / 2) * 4 * D;
                         uint32_t bv[NT][2];
 #pragma unroll
                         for (int q = 0; q < MTV; ++q) {
                             if ((q & QM) == 0) {
                                 const int gv = q >> GVS;
-                                const __half2 s01 = u32_as_h2(prmt(lds32(vpt + oA + 4 * gv), lds32(vpt + oB + 4 * gv), 0x5410u));
-                                const __half2 s23 = u32_as_h2(prmt(lds32(vpt + oC + 4 * gv), lds32(vpt + oD + 4 * gv), 0x5410u));
+                                const uint2 sc = lds64(vsc + 2 * G * gv);
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt) {
-                                    bv[nt][0] = split_mul(s01, px1[nt], py1[nt]);
-                                    bv[nt][1] = split_mul(s23, px2[nt], py2[nt]);
+                                    bv[nt][0] = split_mul(u32_as_h2(sc.x), px1[nt], py1[nt]);
+                                    bv[nt][1] = split_mul(u32_as_h2(sc.y), px2[nt], py2[nt]);
                                 }
                             }
-                            const uint32_t w0 = lds32(vct + (16 * q) * cstride) >> vsh;
-                            const uint32_t w1 = lds32(vct + (16 * q + 8) * cstride) >> vsh;
+                            const uint32_t w0 = lds32(vrow + vcol0 + 64 * q) >> vsh;
+                            const uint32_t w1 = lds32(vrow + vcol1 + 64 * q) >> vsh;
                             uint32_t af[4];
                             af[0] = code_bits<BITS>(w0, 0);
                             af[1] = code_bits<BITS>(w1, 0);

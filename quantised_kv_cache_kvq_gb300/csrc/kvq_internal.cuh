@@ -11,10 +11,15 @@
 //            everything a decode block needs for G tokens, so a run of groups is one
 //            contiguous span (one bulk copy):
 //              K codes  G*D*b/8 B, token-major: (token t, channel c) at bit (t*D + c)*b
-//              V codes  D*G*b/8 B, channel-major: (channel c, token t) at bit (c*G + t)*b
+//              V codes  D*G*b/8 B of 32-bit words [token word][column], D columns per
+//                       token word, 32/b tokens per word: in each 16-token tile, token tt
+//                       lies in half tt / 8 (a word's halves hold tokens tt and tt + 8),
+//                       word (tt mod 8) / (16/b) of the tile's b/2 words, at bit
+//                       b * ((tt mod 8) mod (16/b)) of the half; for b >= 4, odd token
+//                       words keep channel c in column c ^ 8
 //              K params 4*D B: fp16 scale[D] then fp16 zero[D] (per channel, "min")
-//              V params 4*G*(D/Gv) B: for token t and value group j, fp16 scale then fp16
-//                       zero at byte 4*(t*(D/Gv) + j)
+//              V params 4*G*(D/Gv) B: fp16 scale[D/Gv][G] then fp16 zero[D/Gv][G], tile
+//                       token tt of a group's row at position 2 (tt mod 8) + tt / 8
 //            then the bf16 window ("ring"): per (layer, sequence, kv head) C = R + G slots
 //            of [K row bf16[D], V row bf16[D]]; token t (qn <= t < n) lives in slot t % C.
 //   INT8     per (layer, sequence, kv head), T16 = max_tokens rounded up to 16:

@@ -436,6 +436,28 @@ def test_layout_golden_record():
     assert img.regions()["unit"] == 16 * 64 * 2 // 8 * 2 + 4 * 64 + 4 * 16 * 4
 
 
+def test_layout_golden_record_4bit_tile_order():
+    cfg = O.make_config(scheme=0, batch=1, kv_heads=1, q_heads=1, head_dim=64, bits=4, group_k=16,
+                        group_v=16, residual=0, max_tokens=16)
+    img = O.Image(cfg)
+    t = np.arange(16)[:, None]
+    c = np.arange(64)[None, :]
+    K = ((c + t) % 16).astype(np.float32)
+    V = (((c + t) % 16) * np.where(t >= 8, 2, 1)).astype(np.float32)
+    kb = _bf16_bits(torch.tensor(K).to(torch.bfloat16)).reshape(1, 16, 1, 64)
+    vb = _bf16_bits(torch.tensor(V).to(torch.bfloat16)).reshape(1, 16, 1, 64)
+    assert img.append(0, 0, kb, vb) == 0
+    rec = img.buf[img.regions()["data"]:]
+    rows = _golden("layout_kivi4.txt")
+    assert len(rows) >= 25
+    for off, byte in rows:
+        assert rec[int(off)] == int(byte, 16), off
+    # every value code reads back as (c + t) mod 16 through the oracle's own dequantiser
+    for tok in range(16):
+        _, vt = img.dequant_token(0, 0, 0, tok)
+        assert np.array_equal(vt, V[tok]), tok
+
+
 def test_packed_tokens_dequantise_to_their_groups():
     # keys: Q_b per channel over the G tokens of the group; values: Q_b per token over each Gv
     # block of channels ("Per-channel and per-token grouping"; KIVI "How It Works")
