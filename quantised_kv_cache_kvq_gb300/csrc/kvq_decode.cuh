@@ -560,7 +560,8 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     const int nstage = a.plan.NSTAGE;
     const uint32_t rec = static_cast<uint32_t>(lo.rec);
     const uint32_t stage_bytes = static_cast<uint32_t>(CH / G) * rec;
-    const int nch = static_cast<int>((t1 - t0 + CH - 1) / CH);
+    const int ntok = static_cast<int>(t1 - t0);
+    const int nch = (ntok + CH - 1) / CH;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + so.bar);
     float* red = reinterpret_cast<float*>(smem + so.red);
     float* qs = reinterpret_cast<float*>(smem + so.qs);
@@ -571,13 +572,17 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     const int64_t u = unit_index(lo, a.layer, b, h);
     const uint8_t* src_unit = a.cache + lo.data_off + u * lo.unit;
 
+    // the item's groups (t0 and t1 are group boundaries): chunk j holds gpc of them
+    const int gpc = CH / G;
+    const uint8_t* src_groups = src_unit + (t0 / G) * (int64_t)rec;
+    const int ngroups = ntok / G;
     auto issue = [&](int j) {       // stage chunk j (thread 0 only)
-        const int64_t c0 = t0 + (int64_t)j * CH;
-        const int64_t ctok = (t1 - c0) < CH ? (t1 - c0) : CH;
-        const uint32_t bytes = static_cast<uint32_t>(ctok / G) * rec;
-        uint64_t* bar = bars + (j % nstage);
+        const int gj = min(gpc, ngroups - j * gpc);
+        const uint32_t bytes = static_cast<uint32_t>(gj) * rec;
+        const int sj = nstage == 2 ? (j & 1) : 0;   // stage of chunk j
+        uint64_t* bar = bars + sj;
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_copy_pieces(smem + so.data + (j % nstage) * stage_bytes, src_unit + (c0 / G) * (int64_t)rec, bytes, bar);
+        bulk_copy_pieces(smem + so.data + sj * stage_bytes, src_groups + (int64_t)j * gpc * rec, bytes, bar);
     };
     if (tid == 0) {
         for (int s2 = 0; s2 < nstage; ++s2) mbar_init(bars + s2, 1);
@@ -591,10 +596,39 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     // overflow, and per-lane tables of the query in the lanes' key-pair order split into
     // fp16 major + minor parts: row 32 * nt + lane holds x = (0 | major) and y = (major |
     // minor) for B column g = 2 * head + part of that lane (split_mul)
-    load_query(a, b, h, qs);
-    __syncthreads();
     float qmax = 0.0f;
-    for (int i = tid; i < gqa * D; i += blockDim.x) qmax = fmaxf(qmax, fabsf(qs[i]));
+    {
+        // scaled query of the kv head's gqa query heads into shared fp32, vector loads
+        const int64_t base = ((int64_t)b * lo.Hq + (int64_t)h * gqa) * D;
+        if (lo.dtype == KVQ_DTYPE_BF16) {
+            const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + base);
+            for (int i = tid; i < gqa * D / 8; i += blockDim.x) {
+                const uint4 v = src[i];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    f[2 * e] = __uint_as_float(w[e] << 16) * a.qscale;
+                    f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u) * a.qscale;
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) qmax = fmaxf(qmax, fabsf(f[e]));
+                reinterpret_cast<float4*>(qs)[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
+                reinterpret_cast<float4*>(qs)[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
+            }
+        } else {
+            const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.q) + base);
+            for (int i = tid; i < gqa * D / 4; i += blockDim.x) {
+                float4 v = src[i];
+                v.x *= a.qscale;
+                v.y *= a.qscale;
+                v.z *= a.qscale;
+                v.w *= a.qscale;
+                qmax = fmaxf(fmaxf(qmax, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+                reinterpret_cast<float4*>(qs)[i] = v;
+            }
+        }
+    }
     qmax = warp_max(qmax);
     if (lane == 0) red[warp * 32] = qmax;
     __syncthreads();
@@ -602,9 +636,11 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     int qexp = 0;
     if (qmax > 0.0f) frexpf(qmax, &qexp);
     const float qdown = ldexpf(1.0f, -qexp), qup = ldexpf(1.0f, qexp);
-    for (int i = tid; i < 32 * NT * NPAIR; i += blockDim.x) {
-        const int m = i % NPAIR, row = i / NPAIR;
-        const int ln = row & 31, hh = 4 * (row >> 5) + (ln >> 3), pt = (ln >> 2) & 1, tg = ln & 3;
+    // one entry per (head hh, lane quarter tg, key pair m), written to the rows of the two
+    // lanes (parts) of B columns 2 (hh mod 4) and 2 (hh mod 4) + 1
+    for (int i = tid; i < 16 * NT * NPAIR; i += blockDim.x) {
+        const int m = i % NPAIR, r = i / NPAIR;
+        const int hh = r >> 2, tg = r & 3;
         const int wi = m / HPW, jj = m % HPW;
         const int clo = tg * (D / 4) + wi * CPW + jj, chi = clo + HPW;
         float vlo = 0.0f, vhi = 0.0f;
@@ -615,8 +651,11 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         const __half2 major = __floats2half2_rn(vlo, vhi);
         const float2 mf = __half22float2(major);
         const uint32_t mj = h2_as_u32(major), mn = h2_as_u32(__floats2half2_rn(vlo - mf.x, vhi - mf.y));
-        qx[row * QROW + m] = pt ? mj : 0u;
-        qy[row * QROW + m] = pt ? mn : mj;
+        const int row0 = 32 * (hh >> 2) + 8 * (hh & 3) + tg;   // lane of part 0; part 1 is 4 lanes on
+        qx[row0 * QROW + m] = 0u;
+        qy[row0 * QROW + m] = mj;
+        qx[(row0 + 4) * QROW + m] = mj;
+        qy[(row0 + 4) * QROW + m] = mn;
     }
     __syncthreads();
 
@@ -666,29 +705,31 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     }
     int Ev = 15;
     bool live = true;
+    // the warp's tokens start W * warp tokens into every chunk: group g0 of the chunk's
+    // records, offset ti0 in it (a group may be shared by two warps)
+    const int g0 = (warp * W) / G, ti0 = (warp * W) % G;
     for (int j = 0; j < nch; ++j) {
-        bool ok = mbar_wait_bounded(bars + (j % nstage), (j / nstage) & 1, kWaitLimit);
+        const int sj = nstage == 2 ? (j & 1) : 0;                       // stage of chunk j
+        const uint32_t par = nstage == 2 ? ((j >> 1) & 1) : (j & 1);    // its barrier phase
+        bool ok = mbar_wait_bounded(bars + sj, par, kWaitLimit);
         ok = __syncthreads_and(ok);
         if (!ok) {
             if (tid == 0) atomicOr(reinterpret_cast<uint32_t*>(a.ws), KVQ_STATUS_TIMEOUT);
-            mbar_wait_bounded(bars + (j % nstage), (j / nstage) & 1, kWaitLimit);
+            mbar_wait_bounded(bars + sj, par, kWaitLimit);
             live = false;
             break;
         }
-        const int64_t c0 = t0 + (int64_t)j * CH;
-        const int ctok = static_cast<int>((t1 - c0) < CH ? (t1 - c0) : CH);
+        const int ctok = min(ntok - j * CH, CH);
         const int wtok = ctok - warp * W < 0 ? 0 : (ctok - warp * W > W ? W : ctok - warp * W);   // multiple of 16
-        // the warp's tokens start W * warp tokens into the chunk: group g0 of the chunk's
-        // records, offset ti0 in it (a group may be shared by two warps)
-        const int g0 = (warp * W) / G, ti0 = (warp * W) % G;
-        const uint32_t st0 = sbase + static_cast<uint32_t>(so.data) + (j % nstage) * stage_bytes + g0 * rec;
+        const uint32_t st0 = sbase + static_cast<uint32_t>(so.data) + sj * stage_bytes + g0 * rec;
+        int ngrp = 0;                                  // groups the warp's tokens touch (<= 8)
+        for (int x = ti0 + wtok; x > 0; x -= G) ++ngrp;
         if (wtok > 0) {
             const int ntl = wtok >> 4;
             // offset term of every group of the warp: cst[group][head] = sum_c q_c zero_c,
             // as one small tensor-core product (rows = groups, k = channels in pair order)
             float cstf[NT][4];
             {
-                const int ngrp = (ti0 + wtok + G - 1) / G;   // groups the warp's tokens touch (<= 8)
                 uint32_t zreg[D / 8];
                 if (g < ngrp) {
                     lds_words<D / 8>(st0 + g * rec + kzero_lane, zreg);
@@ -811,16 +852,17 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
             // lie in must stay below 2^(15 - Ev); lower Ev (and rescale) when it does not
             {
                 uint32_t smx = 0;
-                const int nrec = (ti0 + wtok + G - 1) / G;
                 const int nv = NGv * G / 8;      // 16-byte runs of value scales per record
 #pragma unroll 1
-                for (int k = lane; k < nrec * nv; k += 32) {
-                    const int r = k / nv, o = k - r * nv;
-                    const uint4 v = lds128(st0 + r * rec + vpar + 16 * o);
-                    const __half2 m2 = __hmax2(__hmax2(u32_as_h2(v.x), u32_as_h2(v.y)),
-                                               __hmax2(u32_as_h2(v.z), u32_as_h2(v.w)));
-                    const uint32_t mb = h2_as_u32(m2);
-                    smx = max(smx, max(mb & 0xffffu, mb >> 16));
+                for (int r = 0; r < ngrp; ++r) {
+#pragma unroll 1
+                    for (int o = lane; o < nv; o += 32) {
+                        const uint4 v = lds128(st0 + r * rec + vpar + 16 * o);
+                        const __half2 m2 = __hmax2(__hmax2(u32_as_h2(v.x), u32_as_h2(v.y)),
+                                                   __hmax2(u32_as_h2(v.z), u32_as_h2(v.w)));
+                        const uint32_t mb = h2_as_u32(m2);
+                        smx = max(smx, max(mb & 0xffffu, mb >> 16));
+                    }
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) smx = max(smx, __shfl_xor_sync(0xffffffffu, smx, o));
