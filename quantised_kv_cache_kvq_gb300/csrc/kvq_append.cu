@@ -337,6 +337,13 @@ __global__ void __launch_bounds__(kThreads) k_append_small(AppendArgs a) {
     grid_launch_dependents();   // a decode launched next may start launching (it waits for us)
     const Layout& lo = a.lo;
     const int h = blockIdx.x, bi = blockIdx.y, b = a.seq_begin + bi;
+    if (lo.scheme == KVQ_SCHEME_KIVI && (threadIdx.x >> 5) < a.n_new) {
+        // the new rows' addresses do not depend on the cache state: start bringing them
+        // into L2 while the state is read
+        const int64_t row = input_row(lo, a.n_new, bi, threadIdx.x >> 5, h) + (threadIdx.x & 31) * (lo.D / 32);
+        prefetch_l2(reinterpret_cast<const uint16_t*>(a.k_new) + row);
+        prefetch_l2(reinterpret_cast<const uint16_t*>(a.v_new) + row);
+    }
     int32_t* st = state_ptr(lo, a.cache, a.layer, b);
     const int n = st[0], qn = st[1];
     uint32_t status = 0;
@@ -375,12 +382,13 @@ __global__ void __launch_bounds__(kThreads) k_append_small(AppendArgs a) {
     bad = __syncthreads_or(bad);
     if (threadIdx.x == 0) {
         if (bad) atomicOr(reinterpret_cast<uint32_t*>(a.cache), KVQ_STATUS_NONFINITE);
-        __threadfence();
+        // every block has used its reads of the old counts before it arrives here (its
+        // control flow depends on them); the rows it wrote are for later kernels, which see
+        // them at this kernel's end, so no fence is needed before the arrival
         if (atomicAdd(&st[2], 1) == lo.H - 1) {
             st[0] = n + m;
             st[1] = qn2;
             st[2] = 0;
-            __threadfence();
         }
     }
 }

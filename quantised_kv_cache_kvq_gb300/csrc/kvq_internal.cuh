@@ -211,6 +211,12 @@ inline cudaError_t launch_dependent(void (*fn)(P...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, fn, std::forward<A>(args)...);
 }
 
+// Bring the 128-byte line holding `p` into L2 (no register result, no fault semantics
+// beyond those of a load of `p`).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
