@@ -282,7 +282,8 @@ void kvqo_int8_token(const float* x, int n, float* scale_out, int8_t* codes)
  *   INT8:  per (l, b, h) block over T16 = T rounded up to 16:
  *            K codes int8 [T16][D], V codes int8 [T16][D], K scale f32 [T16], V scale f32 [T16]
  *   FP8:   scale table f32 [layers][kv heads][2] (K, V), then per (l, b, h) block:
- *            K codes e4m3 [T16][D], V codes e4m3 [T16][D]
+ *            K codes e4m3 [T16][D], each row in the channel order of fp8_kbyte
+ *            V codes e4m3 [T16 / 16 tiles][D][16 tokens], tokens in the order of fp8_vbyte
  * Bits are numbered LSB-first within a byte: bit i is bit (i mod 8) of byte i / 8.
  * ---------------------------------------------------------------------------------- */
 typedef struct {
@@ -307,6 +308,26 @@ static int64_t vcode_bit(int64_t D, int bits, int64_t t, int64_t ch)
     int64_t tw = tile * wpt + w;
     int64_t col = bits >= 4 && (tw & 1) ? (ch ^ 8) : ch;
     return (tw * D + col) * 32 + 16 * half + bits * i;
+}
+
+/* FP8 keys: byte of channel ch within a token's D-byte row.  Channel r = ch mod 16 of the
+ * 16-channel block kb = ch / 16 goes to quarter ((r mod 8) / 2) of the row, at byte
+ * 4 kb + 2 (r / 8) + (r mod 2) of the quarter: a quarter holds, per block, the channels
+ * 2i, 2i + 1, 2i + 8, 2i + 9 (i = the quarter) side by side. */
+static int64_t fp8_kbyte(int64_t D, int64_t ch)
+{
+    int64_t kb = ch / 16, r = ch % 16;
+    return ((r % 8) / 2) * (D / 4) + 4 * kb + 2 * (r / 8) + (r % 2);
+}
+
+/* FP8 values: byte of (token t, channel ch) within the value codes of a (l, b, h) block.
+ * Tokens come in tiles of 16 stored [channel][16 bytes]; token tt of a tile sits at byte
+ * 4 ((tt mod 8) / 2) + 2 (tt mod 2) + tt / 8 of its channel's 16 bytes, so the four bytes
+ * from 4i hold tokens 2i, 2i + 8, 2i + 1, 2i + 9. */
+static int64_t fp8_vbyte(int64_t D, int64_t t, int64_t ch)
+{
+    int64_t tt = t % 16;
+    return (t - tt) * D + ch * 16 + 4 * ((tt % 8) / 2) + 2 * (tt % 2) + tt / 8;
 }
 
 /* Byte offset, within a record's value parameters, of the fp16 scale of token t
@@ -586,8 +607,10 @@ uint32_t kvqo_append(const kvqo_config* c, uint8_t* img, int l, int seq_begin, i
                     for (int kv = 0; kv < 2; kv++) {
                         float sc = tab[2 * h + kv];
                         input_row(c, kv ? v_new : k_new, n_new, bi, j, h, row);
-                        for (int ch = 0; ch < D; ch++)
-                            base[kv * L.t16 * D + t * D + ch] = kvqo_e4m3_from_float(row[ch] / sc);
+                        for (int ch = 0; ch < D; ch++) {
+                            int64_t at = kv ? L.t16 * D + fp8_vbyte(D, t, ch) : t * D + fp8_kbyte(D, ch);
+                            base[at] = kvqo_e4m3_from_float(row[ch] / sc);
+                        }
                     }
                 }
             }
@@ -666,8 +689,8 @@ void kvqo_dequant_token(const kvqo_config* c, const uint8_t* img, int l, int b, 
     } else {
         const float* tab = (const float*)(img + L.scales) + (int64_t)l * c->kv_heads * 2;
         for (int ch = 0; ch < D; ch++) {
-            kout[ch] = kvqo_e4m3_to_float(base[t * D + ch]) * tab[2 * h];
-            vout[ch] = kvqo_e4m3_to_float(base[L.t16 * D + t * D + ch]) * tab[2 * h + 1];
+            kout[ch] = kvqo_e4m3_to_float(base[t * D + fp8_kbyte(D, ch)]) * tab[2 * h];
+            vout[ch] = kvqo_e4m3_to_float(base[L.t16 * D + fp8_vbyte(D, t, ch)]) * tab[2 * h + 1];
         }
     }
 }

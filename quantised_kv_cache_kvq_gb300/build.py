@@ -27,6 +27,7 @@ UNITS = {
     "kvq_decode_kivi4.cu": [],
     "kvq_decode_kivi8.cu": [],
     "kvq_decode_rows.cu": [],
+    "kvq_decode_fp8.cu": [],
     "kvq_noalloc.cu": [],
 }
 

@@ -121,6 +121,27 @@ int make_plan(const Layout& lo, DecodePlan* p) {
             if (resident_blocks(decode_smem(lo, *p).total) < res1) p->NSTAGE = 1;
         }
         p->NQ = static_cast<int>((chunks + cpi - 1) / cpi);
+    } else if (lo.scheme == KVQ_SCHEME_FP8_E4M3) {
+        // FP8 on the tensor cores: warps of W = 32 tokens, chunks of 128, as many chunks
+        // per item as make the items fit one wave, double-buffered when that costs no
+        // resident block
+        p->CHR = 0;
+        p->NRC = 0;
+        p->W = 32;
+        p->CH = 4 * p->W;
+        const int64_t chunks = (lo.T + p->CH - 1) / p->CH;
+        p->CPI = 1;
+        p->NSTAGE = 1;
+        const int res1 = resident_blocks(decode_smem(lo, *p).total);
+        const int64_t slots = (int64_t)kNumSMs * res1;
+        int64_t cpi = (units * chunks + slots - 1) / slots;
+        cpi = cpi < 1 ? 1 : (cpi > 64 ? 64 : cpi);
+        p->CPI = static_cast<int>(cpi);
+        if (cpi > 1) {
+            p->NSTAGE = 2;
+            if (resident_blocks(decode_smem(lo, *p).total) < res1) p->NSTAGE = 1;
+        }
+        p->NQ = static_cast<int>((chunks + cpi - 1) / cpi);
     } else {
         p->CHR = 128;
         p->NRC = (lo.T + p->CHR - 1) / p->CHR;

@@ -300,12 +300,23 @@ __device__ __forceinline__ uint32_t quantise_row(const Layout& lo, uint8_t* cach
             if (lane == 0)
                 reinterpret_cast<float*>(base + 2 * (int64_t)lo.T16 * D)[(int64_t)kv * lo.T16 + t] = s;
         } else {
+            // keys: channel r of 16-channel block kb at quarter (r mod 8) / 2 of the row,
+            // byte 4 kb + 2 (r / 8) + (r mod 2) of it; values: tiles of 16 tokens stored
+            // [channel][16], token tt at byte 4 ((tt mod 8) / 2) + 2 (tt mod 2) + tt / 8
             const float s = fp8_scales[2 * h + kv];
+            const int tt = static_cast<int>(t % 16);
+            uint8_t* vtile = base + (int64_t)lo.T16 * D + (t - tt) * D + 4 * ((tt % 8) / 2) + 2 * (tt % 2) + tt / 8;
+            uint8_t* krow = base + t * D;
             for (int c = lane; c < D; c += 32) {
                 float x = load_input(src, row + c, lo.dtype);
                 bad |= nonfinite(x);
-                codes[c] = static_cast<uint8_t>(
+                const uint8_t code = static_cast<uint8_t>(
                     __nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3));
+                const int r = c % 16;
+                if (kv == 0)
+                    krow[((r % 8) / 2) * (D / 4) + 4 * (c / 16) + 2 * (r / 8) + (r % 2)] = code;
+                else
+                    vtile[c * 16] = code;
             }
         }
     }

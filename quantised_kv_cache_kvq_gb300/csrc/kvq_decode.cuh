@@ -22,7 +22,8 @@
 //           32-bit words [token word][channel], the halves of a word holding tokens tt
 //           and tt + 8 of a tile), Bp = p_t * value scale split into major/minor parts;
 //           the offset term sum_t p_t * zero_t is one more small product.
-// The bf16 window (KIVI), INT8 rows and FP8 rows go through a CUDA-core row path.
+// The bf16 window (KIVI) and INT8 rows go through a CUDA-core row path; FP8 caches run
+// on the tensor cores in kvq_decode_fp8.cu.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -155,7 +156,7 @@ __device__ __forceinline__ void chunk_softmax(const Layout& lo, float* sc, int n
 }
 
 // ------------------------------------------------------------------------ row path
-// Tokens held as whole rows: the bf16 window of a KIVI cache, or INT8 / FP8 rows.
+// Tokens held as whole rows: the bf16 window of a KIVI cache, or INT8 rows.
 template <int D>
 __device__ void rows_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& so, int b, int h,
                           int item, int64_t t0, int64_t t1) {
@@ -183,49 +184,32 @@ __device__ void rows_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets&
             if (cnt > first)
                 bulk_copy_pieces(data + (int64_t)first * 4 * D, ring, static_cast<uint32_t>(cnt - first) * 4 * D, bar);
         } else {
+            // INT8 rows (FP8 has its own tensor-core path)
             const uint8_t* unit = a.cache + lo.data_off + u * lo.unit;
             const uint32_t cb = static_cast<uint32_t>(cnt) * D;
-            if (lo.scheme == KVQ_SCHEME_INT8) {
-                const uint32_t sb = static_cast<uint32_t>((cnt + 3) / 4 * 4) * 4;
-                mbar_arrive_expect_tx(bar, 2 * cb + 2 * sb);
-                bulk_copy_pieces(data, unit + t0 * D, cb, bar);
-                bulk_copy_pieces(data + (int64_t)CHR * D, unit + (int64_t)lo.T16 * D + t0 * D, cb, bar);
-                const uint8_t* scales = unit + 2 * (int64_t)lo.T16 * D;
-                bulk_copy_pieces(data + 2 * (int64_t)CHR * D, scales + 4 * t0, sb, bar);
-                bulk_copy_pieces(data + 2 * (int64_t)CHR * D + 4 * CHR, scales + 4 * (int64_t)lo.T16 + 4 * t0, sb, bar);
-            } else {
-                mbar_arrive_expect_tx(bar, 2 * cb);
-                bulk_copy_pieces(data, unit + t0 * D, cb, bar);
-                bulk_copy_pieces(data + (int64_t)CHR * D, unit + (int64_t)lo.T16 * D + t0 * D, cb, bar);
-            }
+            const uint32_t sb = static_cast<uint32_t>((cnt + 3) / 4 * 4) * 4;
+            mbar_arrive_expect_tx(bar, 2 * cb + 2 * sb);
+            bulk_copy_pieces(data, unit + t0 * D, cb, bar);
+            bulk_copy_pieces(data + (int64_t)CHR * D, unit + (int64_t)lo.T16 * D + t0 * D, cb, bar);
+            const uint8_t* scales = unit + 2 * (int64_t)lo.T16 * D;
+            bulk_copy_pieces(data + 2 * (int64_t)CHR * D, scales + 4 * t0, sb, bar);
+            bulk_copy_pieces(data + 2 * (int64_t)CHR * D + 4 * CHR, scales + 4 * (int64_t)lo.T16 + 4 * t0, sb, bar);
         }
     }
     load_query(a, b, h, qs);
-    float kscale = 1.0f, vscale = 1.0f;
-    if (lo.scheme == KVQ_SCHEME_FP8_E4M3) {
-        const float* tab = reinterpret_cast<const float*>(a.cache + lo.scales_off) + ((int64_t)a.layer * lo.H + h) * 2;
-        kscale = tab[0];
-        vscale = tab[1];
-    }
     if (!wait_staged(bar, a.ws)) return;
 
     auto kval = [&](int i, int c) -> float {
         if (lo.scheme == KVQ_SCHEME_KIVI)
             return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(data + (int64_t)i * 4 * D)[c]);
-        if (lo.scheme == KVQ_SCHEME_INT8)
-            return static_cast<float>(reinterpret_cast<const int8_t*>(data)[i * D + c]) *
-                   reinterpret_cast<const float*>(data + 2 * (int64_t)CHR * D)[i];
-        const __half_raw hr = __nv_cvt_fp8_to_halfraw(data[i * D + c], __NV_E4M3);
-        return __half2float(__half(hr)) * kscale;
+        return static_cast<float>(reinterpret_cast<const int8_t*>(data)[i * D + c]) *
+               reinterpret_cast<const float*>(data + 2 * (int64_t)CHR * D)[i];
     };
     auto vval = [&](int i, int c) -> float {
         if (lo.scheme == KVQ_SCHEME_KIVI)
             return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(data + (int64_t)i * 4 * D + 2 * D)[c]);
-        if (lo.scheme == KVQ_SCHEME_INT8)
-            return static_cast<float>(reinterpret_cast<const int8_t*>(data + (int64_t)CHR * D)[i * D + c]) *
-                   reinterpret_cast<const float*>(data + 2 * (int64_t)CHR * D + 4 * CHR)[i];
-        const __half_raw hr = __nv_cvt_fp8_to_halfraw(data[(int64_t)CHR * D + i * D + c], __NV_E4M3);
-        return __half2float(__half(hr)) * vscale;
+        return static_cast<float>(reinterpret_cast<const int8_t*>(data + (int64_t)CHR * D)[i * D + c]) *
+               reinterpret_cast<const float*>(data + 2 * (int64_t)CHR * D + 4 * CHR)[i];
     };
 
     // scores: a warp per token, lanes over channels, one reduction per head
@@ -1073,5 +1057,6 @@ int launch_decode_kivi2(const DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi4(const DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi8(const DecodeArgs& a, cudaStream_t stream);
 int launch_decode_rows(const DecodeArgs& a, cudaStream_t stream);
+int launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace kvq

@@ -117,6 +117,8 @@ int launch_decode(const Layout& lo, const DecodePlan& plan, const uint8_t* cache
         rc = lo.bits == 2 ? launch_decode_kivi2(a, stream)
            : lo.bits == 4 ? launch_decode_kivi4(a, stream)
                           : launch_decode_kivi8(a, stream);
+    } else if (lo.scheme == KVQ_SCHEME_FP8_E4M3) {
+        rc = launch_decode_fp8(a, stream);
     } else {
         rc = launch_decode_rows(a, stream);
     }

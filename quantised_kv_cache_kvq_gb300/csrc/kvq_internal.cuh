@@ -96,7 +96,7 @@ __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const Decod
     } else if (lo.scheme == KVQ_SCHEME_INT8) {
         rows = (int64_t)p.CHR * (2 * lo.D + 8);
     } else {
-        rows = (int64_t)p.CHR * 2 * lo.D;
+        rows = (int64_t)p.NSTAGE * p.CH * 2 * lo.D;      // FP8: key rows + value tiles per stage
     }
     off += rows > packed ? rows : packed;
     o.total = off;

@@ -458,6 +458,26 @@ def test_layout_golden_record_4bit_tile_order():
         assert np.array_equal(vt, V[tok]), tok
 
 
+def test_layout_golden_fp8_block():
+    cfg = O.make_config(scheme=2, batch=1, kv_heads=1, q_heads=1, head_dim=32, max_tokens=16)
+    img = O.Image(cfg)
+    t = np.arange(16)[:, None]
+    c = np.arange(32)[None, :]
+    K = (c % 16 + 0 * t).astype(np.float32)
+    V = (t + 0 * c).astype(np.float32)
+    kb = _bf16_bits(torch.tensor(K).to(torch.bfloat16)).reshape(1, 16, 1, 32)
+    vb = _bf16_bits(torch.tensor(V).to(torch.bfloat16)).reshape(1, 16, 1, 32)
+    assert img.append(0, 0, kb, vb, fp8_scales=np.array([[1.0, 1.0]], np.float32)) == 0
+    blk = img.buf[img.regions()["data"]:]
+    rows = _golden("layout_fp8.txt")
+    assert len(rows) >= 30
+    for off, byte in rows:
+        assert blk[int(off)] == int(byte, 16), off
+    for tok in (0, 5, 9, 15):
+        kt, vt = img.dequant_token(0, 0, 0, tok)
+        assert np.array_equal(kt, K[tok]) and np.array_equal(vt, V[tok]), tok
+
+
 def test_packed_tokens_dequantise_to_their_groups():
     # keys: Q_b per channel over the G tokens of the group; values: Q_b per token over each Gv
     # block of channels ("Per-channel and per-token grouping"; KIVI "How It Works")
