@@ -95,22 +95,25 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- byte model
-def decode_bytes(w, n_tokens):
-    """Algorithmic bytes one decode launch reads for a batch whose sequences hold
-    n_tokens each: packed group records + bf16 window rows + the queries."""
+def decode_bytes(w, lengths):
+    """Algorithmic bytes one decode launch (one layer) reads for sequences holding
+    `lengths[b]` tokens: packed group records + bf16 window rows + the queries."""
     H, D, gqa = w.kv_heads, w.head_dim, w.gqa
-    if w.scheme == 0:
-        G, b, R = w.group_k, w.bits, w.residual
-        qn = G * ((n_tokens - R) // G) if n_tokens >= R + G else 0
-        r = n_tokens - qn
-        rec = G * D * b // 8 * 2 + 4 * D + 4 * G * (D // w.group_v)
-        cache = (qn // G) * rec + r * 4 * D
-    elif w.scheme == 1:
-        cache = n_tokens * (2 * D + 8)
-    else:
-        cache = n_tokens * 2 * D
     qbytes = gqa * D * (2 if w.in_dtype == "bf16" else 4)
-    return w.batch * H * (cache + qbytes)
+    total = 0
+    for n_tokens in lengths:
+        if w.scheme == 0:
+            G, b, R = w.group_k, w.bits, w.residual
+            qn = G * ((n_tokens - R) // G) if n_tokens >= R + G else 0
+            r = n_tokens - qn
+            rec = G * D * b // 8 * 2 + 4 * D + 4 * G * (D // w.group_v)
+            cache = (qn // G) * rec + r * 4 * D
+        elif w.scheme == 1:
+            cache = n_tokens * (2 * D + 8)
+        else:
+            cache = n_tokens * 2 * D
+        total += H * (cache + qbytes)
+    return total
 
 
 def sources_sha256():
@@ -161,35 +164,44 @@ def run_gpu(args, w, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     K.load()
-    n0 = w.context[0]
-    per_cache = decode_bytes(w, n0)
-    reps = max(2, math.ceil(4 * L2_BYTES / per_cache)) if args.replicas <= 0 else args.replicas
+    lens0 = [int(x) for x in W.context_lengths(w).tolist()]
+    layers = w.layers if args.all_layers else 1
+    per_cache = layers * decode_bytes(w, lens0)
+    # replicas rotated per step so that consecutive steps read their caches from HBM
+    reps = max(1, math.ceil(4 * L2_BYTES / per_cache)) if args.replicas <= 0 else args.replicas
+    reps = max(reps, 2) if per_cache < 4 * L2_BYTES else reps
     total_steps = args.warmup + args.steps
     e2e_steps = min(args.steps, 200)
     appends_per_rep = math.ceil((total_steps + e2e_steps) / reps) + 1
-    max_tokens = n0 + appends_per_rep + 64
-    # one layer of the workload: a step is one layer's append + decode
-    cfg = K.make_config(w.scheme, 1, w.batch, w.q_heads, w.kv_heads, w.head_dim, max_tokens,
+    max_tokens = max(lens0) + appends_per_rep + 64
+    cfg = K.make_config(w.scheme, layers, w.batch, w.q_heads, w.kv_heads, w.head_dim, max_tokens,
                         bits=w.bits, group_k=w.group_k, group_v=w.group_v, residual=w.residual,
                         in_dtype=w.in_dtype)
     caches = []
     fp8 = None
     if w.scheme == 2:   # static per-(kv head) scales from the first replica's fill
-        k, v = W.kv_tokens(w, 0, 0, min(8, w.batch), 0, n0, device=dev, tag="rep0")
+        k, v = W.kv_tokens(w, 0, 0, min(8, w.batch), 0, min(lens0[:8]), device=dev, tag="rep0")
         fp8 = W.fp8_scales(w, k, v)
         del k, v
+    t_fill = time.perf_counter()
     for r in range(reps):
         c = K.QuantizedKVCache(cfg, dev)
         for s0 in range(0, w.batch, 8):
             ns = min(8, w.batch - s0)
-            k, v = W.kv_tokens(w, 0, s0, ns, 0, n0, device=dev, tag="rep%d" % r)
-            c.append(0, k, v, seq_begin=s0, fp8_scales=fp8)
+            nl = lens0[s0:s0 + ns]
+            k, v = W.kv_tokens(w, 0, s0, ns, 0, max(nl), device=dev, tag="rep%d" % r)
+            nv = torch.tensor(nl, dtype=torch.int32, device=dev)
+            # every layer is filled from the same seeded draw (the timing does not depend on
+            # the values; each layer is a separate cache region read from HBM)
+            for layer in range(layers):
+                c.append(layer, k, v, seq_begin=s0, n_valid=nv, fp8_scales=fp8)
             del k, v
         caches.append(c)
     torch.cuda.synchronize()
+    t_fill = time.perf_counter() - t_fill
     ws = caches[0].workspace
-    # per-step inputs: one new token per sequence and the step's queries
-    kn, vn = W.kv_tokens(w, 0, 0, w.batch, n0, total_steps, device=dev, tag="steps")
+    # per-step inputs: one new token per sequence (shared by the layers) and the step's queries
+    kn, vn = W.kv_tokens(w, 0, 0, w.batch, max(lens0), total_steps, device=dev, tag="steps")
     k_steps = kn.permute(1, 0, 2, 3).contiguous().unsqueeze(2)   # [step][batch][1][H][D]
     v_steps = vn.permute(1, 0, 2, 3).contiguous().unsqueeze(2)
     del kn, vn
@@ -204,11 +216,12 @@ def run_gpu(args, w, rank, world):
 
     def step(i):
         c = caches[i % reps]
-        K.kvq_quantize_append(cfg, c.cache, 0, 0, w.batch, k_steps[i], v_steps[i], 1, fp8_scales=fp8,
-                              stream=stream)
-        K.kvq_decode_attention(cfg, c.cache, 0, q_steps[i], scale, outs[i % reps], ws, stream=stream)
+        for layer in range(layers):
+            K.kvq_quantize_append(cfg, c.cache, layer, 0, w.batch, k_steps[i], v_steps[i], 1, fp8_scales=fp8,
+                                  stream=stream)
+            K.kvq_decode_attention(cfg, c.cache, layer, q_steps[i], scale, outs[i % reps], ws, stream=stream)
 
-    launches_per_step = 3  # append (one kernel for a one-token append), decode, merge
+    launches_per_step = 3 * layers  # per layer: append (one kernel for a one-token append), decode, merge
     # warm-up (eager), then the timed steps as one graph
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -223,8 +236,8 @@ def run_gpu(args, w, rank, world):
     with torch.cuda.graph(dgraph, stream=stream):
         for i in range(args.steps):
             c = caches[i % reps]
-            K.kvq_decode_attention(cfg, c.cache, 0, q_steps[i], scale, outs[i % reps], ws, stream=stream)
-    ctx_after = [n0 + (args.warmup // reps) + (1 if r < args.warmup % reps else 0) for r in range(reps)]
+            for layer in range(layers):
+                K.kvq_decode_attention(cfg, c.cache, layer, q_steps[i], scale, outs[i % reps], ws, stream=stream)
 
     def barrier():
         if world > 1:
@@ -258,22 +271,27 @@ def run_gpu(args, w, rank, world):
         status |= c.status()
     if status:
         raise RuntimeError("device status word %#x after the benchmark" % status)
-    # bytes of the timed steps (each replica's context grows by one token per visit)
+
+    # bytes of the timed steps (every replica's sequences grow by one token per visit)
+    def lengths_after(visits):
+        return [n + visits for n in lens0]
+
+    def visits(r, steps_done):
+        return steps_done // reps + (1 if r < steps_done % reps else 0)
+
     bytes_steps = 0
-    ctx = list(ctx_after)
     for i in range(args.warmup, total_steps):
         r = i % reps
-        ctx[r] += 1
-        bytes_steps += decode_bytes(w, ctx[r])
-    ctx2 = [n0 + ((total_steps // reps) + (1 if r < total_steps % reps else 0)) for r in range(reps)]
-    bytes_decode = sum(decode_bytes(w, ctx2[i % reps]) for i in range(args.steps))
+        bytes_steps += layers * decode_bytes(w, lengths_after(visits(r, i) + 1))
+    bytes_decode = sum(layers * decode_bytes(w, lengths_after(visits(i % reps, total_steps)))
+                       for i in range(args.steps))
 
     # end to end through the C ABI with host buffers: per step copy the new token and the
-    # queries from pinned host memory, append, decode, copy the output back
+    # queries from pinned host memory, append, decode every layer, copy the outputs back
     hk = k_steps[:e2e_steps].cpu().pin_memory()
     hv = v_steps[:e2e_steps].cpu().pin_memory()
     hq = q_steps[:e2e_steps].cpu().pin_memory()
-    hout = torch.empty(e2e_steps, w.batch, w.q_heads, w.head_dim, dtype=torch.float32).pin_memory()
+    hout = torch.empty(e2e_steps, layers, w.batch, w.q_heads, w.head_dim, dtype=torch.float32).pin_memory()
     dk = torch.empty_like(k_steps[0])
     dv = torch.empty_like(v_steps[0])
     dq = torch.empty_like(q_steps[0])
@@ -286,20 +304,22 @@ def run_gpu(args, w, rank, world):
             dk.copy_(hk[i], non_blocking=True)
             dv.copy_(hv[i], non_blocking=True)
             dq.copy_(hq[i], non_blocking=True)
-            K.kvq_quantize_append(cfg, c.cache, 0, 0, w.batch, dk, dv, 1, fp8_scales=fp8, stream=stream)
-            K.kvq_decode_attention(cfg, c.cache, 0, dq, scale, outs[0], ws, stream=stream)
-            hout[i].copy_(outs[0], non_blocking=True)
+            for layer in range(layers):
+                K.kvq_quantize_append(cfg, c.cache, layer, 0, w.batch, dk, dv, 1, fp8_scales=fp8, stream=stream)
+                K.kvq_decode_attention(cfg, c.cache, layer, dq, scale, outs[0], ws, stream=stream)
+                hout[i, layer].copy_(outs[0], non_blocking=True)
         x1.record(stream)
     barrier()
     e2e_ms = x0.elapsed_time(x1)
     h2d = (dk.numel() * dk.element_size() + dv.numel() * dv.element_size() + dq.numel() * dq.element_size())
-    d2h = outs[0].numel() * 4
+    d2h = layers * outs[0].numel() * 4
 
     step_ms, decode_ms, e2e_ms = max_over_ranks([step_ms, decode_ms, e2e_ms], world, dev)
     return dict(step_ms=step_ms, decode_ms=decode_ms, e2e_ms=e2e_ms, e2e_steps=e2e_steps,
-                bytes_steps=bytes_steps, bytes_decode=bytes_decode, reps=reps,
+                bytes_steps=bytes_steps, bytes_decode=bytes_decode, reps=reps, layers=layers,
                 cache_mb=per_cache / 1e6, launches=launches_per_step * args.steps,
-                clocks=sampler.summary(), h2d=h2d, d2h=d2h, max_tokens=max_tokens)
+                clocks=sampler.summary(), h2d=h2d, d2h=d2h, max_tokens=max_tokens, fill_s=t_fill,
+                mean_context=sum(lens0) / len(lens0))
 
 
 # ---------------------------------------------------------------------------- CPU oracle
@@ -307,7 +327,8 @@ def oracle_setup(w, nseq):
     import numpy as np
     import oracle as O
     from quantised_kv_cache_kvq_gb300 import workloads as W
-    n0 = w.context[0]
+    lens = [int(x) for x in W.context_lengths(w).tolist()[:nseq]]
+    n0 = max(lens)
     kw = dict(scheme=w.scheme, layers=1, batch=nseq, q_heads=w.q_heads, kv_heads=w.kv_heads,
               head_dim=w.head_dim, bits=w.bits, group_k=w.group_k, group_v=w.group_v,
               residual=w.residual, max_tokens=n0 + 4096, in_dtype=0 if w.in_dtype == "bf16" else 1)
@@ -315,13 +336,14 @@ def oracle_setup(w, nseq):
     import torch
     k, v = W.kv_tokens(w, 0, 0, nseq, 0, n0, device="cpu", tag="cpu")
     to = (lambda t: t.view(torch.int16).numpy().view(np.uint16)) if w.in_dtype == "bf16" else (lambda t: t.numpy())
-    img.append(0, 0, to(k), to(v))
+    sc = W.fp8_scales(w, k, v).numpy() if w.scheme == 2 else None
+    img.append(0, 0, to(k), to(v), n_valid=np.asarray(lens, np.int32), fp8_scales=sc)
     q = W.queries(w, 0, device="cpu").float().numpy()[:nseq]
     kn, vn = W.kv_tokens(w, 0, 0, nseq, n0, 4096, device="cpu", tag="cpu-steps")
-    return img, q, to(kn), to(vn)
+    return img, q, to(kn), to(vn), sc
 
 
-def oracle_steps(w, img, q, kn, vn, nsteps, seqs_per_step, threads, t_index):
+def oracle_steps(w, img, q, kn, vn, sc, nsteps, seqs_per_step, threads, t_index):
     """nsteps oracle steps; each appends one token to every sequence and decodes
     `seqs_per_step` of them (one thread per sequence).  Returns decoded sequences."""
     nseq = q.shape[0]
@@ -329,7 +351,7 @@ def oracle_steps(w, img, q, kn, vn, nsteps, seqs_per_step, threads, t_index):
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
         for s in range(nsteps):
             j = (t_index + s) % kn.shape[1]
-            img.append(0, 0, kn[:, j:j + 1], vn[:, j:j + 1])
+            img.append(0, 0, kn[:, j:j + 1], vn[:, j:j + 1], fp8_scales=sc)
             seqs = [(t_index + s + i) % nseq for i in range(seqs_per_step)]
             list(ex.map(lambda b: img.decode(0, q, w.scale, seq_begin=b, seq_count=1), seqs))
             done += seqs_per_step
@@ -341,16 +363,16 @@ def run_oracle(w, steps, warmup, budget_s, adapt_steps=False):
     threads, sequences decoded per step, sequences in the image, steps run)."""
     nseq = min(w.batch, 8)
     cores = len(os.sched_getaffinity(0))
-    img, q, kn, vn = oracle_setup(w, nseq)
+    img, q, kn, vn, sc = oracle_setup(w, nseq)
     threads = min(cores, nseq)
     t = time.perf_counter()
-    oracle_steps(w, img, q, kn, vn, max(1, warmup), 1, 1, 0)
+    oracle_steps(w, img, q, kn, vn, sc, max(1, warmup), 1, 1, 0)
     per_seq = (time.perf_counter() - t) / max(1, warmup)
     if adapt_steps:
         steps = int(max(1, min(steps, budget_s / max(1e-9, per_seq * nseq / threads))))
     spp = int(max(1, min(nseq, budget_s / max(1e-9, steps * per_seq) * threads)))
     t = time.perf_counter()
-    done = oracle_steps(w, img, q, kn, vn, steps, spp, threads, warmup)
+    done = oracle_steps(w, img, q, kn, vn, sc, steps, spp, threads, warmup)
     el = time.perf_counter() - t
     return done / el, el, threads, spp, nseq, steps
 
@@ -365,6 +387,8 @@ def main():
     ap.add_argument("--workload", default="kivi2_llama3_8b")
     ap.add_argument("--replicas", type=int, default=0, help="cache replicas (0: enough to exceed 4x L2)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work per run")
+    ap.add_argument("--all-layers", action="store_true",
+                    help="time every layer of a multi-layer workload in each step (default: one layer)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -373,10 +397,12 @@ def main():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     peak, peak_kind = peaks()
+    ragged = w.context[0] != w.context[1]
     config = {"workload": w.name, "scheme": ["kivi", "int8", "fp8"][w.scheme], "bits": w.bits,
               "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads, "head_dim": w.head_dim,
-              "context": w.context[0], "group_k": w.group_k, "group_v": w.group_v,
-              "residual": w.residual, "layers": 1}
+              "context": list(w.context) if ragged else w.context[0], "group_k": w.group_k,
+              "group_v": w.group_v, "residual": w.residual,
+              "layers": w.layers if args.all_layers else 1}
 
     if args.impl == "reference":
         if rank != 0:
@@ -386,7 +412,8 @@ def main():
         ob.build()
         tps, el, threads, spp, nseq, _ = run_oracle(w, args.steps, args.warmup, args.cpu_budget)
         sample = ("%d steps; each appends one token to %d sequences and decodes %d of them "
-                  "(%d KV heads, context %d)" % (args.steps, nseq, spp, w.kv_heads, w.context[0]))
+                  "(%d KV heads, contexts of the workload's first %d sequences, one layer)"
+                  % (args.steps, nseq, spp, w.kv_heads, nseq))
         line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -408,20 +435,24 @@ def main():
         return
     tokens = w.batch * args.steps * world
     value = tokens / (r["step_ms"] / 1e3)
-    dec_avg_ms = r["decode_ms"] / args.steps
-    achieved = (r["bytes_decode"] / args.steps) / (dec_avg_ms / 1e3) / 1e9
+    launches = args.steps * r["layers"]                 # decode calls in the decode-only graph
+    dec_avg_ms = r["decode_ms"] / launches
+    achieved = (r["bytes_decode"] / launches) / (dec_avg_ms / 1e3) / 1e9
     step_gbs = r["bytes_steps"] / (r["step_ms"] / 1e3) / 1e9
     cpu = None
     try:
         tps, el, threads, spp, nseq, ns = run_oracle(w, 8, 1, args.cpu_budget, adapt_steps=True)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        cpu = {"value": tps / r["layers"], "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": "%d oracle steps of the same workload on %d sequences, each appending one token "
-                         "to all and decoding %d of them (%.1f s)" % (ns, nseq, spp, el)}
+                         "to all and decoding %d of them (%.1f s)%s"
+                         % (ns, nseq, spp, el, "; one layer timed, divided by the %d layers a token "
+                            "needs" % r["layers"] if r["layers"] > 1 else "")}
     except Exception as exc:  # the GPU number stands without it
         cpu = {"value": None, "unit": "tokens/s", "cores": 0, "kind": "oracle", "sample": "failed: %s" % exc}
     cfg = dict(config)
     cfg.update({"replicas": r["reps"], "cache_mb_per_replica": round(r["cache_mb"], 2),
-                "l2": "inputs larger than L2: %d cache replicas rotated per step (%.0f MB > 129 MB)"
+                "mean_context": round(r["mean_context"], 1), "fill_s": round(r["fill_s"], 1),
+                "l2": "inputs larger than L2: %d cache replica(s) rotated per step (%.0f MB > 129 MB)"
                       % (r["reps"], r["reps"] * r["cache_mb"]),
                 "timing": "CUDA graph of the timed steps, CUDA events on the launch stream",
                 "parallelism": "replicas" if world > 1 else "single"})
@@ -434,7 +465,7 @@ def main():
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "traffic": profiled_traffic(w.name),
                      "avg_launch_us": 1e3 * dec_avg_ms,
-                     "bytes_per_launch": r["bytes_decode"] / args.steps},
+                     "bytes_per_launch": r["bytes_decode"] / launches},
         "cpu_baseline": cpu,
         "e2e": {"value": w.batch * r["e2e_steps"] * world / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"]},
