@@ -309,14 +309,15 @@ __device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* 
 // ------------------------------------------------------------------------ window path
 // The bf16 window of a KIVI cache.  Keys and queries are exact bf16 values, so the scores
 // go straight to the tensor cores (no conversion, no operand split): rows = 16 tokens,
-// columns = up to 8 query heads.  Each warp takes one 16-token tile, keeps its own
-// softmax partial, and accumulates P.V on CUDA cores with every lane owning D/32
-// consecutive channels; the block then combines its 4 warps.
-template <int D>
+// columns = up to 8 query heads.  Each warp takes one 16-token tile and keeps its own
+// softmax partial; P.V runs on the tensor cores too, with V^T fragments read from the
+// token-major rows by ldmatrix.trans and p split into bf16 major and minor parts.  The
+// block then combines its 4 warps.
+template <int D, int NT>
 __device__ void window_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& so, int b, int h,
                             int item, int64_t t0, int64_t t1) {
     constexpr int KSTEPS = D / 16;
-    constexpr int CPL = D / 32;
+    constexpr int MTV = D / 16;
     const Layout& lo = a.lo;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
     const int cnt = static_cast<int>(t1 - t0);
@@ -355,11 +356,11 @@ __device__ void window_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     const bool ok = wait_staged(bar, a.ws);
     const int tok0 = 16 * warp;
     const int ntok = cnt - tok0 < 0 ? 0 : (cnt - tok0 > 16 ? 16 : cnt - tok0);
-    float o[8][CPL];
+    float oacc[MTV][NT][4];
 #pragma unroll
-    for (int hh = 0; hh < 8; ++hh)
+    for (int mt = 0; mt < MTV; ++mt)
 #pragma unroll
-        for (int e = 0; e < CPL; ++e) o[hh][e] = 0.0f;
+        for (int nt = 0; nt < NT; ++nt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.0f;
     float mh = -INFINITY, lh = 0.0f;      // this lane's head (lane < gqa): max and sum
     if (ok && ntok > 0) {
         // scores: rows g, g + 8 of the tile (tokens beyond the window read as zero rows)
@@ -407,37 +408,62 @@ __device__ void window_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         const float ll0 = __shfl_sync(0xffffffffu, l0, src), ll1 = __shfl_sync(0xffffffffu, l1, src);
         mh = (lane & 1) ? mm1 : mm0;
         lh = (lane & 1) ? ll1 : ll0;
+        // value rows past the window's end hold stale bytes: zero them (their p is 0,
+        // and a stale pattern could read as NaN)
+        if (ntok < 16) {
+            for (int i = ntok + (lane >> 4); i < 16; i += 2) {
+                uint4* vr = reinterpret_cast<uint4*>(data + (int64_t)(tok0 + i) * 4 * D + 2 * D);
+                for (int e = lane & 15; e < D / 8; e += 16) vr[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
         __syncwarp();
-        // values: lane owns channels [lane * CPL, lane * CPL + CPL)
-        for (int i = 0; i < ntok; ++i) {
-            const uint16_t* vr = reinterpret_cast<const uint16_t*>(data + (int64_t)(tok0 + i) * 4 * D + 2 * D) + lane * CPL;
-            float v[CPL];
+        // values on the tensor cores: A = the 16 x 16 (channels x tokens) tile of V^T, read
+        // from the token-major bf16 rows by ldmatrix.trans; B = p (k = tokens, column
+        // 2h + part) split into bf16 major and minor parts, from the warp's p table
+        uint32_t b0[NT], b1[NT];
 #pragma unroll
-            for (int e = 0; e < CPL; e += 2) {
-                const uint32_t two = *reinterpret_cast<const uint32_t*>(vr + e);
-                v[e] = __uint_as_float(two << 16);
-                v[e + 1] = __uint_as_float(two & 0xffff0000u);
-            }
-            const float4 pa = *reinterpret_cast<const float4*>(pt + i * 8);
-            const float4 pb = *reinterpret_cast<const float4*>(pt + i * 8 + 4);
-            const float pp[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+        for (int nt = 0; nt < NT; ++nt) {
+            const int head = 4 * nt + (g >> 1);
+            const float p0 = pt[(2 * tig) * 8 + head], p1 = pt[(2 * tig + 1) * 8 + head];
+            const float p2 = pt[(2 * tig + 8) * 8 + head], p3 = pt[(2 * tig + 9) * 8 + head];
+            const __nv_bfloat162 m01 = __floats2bfloat162_rn(p0, p1), m23 = __floats2bfloat162_rn(p2, p3);
+            const float2 f01 = __bfloat1622float2(m01), f23 = __bfloat1622float2(m23);
+            const __nv_bfloat162 r01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
+            const __nv_bfloat162 r23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
+            const uint32_t um01 = *reinterpret_cast<const uint32_t*>(&m01), um23 = *reinterpret_cast<const uint32_t*>(&m23);
+            const uint32_t ur01 = *reinterpret_cast<const uint32_t*>(&r01), ur23 = *reinterpret_cast<const uint32_t*>(&r23);
+            b0[nt] = (g & 1) ? ur01 : um01;
+            b1[nt] = (g & 1) ? ur23 : um23;
+        }
+        // ldmatrix rows: lane l addresses token (l mod 8) + 8 (l / 16), channels from
+        // 16 q + 8 ((l / 8) mod 2): the four 8 x 8 blocks land as a0..a3
+        const uint32_t vrow = smem_addr(data) + (tok0 + (lane & 7) + 8 * (lane >> 4)) * 4 * D + 2 * D +
+                              2 * 8 * ((lane >> 3) & 1);
 #pragma unroll
-            for (int hh = 0; hh < 8; ++hh) {
-                if (hh >= gqa) break;
+        for (int q = 0; q < MTV; ++q) {
+            uint32_t af[4];
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(af[0]), "=r"(af[1]), "=r"(af[2]), "=r"(af[3])
+                         : "r"(vrow + 32 * q)
+                         : "memory");
 #pragma unroll
-                for (int e = 0; e < CPL; ++e) o[hh][e] = fmaf(pp[hh], v[e], o[hh][e]);
-            }
+            for (int nt = 0; nt < NT; ++nt) mma_16816_bf16(oacc[q][nt], af, b0[nt], b1[nt]);
         }
     }
     // warp partial into shared memory, then the 4 warps combined
     float* cw = comb + warp * gqa * D;
     const bool wlive = ok && ntok > 0;
 #pragma unroll
-    for (int hh = 0; hh < 8; ++hh) {
-        if (hh >= gqa) break;
-        if (wlive)
+    for (int nt = 0; nt < NT; ++nt) {
+        const int head = 4 * nt + tig;
+        if (head < gqa && wlive) {
 #pragma unroll
-            for (int e = 0; e < CPL; ++e) cw[hh * D + lane * CPL + e] = o[hh][e];
+            for (int mt = 0; mt < MTV; ++mt) {
+                const int c0 = 16 * mt + g;
+                cw[head * D + c0] = oacc[mt][nt][0] + oacc[mt][nt][1];
+                cw[head * D + c0 + 8] = oacc[mt][nt][2] + oacc[mt][nt][3];
+            }
+        }
     }
     if (lane < gqa) {
         cml[2 * (warp * gqa + lane)] = wlive ? mh : -INFINITY;
@@ -1033,7 +1059,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
         if (item >= a.plan.NRC)
             packed_item<D, BITS, NT>(a, smem, so, b, h, item, r.t0, r.t1);
         else
-            window_item<D>(a, smem, so, b, h, item, r.t0, r.t1);
+            window_item<D, NT>(a, smem, so, b, h, item, r.t0, r.t1);
         return;
     }
     rows_item<D>(a, smem, so, b, h, item, r.t0, r.t1);
