@@ -116,19 +116,25 @@ def decode_bytes(w, lengths):
     return total
 
 
-def sources_sha256():
-    """Digest of the CUDA sources (file names and contents) the library is built from."""
+DECODE_SOURCES = ("kvq_api.cu", "kvq_decode.cuh", "kvq_decode_rows.cu", "kvq_internal.cuh", "kvq_launch.h")
+SCHEME_SOURCES = {0: ("kvq_decode_kivi2.cu", "kvq_decode_kivi4.cu", "kvq_decode_kivi8.cu"),
+                  1: (), 2: ("kvq_decode_fp8.cu",)}
+
+
+def sources_sha256(scheme):
+    """Digest of the CUDA sources (file names and contents) that decide a scheme's decode
+    kernels: the plan, the shared decode code and the scheme's own translation units."""
     import hashlib
     d = os.path.join(ROOT, "quantised_kv_cache_kvq_gb300", "csrc")
     h = hashlib.sha256()
-    for n in sorted(os.listdir(d)):
+    for n in sorted(DECODE_SOURCES + SCHEME_SOURCES[scheme]):
         h.update(n.encode())
         with open(os.path.join(d, n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, scheme):
     """DRAM bytes per decode launch (both kernels) from the committed ncu summary of this
     workload; None without one, or when the kernels' sources changed since its capture."""
     import re
@@ -139,7 +145,7 @@ def profiled_traffic(workload):
         return None
     t = re.search(r"^traffic_bytes_per_launch: (\d+)$", text, re.M)
     h = re.search(r"^sources_sha256: ([0-9a-f]+)$", text, re.M)
-    if not (t and h) or h.group(1) != sources_sha256():
+    if not (t and h) or h.group(1) != sources_sha256(scheme):
         return None
     return int(t.group(1))
 
@@ -463,7 +469,7 @@ def main():
         "hbm_gbs": step_gbs, "hbm_pct_of_peak": 100.0 * step_gbs / peak,
         "roofline": {"kernel": "kvq decode attention (split-context kernel + merge)", "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": profiled_traffic(w.name),
+                     "peak_kind": peak_kind, "traffic": profiled_traffic(w.name, w.scheme),
                      "avg_launch_us": 1e3 * dec_avg_ms,
                      "bytes_per_launch": r["bytes_decode"] / launches},
         "cpu_baseline": cpu,
