@@ -18,10 +18,13 @@
 namespace kvq {
 namespace {
 
-// Two E4M3 codes (bits 0-7 and 8-15 of `w`) as an fp16 pair (low code -> low half).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
-    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
-    return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+// The four E4M3 codes of `w` as two fp16 pairs: lo <- bytes 0, 1 and hi <- bytes 2, 3 (the
+// lower byte of each 16-bit half to the lower fp16).  One conversion per pair, straight
+// from the register halves.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 // One FP8 work item: a run of chunks of CH = 4 * W tokens of one (sequence, kv head).
@@ -191,10 +194,8 @@ __device__ void fp8_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& 
 #pragma unroll
                 for (int ks = 0; ks < KSTEPS; ++ks) {
                     uint32_t af[4];
-                    af[0] = e4m3x2_to_f16x2(wa[ks]);
-                    af[1] = e4m3x2_to_f16x2(wb[ks]);
-                    af[2] = e4m3x2_to_f16x2(wa[ks] >> 16);
-                    af[3] = e4m3x2_to_f16x2(wb[ks] >> 16);
+                    e4m3x4_to_f16x2x2(wa[ks], af[0], af[2]);
+                    e4m3x4_to_f16x2x2(wb[ks], af[1], af[3]);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma_16816(acc[ks & 1][nt], af, bq[nt][2 * ks], bq[nt][2 * ks + 1]);
                 }
@@ -265,10 +266,8 @@ __device__ void fp8_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& 
                     const uint32_t w0 = lds32(vt + 256 * q) & vmask;          // channel 16q + g
                     const uint32_t w1 = lds32(vt + 256 * q + 128) & vmask;    // channel 16q + g + 8
                     uint32_t af[4];
-                    af[0] = e4m3x2_to_f16x2(w0);
-                    af[1] = e4m3x2_to_f16x2(w1);
-                    af[2] = e4m3x2_to_f16x2(w0 >> 16);
-                    af[3] = e4m3x2_to_f16x2(w1 >> 16);
+                    e4m3x4_to_f16x2x2(w0, af[0], af[2]);
+                    e4m3x4_to_f16x2x2(w1, af[1], af[3]);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma_16816(oacc[q][nt], af, b0[nt], b1[nt]);
                 }
