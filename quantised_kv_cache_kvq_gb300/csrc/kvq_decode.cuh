@@ -116,6 +116,16 @@ __device__ __forceinline__ int64_t slot_index(const DecodeArgs& a, int b, int h,
     return (((int64_t)b * a.lo.H + h) * a.plan.S + item) * a.lo.gqa + head;
 }
 
+// An item without tokens (or whose chunks never arrived) leaves an empty partial: m = -inf,
+// l = 0, so the merge gives it weight 0 without reading the cache state.
+__device__ __forceinline__ void empty_partial(const DecodeArgs& a, int b, int h, int item) {
+    if (threadIdx.x < a.lo.gqa) {
+        float* ml = reinterpret_cast<float*>(a.ws + a.plan.ws_ml_off) + 2 * slot_index(a, b, h, item, threadIdx.x);
+        ml[0] = -INFINITY;
+        ml[1] = 0.0f;
+    }
+}
+
 // Scaled query of the block's kv head into shared fp32 qs[gqa][D].
 __device__ __forceinline__ void load_query(const DecodeArgs& a, int b, int h, float* qs) {
     const Layout& lo = a.lo;
@@ -197,7 +207,10 @@ __device__ void rows_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets&
         }
     }
     load_query(a, b, h, qs);
-    if (!wait_staged(bar, a.ws)) return;
+    if (!wait_staged(bar, a.ws)) {
+        empty_partial(a, b, h, item);
+        return;
+    }
 
     auto kval = [&](int i, int c) -> float {
         if (lo.scheme == KVQ_SCHEME_KIVI)
@@ -1053,7 +1066,10 @@ __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
     const int32_t* st = state_ptr(a.lo, a.cache, a.layer, b);
     const int64_t n = st[0], qn = st[1];
     const ItemRange r = item_range(a.lo, a.plan, item, n, qn);
-    if (r.t0 >= r.t1) return;
+    if (r.t0 >= r.t1) {
+        empty_partial(a, b, h, item);
+        return;
+    }
     const SmemOffsets so = decode_smem(a.lo, a.plan);
     if constexpr (BITS != 0) {
         if (item >= a.plan.NRC)

@@ -314,7 +314,10 @@ __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
     const int32_t* st = state_ptr(a.lo, a.cache, a.layer, b);
     const int64_t n = st[0], qn = st[1];
     const ItemRange r = item_range(a.lo, a.plan, item, n, qn);
-    if (r.t0 >= r.t1) return;
+    if (r.t0 >= r.t1) {
+        empty_partial(a, b, h, item);
+        return;
+    }
     const SmemOffsets so = decode_smem(a.lo, a.plan);
     fp8_item<D, NT>(a, smem, so, b, h, item, r.t0, r.t1);
 }

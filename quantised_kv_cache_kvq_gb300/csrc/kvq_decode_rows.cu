@@ -25,8 +25,6 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(DecodeArgs a, int nwc) 
     const int h = hq / lo.gqa, head = hq % lo.gqa;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwi = NW / nwc, wc = warp % nwc, wi = warp / nwc;
-    const int32_t* st = state_ptr(lo, a.cache, a.layer, b);
-    const int64_t n = st[0], qn = st[1];
     const int S = a.plan.S;
     const float* ml = reinterpret_cast<const float*>(a.ws + a.plan.ws_ml_off);
     const float* o = reinterpret_cast<const float*>(a.ws + a.plan.ws_o_off);
@@ -44,14 +42,14 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(DecodeArgs a, int nwc) 
             lv[k] = 0.0f;
             ov[k] = 0.0f;
             if (it < S) {
-                const ItemRange r = item_range(lo, a.plan, it, n, qn);
-                if (r.t0 < r.t1) {
-                    const int64_t sl = slot0 + (int64_t)it * lo.gqa;
-                    const float2 mlv = *reinterpret_cast<const float2*>(ml + 2 * sl);
-                    mv[k] = mlv.y > 0.0f ? mlv.x : -INFINITY;
-                    lv[k] = mlv.y;
-                    ov[k] = o[sl * D + c];
-                }
+                // every item leaves a partial (an empty one has l = 0: weight 0, and its o
+                // is not used), so all loads go out at once without the cache state
+                const int64_t sl = slot0 + (int64_t)it * lo.gqa;
+                const float2 mlv = *reinterpret_cast<const float2*>(ml + 2 * sl);
+                const float ovl = o[sl * D + c];
+                mv[k] = mlv.y > 0.0f ? mlv.x : -INFINITY;
+                lv[k] = mlv.y > 0.0f ? mlv.y : 0.0f;
+                ov[k] = mlv.y > 0.0f ? ovl : 0.0f;
             }
         }
         // the round's maximum over the block (the same in every lane of a warp)
