@@ -271,9 +271,9 @@ void kvqo_int8_token(const float* x, int n, float* scale_out, int8_t* codes)
  *          no call is running, at byte 16 * (l * batch + b).
  *   KIVI:  group records, one per (l, b, kv head h, group slot g), NG = (T - R) / G slots:
  *            K codes  G*D*b/8 bytes, token-major: (token t, channel c) at bit (t*D + c)*b
- *            V codes  D*G*b/8 bytes of 32-bit words [token word][channel column] (see
- *                     vcode_bit: each 16-token tile is laid out so that the two halves of
- *                     a word hold tokens tt and tt + 8 of the tile)
+ *            V codes  D*G*b/8 bytes of 32-bit words, 2*D*b bytes per 16-token tile, in
+ *                     the order of vcode_bit (a word's halves hold tokens tt and tt + 8
+ *                     of a tile)
  *            K params 4*D bytes: fp16 scale[D], then fp16 zero[D]
  *            V params 4*G*NGv bytes: fp16 scale[NGv][G], then fp16 zero[NGv][G], the G
  *                     tokens of a value group in tile order (see vparam_byte)
@@ -295,19 +295,23 @@ typedef struct {
 static int64_t up256(int64_t x) { return (x + 255) / 256 * 256; }
 
 /* Bit index, within a record's value codes, of the code of token t (0 <= t < G) and
- * channel ch.  Codes sit in 32-bit words, tpw = 32 / bits tokens per word, hw = tpw / 2 per
- * 16-bit half, bits / 2 words per 16-token tile.  Token tt of a tile lies in half tt / 8
- * (so a word's halves hold tokens tt and tt + 8), word (tt mod 8) / hw of the tile, at bit
- * bits * ((tt mod 8) mod hw) of the half.  Words are stored [token word tw][column], D
- * columns per token word; for bits >= 4 odd token words store channel ch in column
- * ch XOR 8 (tiles then span several words). */
+ * channel ch.  Each 16-token tile holds 2 * D * bits bytes as 32 "lanes" of wpl = D * bits / 64
+ * 32-bit words.  Lane 4 g + i (g < 8, i < 4) holds the tile tokens 2i + s and 2i + s + 8
+ * (s = 0 in its even words, 1 in its odd words; the lower token in the word's low 16-bit
+ * half, the other in the high half) for the channels 16 q + g + 8 r (q < D / 16, r < 2):
+ * with hw = 16 / bits codes per half, index j = 2 q + r goes to word 2 (j / hw) + s of the
+ * lane, at bit bits * (j mod hw) of each half.  A lane's words are stored in slabs of
+ * sw = min(wpl, 4): word w of lane L at word (w / sw) * 32 * sw + L * sw + (w mod sw) of
+ * the tile. */
 static int64_t vcode_bit(int64_t D, int bits, int64_t t, int64_t ch)
 {
-    int64_t hw = 16 / bits, wpt = bits / 2;
-    int64_t tile = t / 16, tt = t % 16, half = tt / 8, w = (tt % 8) / hw, i = (tt % 8) % hw;
-    int64_t tw = tile * wpt + w;
-    int64_t col = bits >= 4 && (tw & 1) ? (ch ^ 8) : ch;
-    return (tw * D + col) * 32 + 16 * half + bits * i;
+    int64_t hw = 16 / bits, wpl = D * bits / 64, sw = wpl < 4 ? wpl : 4;
+    int64_t tile = t / 16, tt = t % 16, half = tt / 8, i = (tt % 8) / 2, s = tt % 2;
+    int64_t q = ch / 16, g = ch % 8, r = (ch % 16) / 8;
+    int64_t lane = 4 * g + i, j = 2 * q + r;
+    int64_t w = 2 * (j / hw) + s;
+    int64_t word = tile * 32 * wpl + (w / sw) * 32 * sw + lane * sw + (w % sw);
+    return word * 32 + 16 * half + bits * (j % hw);
 }
 
 /* FP8 keys: byte of channel ch within a token's D-byte row.  Channel r = ch mod 16 of the

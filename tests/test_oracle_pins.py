@@ -423,7 +423,7 @@ def test_layout_golden_record():
     t = np.arange(16)[:, None]
     c = np.arange(64)[None, :]
     K = ((c + t) % 4).astype(np.float32)
-    V = ((c + 2 * t) % 4).astype(np.float32)
+    V = ((c + c // 8 + t + t // 8) % 4).astype(np.float32)
     kb = _bf16_bits(torch.tensor(K).to(torch.bfloat16)).reshape(1, 16, 1, 64)
     vb = _bf16_bits(torch.tensor(V).to(torch.bfloat16)).reshape(1, 16, 1, 64)
     assert img.append(0, 0, kb, vb) == 0
@@ -443,7 +443,7 @@ def test_layout_golden_record_4bit_tile_order():
     t = np.arange(16)[:, None]
     c = np.arange(64)[None, :]
     K = ((c + t) % 16).astype(np.float32)
-    V = (((c + t) % 16) * np.where(t >= 8, 2, 1)).astype(np.float32)
+    V = (((c % 16 + 4 * (c // 16) + t) % 16) * np.where(t >= 8, 2, 1)).astype(np.float32)
     kb = _bf16_bits(torch.tensor(K).to(torch.bfloat16)).reshape(1, 16, 1, 64)
     vb = _bf16_bits(torch.tensor(V).to(torch.bfloat16)).reshape(1, 16, 1, 64)
     assert img.append(0, 0, kb, vb) == 0
@@ -452,7 +452,7 @@ def test_layout_golden_record_4bit_tile_order():
     assert len(rows) >= 25
     for off, byte in rows:
         assert rec[int(off)] == int(byte, 16), off
-    # every value code reads back as (c + t) mod 16 through the oracle's own dequantiser
+    # every value code reads back through the oracle's own dequantiser
     for tok in range(16):
         _, vt = img.dequant_token(0, 0, 0, tok)
         assert np.array_equal(vt, V[tok]), tok
@@ -500,3 +500,24 @@ def test_packed_tokens_dequantise_to_their_groups():
                 s, z, codes = O.qb_group(vf[0, t, h, 32 * j:32 * j + 32], 4)
                 for cc in (0, 5, 31):
                     assert vt[32 * j + cc] == O.qb_dequant(int(codes[cc]), s, z)
+
+
+@pytest.mark.parametrize("bits,D", [(2, 64), (2, 128), (2, 256), (4, 64), (4, 128), (8, 128), (8, 256)])
+def test_value_codes_round_trip_every_shape(bits, D):
+    # every value code of a two-tile group reads back as the per-token Q_b code of its own
+    # (token, channel): the value-code order is a bijection for each code width and head size
+    cfg = _kivi_cfg(batch=1, bits=bits, head_dim=D, q_heads=2, kv_heads=1, group_k=32, group_v=16,
+                    residual=0, max_tokens=32)
+    img = O.Image(cfg)
+    g = torch.Generator().manual_seed(bits * 1000 + D)
+    k = torch.randn(1, 32, 1, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 32, 1, D, generator=g).to(torch.bfloat16)
+    img.append(0, 0, _bf16_bits(k), _bf16_bits(v))
+    assert img.state(0, 0) == (32, 32)
+    vf = v.float().numpy()
+    for t in range(32):
+        _, vt = img.dequant_token(0, 0, 0, t)
+        for j in range(D // 16):
+            s, z, codes = O.qb_group(vf[0, t, 0, 16 * j:16 * j + 16], bits)
+            want = np.array([O.qb_dequant(int(c), s, z) for c in codes], np.float32)
+            assert np.array_equal(vt[16 * j:16 * j + 16], want), (t, j)
