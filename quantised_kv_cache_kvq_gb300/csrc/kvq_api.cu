@@ -152,6 +152,7 @@ int make_plan(const Layout& lo, DecodePlan* p) {
         p->NQ = 0;
     }
     p->S = p->NRC + p->NQ;
+    if ((int64_t)p->S * units > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;   // one block per (item, unit)
     const int64_t slots = units * p->S * lo.gqa;
     p->ws_o_off = 256;
     p->ws_ml_off = align256(p->ws_o_off + slots * lo.D * 4);

@@ -196,25 +196,31 @@ __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int 
         }
     }
     __syncthreads();
-    // value codes: 32-bit words [token word][column], D columns per token word.  A word's
-    // 16-bit halves hold tokens tt and tt + 8 of a 16-token tile, hw = 16 / bits codes per
-    // half; bits / 2 words per tile; for bits >= 4 odd token words keep channel c in column
-    // c ^ 8 (the decode's lanes then read distinct shared-memory banks)
+    // value codes: per 16-token tile, 32 lanes of wpl = D * bits / 64 words in the order
+    // of the decode's value fragments.  Lane 4g + i, word w = 2 (j / hw) + s: its halves
+    // hold tokens 2i + s and 2i + s + 8, and index j = 2q + r (channel 16q + g + 8r) sits at
+    // bit bits * (j mod hw) of each half (hw = 16 / bits).  A lane's words go in slabs of
+    // sw = min(wpl, 4) so that a warp reads one slab of a tile with one contiguous
+    // 16-byte (or 8-byte) load per lane.
     {
         uint32_t* vrec = reinterpret_cast<uint32_t*>(rec + lo.kc);
-        const int hw = 16 / bits, wpt = bits / 2;
-        const int words = (G / 16) * wpt * D;
+        const int hw = 16 / bits, wpl = D * bits / 64, sw = wpl < 4 ? wpl : 4;
+        const int words = (G / 16) * 32 * wpl;
         for (int k = threadIdx.x; k < words; k += blockDim.x) {
-            const int tw = k / D, col = k % D;
-            const int ch = (bits >= 4 && (tw & 1)) ? (col ^ 8) : col;
-            const int t0w = (tw / wpt) * 16 + (tw % wpt) * hw;   // first token of the low half
-            const uint8_t* src = codes + ch * G;
-            uint32_t w = 0u;
-            for (int e = 0; e < hw; ++e) {
-                w |= static_cast<uint32_t>(src[t0w + e]) << (bits * e);
-                w |= static_cast<uint32_t>(src[t0w + 8 + e]) << (16 + bits * e);
+            const int tile = k / (32 * wpl), kk = k % (32 * wpl);
+            const int slab = kk / (32 * sw), lane = (kk / sw) % 32;
+            const int w = slab * sw + kk % sw;
+            const int g = lane >> 2, i = lane & 3, sbit = w & 1;
+            const int tlo = tile * 16 + 2 * i + sbit;          // token of the low half
+            uint32_t word = 0u;
+            for (int m = 0; m < hw; ++m) {
+                const int j = (w >> 1) * hw + m;
+                const int ch = 16 * (j >> 1) + g + 8 * (j & 1);
+                const uint8_t* src = codes + ch * G;
+                word |= static_cast<uint32_t>(src[tlo]) << (bits * m);
+                word |= static_cast<uint32_t>(src[tlo + 8]) << (16 + bits * m);
             }
-            vrec[k] = w;
+            vrec[k] = word;
         }
     }
     __syncthreads();

@@ -18,12 +18,13 @@
 //           into an fp16 major part and an fp16 minor part (cols 2h, 2h+1), so the fp32
 //           accumulator sees the product to ~22 bits; the per-group offset term
 //           sum_c q_c * zero_c is added in fp32.  (Q_b equation: xhat = code*s + min.)
-//   values  O[c][col] = sum_t code[t][c] * Bp[t][col], A = value codes (stored as
-//           32-bit words [token word][channel], the halves of a word holding tokens tt
-//           and tt + 8 of a tile), Bp = p_t * value scale split into major/minor parts;
+//   values  O[c][col] = sum_t code[t][c] * Bp[t][col], A = value codes (stored per tile
+//           in the order of the A fragments, so a lane reads its codes of a tile with
+//           one or two wide loads), Bp = p_t * value scale split into major/minor parts;
 //           the offset term sum_t p_t * zero_t is one more small product.
-// The bf16 window (KIVI) and INT8 rows go through a CUDA-core row path; FP8 caches run
-// on the tensor cores in kvq_decode_fp8.cu.
+// The bf16 window of a KIVI cache runs on the tensor cores too (window_item); INT8 rows
+// go through a CUDA-core row path; FP8 caches run on the tensor cores in
+// kvq_decode_fp8.cu.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -66,6 +67,27 @@ __host__ __device__ inline ItemRange item_range(const Layout& lo, const DecodePl
         r.t1 = r.t0 + span < qn ? r.t0 + span : qn;
     }
     return r;
+}
+
+// The work of one decode block.  Blocks are numbered item-major over the units (sequence,
+// kv head): first every unit's packed items (the long ones; a unit's last, possibly
+// partial, item last), then the window or row items.  The blocks left over for a second
+// wave of resident blocks are then the short ones.
+struct BlockWork {
+    int item, h, b;
+};
+__device__ __forceinline__ BlockWork block_work(const Layout& lo, const DecodePlan& p) {
+    const uint32_t units = static_cast<uint32_t>(lo.B) * static_cast<uint32_t>(lo.H);
+    const uint32_t k = blockIdx.x / units, u = blockIdx.x - k * units;
+    BlockWork w;
+    w.item = static_cast<int>(k) < p.NQ ? p.NRC + static_cast<int>(k) : static_cast<int>(k) - p.NQ;
+    w.b = static_cast<int>(u / static_cast<uint32_t>(lo.H));
+    w.h = static_cast<int>(u) - w.b * lo.H;
+    return w;
+}
+// Grid of the decode kernels: one block per (item, unit).
+inline dim3 decode_grid(const DecodeArgs& a) {
+    return dim3(static_cast<unsigned>((int64_t)a.plan.S * a.lo.B * a.lo.H));
 }
 
 __device__ __forceinline__ float load_q(const void* q, int64_t idx, int dtype) {
@@ -536,10 +558,11 @@ template <int BITS>
 __device__ __forceinline__ uint32_t code_bits(uint32_t w, int p) {
     return w & ((((1u << BITS) - 1u) << p) * 0x00010001u);
 }
-// Key pair jj of a word (codes at bits BITS*jj and 16 + BITS*jj): the 2-bit codes above
-// bit 8 are first shifted down by 6 (one shift per word), everything else stays in place.
-template <int BITS> constexpr int key_shift(int jj) { return BITS * jj + BITS > 10 ? 6 : 0; }
-template <int BITS> constexpr int key_pos(int jj) { return BITS * jj - key_shift<BITS>(jj); }
+// Code pair jj of a word (codes at bits BITS*jj and 16 + BITS*jj): codes reaching past
+// bit 10 are first shifted down by 6 (one shift per word), everything else stays in place;
+// the pair then sits at bit code_pos of each half.
+template <int BITS> constexpr int code_shift(int jj) { return BITS * jj + BITS > 10 ? 6 : 0; }
+template <int BITS> constexpr int code_pos(int jj) { return BITS * jj - code_shift<BITS>(jj); }
 
 // (s * x) of fp16 pairs split in two fp16 parts by an error-free product: with x = (0,
 // major) -> the rounded product of s and `major`; with x = (major, minor) -> the rounding
@@ -559,22 +582,22 @@ __device__ __forceinline__ uint32_t split_mul(__half2 s, uint32_t x, uint32_t y)
 // Scales.  Scores: A = key codes c * 2^(p - 24), B = q * s_c * 2^(E - p) with E per group
 // such that the largest key scale of the group times 2^E is below 2^15, so the product
 // is c * q * s_c * 2^(E - 24) and the score is the fp32 sum times 2^(24 - E).  Values:
-// A = value codes c * 2^(p - 24), B = P * s_t * 2^(Ev - p) with Ev per warp such that the
+// A = value codes c * 2^(p - 24), B = P * s_t * 2^Ev with Ev per warp such that the
 // largest value scale seen so far times 2^Ev is below 2^15 (lowered, and what was
-// accumulated rescaled by the exact power of two, when a larger scale arrives).
+// accumulated rescaled by the exact power of two, when a larger scale arrives); the code
+// position p is fixed per accumulator element, so 2^(24 - p) is applied at the end.
 template <int D, int BITS, int NT>
 __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& so, int b, int h,
                             int item, int64_t t0, int64_t t1) {
     constexpr int CPW = 32 / BITS;          // key channels per 32-bit word
-    constexpr int HPW = CPW / 2;            // code pairs per word
+    constexpr int HPW = CPW / 2;            // code pairs per word (keys and values)
     constexpr int NPAIR = D / 8;            // code pairs per thread per token row
     constexpr int KSTEPS = D / 16;
     constexpr int ROWW = D * BITS / 128;    // words per thread per key row
     constexpr int ROWB = D * BITS / 8;      // bytes per key row
     constexpr int MTV = D / 16;             // 16-channel tiles of the value contraction
-    constexpr int TPW = 32 / BITS;          // value tokens per word
-    constexpr int HW = TPW / 2;
-    constexpr int VP1 = 2 * BITS <= 10 ? BITS : 0;   // position of the second value pair
+    constexpr int WPL = D * BITS / 64;      // value-code words per lane per tile
+    constexpr int SW = WPL < 4 ? WPL : 4;   // words per lane per slab (one wide load)
     constexpr int MAXT = 8;                 // a warp holds at most 8 tiles (W <= 128 tokens)
     constexpr int QROW = NPAIR + 4;         // words per row of the query tables (padded)
     const Layout& lo = a.lo;
@@ -686,7 +709,6 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     const uint32_t qx_lane = sbase + static_cast<uint32_t>(so.qpa) + lane * QROW * 4;
     const uint32_t qy_lane = sbase + static_cast<uint32_t>(so.qpb) + lane * QROW * 4;
     const int part = g & 1;                 // B column g = 2 * head + part
-    const int re = g & 1;                   // score rows of this lane: odd token slots when 1
     const uint32_t kpar = lo.kc + lo.vc;                    // key params in a record
     const uint32_t vpar = kpar + lo.kp;                     // value params in a record
     const uint32_t kscale_lane = kpar + tig * (D / 2);      // the lane's quarter of the key scales
@@ -696,15 +718,12 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     // (g', t') (h' = g' / 2): 2t' and 2t' + 8 (k slots 2t', 2t' + 1), 2t' + 1 and 2t' + 9
     // (k slots 2t' + 8, 2t' + 9)
     const uint32_t krow0 = g * ROWB + tig * (ROWW * 4), krow1 = (g + 8) * ROWB + tig * (ROWW * 4);
-    // value codes of a tile: BITS / 2 token words, each with the tile's tokens tt and tt + 8
-    // in its two halves; this lane's tokens 2t, 2t + 8 and 2t + 1, 2t + 9 sit in word vwi at
-    // bits BITS * i0 and BITS * (i0 + 1) of each half: a right shift by BITS * i0 brings
-    // them to bits 0 and BITS.  Odd token words (BITS >= 4) keep channel c in column c ^ 8.
-    const int vwi = (2 * tig) / HW, i0 = (2 * tig) % HW;
-    const uint32_t vsh = BITS * i0;
-    const uint32_t vswz = (BITS >= 4 && (vwi & 1)) ? 8u : 0u;
-    const uint32_t vcol0 = 4 * (g ^ vswz), vcol1 = 4 * ((g + 8) ^ vswz);
-    const uint32_t vword_lane = lo.kc + vwi * 4 * D;
+    // value codes of a tile: 32 lanes of WPL words in slabs of SW; lane (g, t) holds, for
+    // every 16-channel tile q, its A fragment: the codes of channels 16q + g (r = 0) and
+    // 16q + g + 8 (r = 1) for tokens 2t, 2t + 8 (even words, k slots 2t, 2t + 1) and
+    // 2t + 1, 2t + 9 (odd words, k slots 2t + 8, 2t + 9), index j = 2q + r at bits
+    // BITS * (j mod HPW) of word pair j / HPW
+    const uint32_t vlane = lo.kc + lane * SW * 4;
     // value scales and zeros: [group][G] fp16 with tile token tt at position 2 (tt mod 8) +
     // tt / 8, so this lane's four tokens are the 8 bytes at tile position 4t
     const uint32_t vscale_lane = vpar + 8 * tig;
@@ -819,7 +838,7 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                             const int wi = m / HPW, jj = m % HPW;
                             const int lo_l = wi * CPW + jj, hi_l = lo_l + HPW;
                             sp[m] = __hmul2(u32_as_h2(prmt(sreg[lo_l / 2], sreg[hi_l / 2], (jj & 1) ? 0x7632u : 0x5410u)),
-                                            u32_as_h2(exp2i_h2(E - key_pos<BITS>(jj))));
+                                            u32_as_h2(exp2i_h2(E - code_pos<BITS>(jj))));
                         }
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
@@ -851,10 +870,10 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                             const int m0 = 2 * ks, m1 = 2 * ks + 1;
                             const int j0 = m0 % HPW, j1 = m1 % HPW;
                             uint32_t af[4];
-                            af[0] = code_bits<BITS>(wa[m0 / HPW] >> key_shift<BITS>(j0), key_pos<BITS>(j0));
-                            af[1] = code_bits<BITS>(wb[m0 / HPW] >> key_shift<BITS>(j0), key_pos<BITS>(j0));
-                            af[2] = code_bits<BITS>(wa[m1 / HPW] >> key_shift<BITS>(j1), key_pos<BITS>(j1));
-                            af[3] = code_bits<BITS>(wb[m1 / HPW] >> key_shift<BITS>(j1), key_pos<BITS>(j1));
+                            af[0] = code_bits<BITS>(wa[m0 / HPW] >> code_shift<BITS>(j0), code_pos<BITS>(j0));
+                            af[1] = code_bits<BITS>(wb[m0 / HPW] >> code_shift<BITS>(j0), code_pos<BITS>(j0));
+                            af[2] = code_bits<BITS>(wa[m1 / HPW] >> code_shift<BITS>(j1), code_pos<BITS>(j1));
+                            af[3] = code_bits<BITS>(wb[m1 / HPW] >> code_shift<BITS>(j1), code_pos<BITS>(j1));
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) mma_16816(acc[ks & 1][nt], af, bq[nt][m0], bq[nt][m1]);
                         }
@@ -926,9 +945,9 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                         for (int e = 0; e < 4; ++e) oacc[mt][nt][e] *= alpha;
                 }
                 mrun[nt] = mnew;
-                // p' = 2^(s - max + Ev - re * VP1): the value operand's power-of-two scale
-                // for this lane's token slots, applied in the exponent
-                mE[nt] = mnew - static_cast<float>(Ev - re * VP1);
+                // p' = 2^(s - max + Ev): the value operand's power-of-two scale, applied
+                // in the exponent
+                mE[nt] = mnew - static_cast<float>(Ev);
             }
             // ---- pass 2: p' and the value contraction, tile by tile; the value-group
             // size is a template parameter so the per-group operand rebuilds unroll
@@ -976,7 +995,18 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                             zC8 = z8.y & zmask8;
                         }
                         const uint32_t vsc = ro + vscale_lane + 2 * ti;
-                        const uint32_t vrow = ro + vword_lane + (ti / 16) * (BITS / 2) * 4 * D;
+                        const uint32_t vtile = ro + vlane + (ti / 16) * (2 * D * BITS);
+                        uint32_t vw[WPL <= 8 ? WPL : SW];
+                        if constexpr (WPL <= 8) {
+                            // the whole tile: slab sl of the lane's words is 128 * SW bytes on
+#pragma unroll
+                            for (int sl = 0; sl < WPL / SW; ++sl) {
+                                uint32_t part[SW];
+                                lds_words<SW>(vtile + sl * 128 * SW, part);
+#pragma unroll
+                                for (int x = 0; x < SW; ++x) vw[sl * SW + x] = part[x];
+                            }
+                        }
                         uint32_t bv[NT][2];
 #pragma unroll
                         for (int q = 0; q < MTV; ++q) {
@@ -989,23 +1019,27 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
                                     bv[nt][1] = split_mul(u32_as_h2(sc.y), px2[nt], py2[nt]);
                                 }
                             }
-                            const uint32_t w0 = lds32(vrow + vcol0 + 64 * q) >> vsh;
-                            const uint32_t w1 = lds32(vrow + vcol1 + 64 * q) >> vsh;
+                            // word pair of q: even word (k slots 2t, 2t + 1), odd word (2t + 8,
+                            // 2t + 9); rows g at pair j = 2q, rows g + 8 at pair 2q + 1
+                            const int w0 = 2 * ((2 * q) / HPW), m0 = (2 * q) % HPW, m1 = m0 + 1;
+                            if constexpr (WPL > 8) {
+                                // wide codes: one slab at a time, loaded by its first q
+                                if (w0 % SW == 0 && m0 == 0) lds_words<SW>(vtile + (w0 / SW) * 128 * SW, vw);
+                            }
+                            const uint32_t e = vw[(WPL <= 8 ? w0 : w0 % SW)];
+                            const uint32_t o = vw[(WPL <= 8 ? w0 : w0 % SW) + 1];
                             uint32_t af[4];
-                            af[0] = code_bits<BITS>(w0, 0);
-                            af[1] = code_bits<BITS>(w1, 0);
-                            af[2] = code_bits<BITS>(VP1 ? w0 : (w0 >> BITS), VP1);
-                            af[3] = code_bits<BITS>(VP1 ? w1 : (w1 >> BITS), VP1);
+                            af[0] = code_bits<BITS>(e >> code_shift<BITS>(m0), code_pos<BITS>(m0));
+                            af[1] = code_bits<BITS>(e >> code_shift<BITS>(m1), code_pos<BITS>(m1));
+                            af[2] = code_bits<BITS>(o >> code_shift<BITS>(m0), code_pos<BITS>(m0));
+                            af[3] = code_bits<BITS>(o >> code_shift<BITS>(m1), code_pos<BITS>(m1));
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) mma_16816(oacc[q][nt], af, bv[nt][0], bv[nt][1]);
                         }
                         {
-                            // the second k-slot pair carries 2^-VP1 in p': undo it (exactly)
                             uint32_t af[4] = {zA, zA8, zC, zC8};
 #pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-                                mma_16816(ozacc[nt], af, py1[nt],
-                                          h2_as_u32(__hmul2(u32_as_h2(py2[nt]), u32_as_h2(exp2i_h2(VP1)))));
+                            for (int nt = 0; nt < NT; ++nt) mma_16816(ozacc[nt], af, py1[nt], py2[nt]);
                         }
                     }
                     ro += rec;
@@ -1027,7 +1061,7 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     // add the value offset term, combine the 4 warps in shared memory
     float* cw = comb + warp * gqa * D;
     const bool wlive = live && mrun[0] > -INFINITY;
-    const float ofac = exp2i(24 - Ev), zfac = exp2i(-Ev), lfac = exp2i(re * VP1 - Ev);
+    const float zfac = exp2i(-Ev), lfac = exp2i(-Ev);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int head = 4 * nt + tig;
@@ -1041,10 +1075,13 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
             const int gv = mt >> gvs;
             const float zsrc = gv < 8 ? oz01 : oz23;
             const float oz = __shfl_sync(0xffffffffu, zsrc, (gv & 7) * 4 + tig) * zfac;
+            // codes of rows g sat at bit code_pos of pair 2 mt, rows g + 8 of pair 2 mt + 1
+            const int m0 = (2 * mt) % HPW;
+            const float f0 = exp2i(24 - code_pos<BITS>(m0) - Ev), f1 = exp2i(24 - code_pos<BITS>(m0 + 1) - Ev);
             if (head < gqa && wlive) {
                 const int c0 = 16 * mt + g;
-                cw[head * D + c0] = fmaf(oacc[mt][nt][0] + oacc[mt][nt][1], ofac, oz);
-                cw[head * D + c0 + 8] = fmaf(oacc[mt][nt][2] + oacc[mt][nt][3], ofac, oz);
+                cw[head * D + c0] = fmaf(oacc[mt][nt][0] + oacc[mt][nt][1], f0, oz);
+                cw[head * D + c0 + 8] = fmaf(oacc[mt][nt][2] + oacc[mt][nt][3], f1, oz);
             }
         }
         if (g == 0 && head < gqa) {
@@ -1057,12 +1094,14 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     combine_warps<D>(a, comb, cml, red, b, h, item);
 }
 
-// One block per (item, kv head, sequence).  BITS == 0: no packed path (INT8 / FP8).
+// One block per (item, kv head, sequence), in the order of block_work.  BITS == 0: no
+// packed path (INT8 rows).
 template <int D, int BITS, int NT>
 __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2) k_decode(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     grid_dependency_wait();
-    const int item = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const BlockWork bw = block_work(a.lo, a.plan);
+    const int item = bw.item, h = bw.h, b = bw.b;
     const int32_t* st = state_ptr(a.lo, a.cache, a.layer, b);
     const int64_t n = st[0], qn = st[1];
     const ItemRange r = item_range(a.lo, a.plan, item, n, qn);
@@ -1088,8 +1127,7 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(a.plan.smem)) !=
             cudaSuccess)
         return KVQ_ERR_CUDA;
-    dim3 grid(a.plan.S, a.lo.H, a.lo.B);
-    return launch_dependent(fn, grid, kDecodeThreads, static_cast<size_t>(a.plan.smem), stream, a) == cudaSuccess
+    return launch_dependent(fn, decode_grid(a), kDecodeThreads, static_cast<size_t>(a.plan.smem), stream, a) == cudaSuccess
                ? KVQ_OK
                : KVQ_ERR_CUDA;
 }

@@ -305,12 +305,13 @@ __device__ void fp8_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& 
     combine_warps<D>(a, comb, cml, red, b, h, item);
 }
 
-// One block per (item, kv head, sequence).
+// One block per (item, kv head, sequence), in the order of block_work.
 template <int D, int NT>
 __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2) k_decode_fp8(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     grid_dependency_wait();
-    const int item = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const BlockWork bw = block_work(a.lo, a.plan);
+    const int item = bw.item, h = bw.h, b = bw.b;
     const int32_t* st = state_ptr(a.lo, a.cache, a.layer, b);
     const int64_t n = st[0], qn = st[1];
     const ItemRange r = item_range(a.lo, a.plan, item, n, qn);
@@ -329,8 +330,7 @@ int launch_fp8_t(const DecodeArgs& a, cudaStream_t stream) {
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(a.plan.smem)) !=
             cudaSuccess)
         return KVQ_ERR_CUDA;
-    dim3 grid(a.plan.S, a.lo.H, a.lo.B);
-    return launch_dependent(fn, grid, kDecodeThreads, static_cast<size_t>(a.plan.smem), stream, a) == cudaSuccess
+    return launch_dependent(fn, decode_grid(a), kDecodeThreads, static_cast<size_t>(a.plan.smem), stream, a) == cudaSuccess
                ? KVQ_OK
                : KVQ_ERR_CUDA;
 }
