@@ -11,12 +11,12 @@
 //            everything a decode block needs for G tokens, so a run of groups is one
 //            contiguous span (one bulk copy):
 //              K codes  G*D*b/8 B, token-major: (token t, channel c) at bit (t*D + c)*b
-//              V codes  D*G*b/8 B of 32-bit words [token word][column], D columns per
-//                       token word, 32/b tokens per word: in each 16-token tile, token tt
-//                       lies in half tt / 8 (a word's halves hold tokens tt and tt + 8),
-//                       word (tt mod 8) / (16/b) of the tile's b/2 words, at bit
-//                       b * ((tt mod 8) mod (16/b)) of the half; for b >= 4, odd token
-//                       words keep channel c in column c ^ 8
+//              V codes  D*G*b/8 B of 32-bit words, 2*D*b B per 16-token tile, in the
+//                       order of the decode's value fragments: 32 lanes of wpl = D*b/64
+//                       words, lane 4g + i holding tokens 2i + s (low half) and 2i + s + 8
+//                       (high half) in its words 2m + s, with channel 16q + g + 8r
+//                       (j = 2q + r) at bit b * (j mod 16/b) of word pair j / (16/b); a
+//                       lane's words sit in slabs of min(wpl, 4), lanes contiguous
 //              K params 4*D B: fp16 scale[D] then fp16 zero[D] (per channel, "min")
 //              V params 4*G*(D/Gv) B: fp16 scale[D/Gv][G] then fp16 zero[D/Gv][G], tile
 //                       token tt of a group's row at position 2 (tt mod 8) + tt / 8
@@ -25,7 +25,10 @@
 //   INT8     per (layer, sequence, kv head), T16 = max_tokens rounded up to 16:
 //            K codes int8[T16][D], V codes int8[T16][D], K scale f32[T16], V scale f32[T16]
 //   FP8      scale table f32[layers][kv heads][2] (K, V), then per (layer, sequence, kv
-//            head): K codes e4m3[T16][D], V codes e4m3[T16][D]
+//            head): K codes e4m3[T16][D], each row's channels in fragment order (channel
+//            r of 16-channel block kb in quarter (r mod 8)/2 at byte 4 kb + 2 (r/8) +
+//            r mod 2); V codes e4m3 in 16-token tiles [channel][16], token tt at byte
+//            4 ((tt mod 8)/2) + 2 (tt mod 2) + tt/8
 // Bits are numbered LSB-first within a byte.
 #pragma once
 
@@ -71,7 +74,7 @@ struct SmemOffsets {
 __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const DecodePlan& p) {
     SmemOffsets o;
     int64_t off = 0;
-    o.bar = off;   off += 64;                         // one mbarrier per warp
+    o.bar = off;   off += 64;                         // mbarriers, one per stage
     o.red = off;   off += 4 * 32 * 4;                 // [warp][32] floats
     o.hstat = off; off += 2 * 32 * 4;                 // per-head max and sum
     o.qs = off;    off += (int64_t)lo.gqa * lo.D * 4; // scaled query, fp32
