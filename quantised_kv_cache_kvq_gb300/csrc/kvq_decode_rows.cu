@@ -1,5 +1,5 @@
-// kvq_decode_rows.cu -- decode kernels for INT8 and FP8 caches, the log-sum-exp merge of
-// the per-chunk partial results, and the decode dispatcher.
+// kvq_decode_rows.cu -- the INT8 decode dispatch, the log-sum-exp merge of the per-chunk
+// partial results, and the decode dispatcher.
 #include "kvq_decode.cuh"
 
 namespace kvq {
@@ -87,6 +87,71 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(DecodeArgs a, int nwc) 
     }
 }
 
+// The same merge for plans with at most kSmallS chunks per (sequence, query head): one
+// thread per output element loads all of its chunks' partials at once, so the whole merge
+// is one wave of small blocks with two rounds of loads.
+constexpr int kSmallS = 4;
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) k_merge_small(DecodeArgs a) {
+    grid_dependency_wait();
+    const Layout& lo = a.lo;
+    const int64_t idx = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x;   // (b, hq, c)
+    if (idx >= (int64_t)lo.B * lo.Hq * D) return;
+    const int c = static_cast<int>(idx % D);
+    const int64_t bh = idx / D;
+    const int hq = static_cast<int>(bh % lo.Hq), b = static_cast<int>(bh / lo.Hq);
+    const int h = hq / lo.gqa, head = hq % lo.gqa;
+    const int S = a.plan.S;
+    const float* ml = reinterpret_cast<const float*>(a.ws + a.plan.ws_ml_off);
+    const float* o = reinterpret_cast<const float*>(a.ws + a.plan.ws_o_off);
+    const int64_t slot0 = (((int64_t)b * lo.H + h) * S) * lo.gqa + head;
+    float mv[kSmallS], lv[kSmallS], ov[kSmallS];
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kSmallS; ++k) {
+        mv[k] = -INFINITY;
+        lv[k] = 0.0f;
+        ov[k] = 0.0f;
+        if (k < S) {
+            const int64_t sl = slot0 + (int64_t)k * lo.gqa;
+            const float2 mlv = *reinterpret_cast<const float2*>(ml + 2 * sl);
+            const float ovl = o[sl * D + c];
+            mv[k] = mlv.y > 0.0f ? mlv.x : -INFINITY;
+            lv[k] = mlv.y > 0.0f ? mlv.y : 0.0f;
+            ov[k] = mlv.y > 0.0f ? ovl : 0.0f;
+        }
+        M = fmaxf(M, mv[k]);
+    }
+    float L = 0.0f, v = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kSmallS; ++k) {
+        const float w = lv[k] > 0.0f ? fast_exp2(mv[k] - M) : 0.0f;
+        v = fmaf(ov[k], w, v);
+        L = fmaf(lv[k], w, L);
+    }
+    a.out[idx] = L > 0.0f ? v / L : 0.0f;
+}
+
+template <int D>
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
+    const Layout& lo = a.lo;
+    if (a.plan.S <= kSmallS) {
+        const int64_t n = (int64_t)lo.B * lo.Hq * D;
+        return launch_dependent(k_merge_small<D>, dim3(static_cast<unsigned>((n + kMergeThreads - 1) / kMergeThreads)),
+                                kMergeThreads, 0, stream, a);
+    }
+    // warps over chunks: enough for one round of 12 chunks each (at most all 8), the rest
+    // of the block's warps over channels (at most D / 32)
+    int nwi = 1;
+    while (nwi < kMergeThreads / 32 && nwi * 12 < a.plan.S) nwi *= 2;
+    int nwc = kMergeThreads / 32 / nwi;
+    if (nwc > D / 32) {
+        nwc = D / 32;
+        nwi = kMergeThreads / 32 / nwc;
+    }
+    return launch_dependent(k_merge<D>, dim3(D / (32 * nwc), lo.Hq, lo.B), kMergeThreads, 0, stream, a, nwc);
+}
+
 }  // namespace
 
 int launch_decode_rows(const DecodeArgs& a, cudaStream_t stream) {
@@ -121,22 +186,12 @@ int launch_decode(const Layout& lo, const DecodePlan& plan, const uint8_t* cache
         rc = launch_decode_rows(a, stream);
     }
     if (rc != KVQ_OK) return rc;
-    // warps over chunks: enough for one round of 12 chunks each (at most all 8), the rest
-    // of the block's warps over channels (at most D / 32)
-    int nwi = 1;
-    while (nwi < kMergeThreads / 32 && nwi * 12 < plan.S) nwi *= 2;
-    int nwc = kMergeThreads / 32 / nwi;
-    if (nwc > lo.D / 32) {
-        nwc = lo.D / 32;
-        nwi = kMergeThreads / 32 / nwc;
-    }
-    const dim3 mgrid(lo.D / (32 * nwc), lo.Hq, lo.B);
     cudaError_t e;
     switch (lo.D) {
-        case 32: e = launch_dependent(k_merge<32>, mgrid, kMergeThreads, 0, stream, a, nwc); break;
-        case 64: e = launch_dependent(k_merge<64>, mgrid, kMergeThreads, 0, stream, a, nwc); break;
-        case 128: e = launch_dependent(k_merge<128>, mgrid, kMergeThreads, 0, stream, a, nwc); break;
-        default: e = launch_dependent(k_merge<256>, mgrid, kMergeThreads, 0, stream, a, nwc); break;
+        case 32: e = launch_merge<32>(a, stream); break;
+        case 64: e = launch_merge<64>(a, stream); break;
+        case 128: e = launch_merge<128>(a, stream); break;
+        default: e = launch_merge<256>(a, stream); break;
     }
     return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
