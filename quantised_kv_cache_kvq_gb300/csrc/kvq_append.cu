@@ -351,16 +351,19 @@ __device__ __forceinline__ int new_tokens(const AppendArgs& a, int bi) {
 // (an arrival counter in the sequence's state entry, zero at rest) writes the new ones.
 __global__ void __launch_bounds__(kThreads) k_append_small(AppendArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
-    grid_launch_dependents();   // a decode launched next may start launching (it waits for us)
     const Layout& lo = a.lo;
     const int h = blockIdx.x, bi = blockIdx.y, b = a.seq_begin + bi;
     if (lo.scheme == KVQ_SCHEME_KIVI && (threadIdx.x >> 5) < a.n_new) {
         // the new rows' addresses do not depend on the cache state: start bringing them
-        // into L2 while the state is read
+        // into L2 (a hint only; nothing is read before the wait below)
         const int64_t row = input_row(lo, a.n_new, bi, threadIdx.x >> 5, h) + (threadIdx.x & 31) * (lo.D / 32);
         prefetch_l2(reinterpret_cast<const uint16_t*>(a.k_new) + row);
         prefetch_l2(reinterpret_cast<const uint16_t*>(a.v_new) + row);
     }
+    // launched as a dependent of the stream's previous kernel: everything it wrote (the
+    // inputs, the cache) is visible after this wait, and nothing is read before it
+    grid_dependency_wait();
+    grid_launch_dependents();   // a decode launched next may start launching (it waits for us)
     int32_t* st = state_ptr(lo, a.cache, a.layer, b);
     const int n = st[0], qn = st[1];
     uint32_t status = 0;
@@ -554,8 +557,9 @@ int launch_append(const Layout& lo, uint8_t* cache, int layer, int seq_begin, in
     const size_t smem = group_smem(lo);
     if (n_new <= kSmallAppend) {
         if (set_smem(reinterpret_cast<const void*>(k_append_small), smem)) return KVQ_ERR_CUDA;
-        k_append_small<<<dim3(lo.H, seq_count), kThreads, smem, stream>>>(a);
-        return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+        return launch_dependent(k_append_small, dim3(lo.H, seq_count), kThreads, smem, stream, a) == cudaSuccess
+                   ? KVQ_OK
+                   : KVQ_ERR_CUDA;
     }
     if (lo.scheme == KVQ_SCHEME_KIVI) {
         // at most (window - 1 + n_new) / G groups leave the window in one append
