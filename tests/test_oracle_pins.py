@@ -521,3 +521,43 @@ def test_value_codes_round_trip_every_shape(bits, D):
             s, z, codes = O.qb_group(vf[0, t, 0, 16 * j:16 * j + 16], bits)
             want = np.array([O.qb_dequant(int(c), s, z) for c in codes], np.float32)
             assert np.array_equal(vt[16 * j:16 * j + 16], want), (t, j)
+
+
+@pytest.mark.parametrize("bits,D", [(2, 128), (4, 128), (8, 64), (2, 256)])
+def test_value_codes_read_lane_by_lane(bits, D):
+    # the value-code order stated lane by lane: in each 16-token tile, lane 4g + i owns
+    # D * bits / 64 words stored in slabs of min(that, 4) words with the 32 lanes of a slab
+    # contiguous; its words 2m + s hold tokens 2i + s (low half) and 2i + s + 8 (high half),
+    # and index j = 2q + r (channel 16q + g + 8r) at bits * (j mod 16/bits) of word pair
+    # m = j / (16/bits).  Read the oracle's record that way and compare with the codes.
+    cfg = _kivi_cfg(batch=1, bits=bits, head_dim=D, q_heads=1, kv_heads=1, group_k=32, group_v=16,
+                    residual=0, max_tokens=32)
+    img = O.Image(cfg)
+    rng = np.random.default_rng(bits + D)
+    lv = (1 << bits) - 1
+    V = rng.integers(0, lv + 1, size=(32, D))
+    V[:, 0::16], V[:, 1::16] = 0, lv               # every value group spans 0..lv: codes = values
+    K = rng.integers(0, 2, size=(32, D))
+    kb = _bf16_bits(torch.tensor(K, dtype=torch.float32).to(torch.bfloat16)).reshape(1, 32, 1, D)
+    vb = _bf16_bits(torch.tensor(V, dtype=torch.float32).to(torch.bfloat16)).reshape(1, 32, 1, D)
+    assert img.append(0, 0, kb, vb) == 0
+    reg = img.regions()
+    rec = bytes(img.buf[reg["data"]:reg["data"] + reg["unit"]])
+    vcodes = rec[32 * D * bits // 8:]
+    wpl, hw = D * bits // 64, 16 // bits
+    sw = min(wpl, 4)
+    for tile in range(2):
+        base = tile * 2 * D * bits
+        for lane in range(32):
+            g, i = lane // 4, lane % 4
+            for w in range(wpl):
+                at = base + 4 * ((w // sw) * 32 * sw + lane * sw + w % sw)
+                word = int.from_bytes(vcodes[at:at + 4], "little")
+                s, m = w % 2, w // 2
+                for jj in range(hw):
+                    j = m * hw + jj
+                    ch = 16 * (j // 2) + g + 8 * (j % 2)
+                    lo = (word >> (bits * jj)) & lv
+                    hi = (word >> (16 + bits * jj)) & lv
+                    t = 16 * tile + 2 * i + s
+                    assert (lo, hi) == (V[t, ch], V[t + 8, ch]), (tile, lane, w, jj)
