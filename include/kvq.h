@@ -35,10 +35,10 @@
  *   queries             [batch][q_heads][head_dim]
  *   decode output       [batch][q_heads][head_dim] fp32
  * Query head hq attends with KV head hq / (q_heads / kv_heads) (grouped-query
- * attention, "Quantizing the KV cache", "Two levers").
+ * attention, "Quantizing the KV cache", "The other big memory user").
  *
- * The byte layout of the cache is specified in full in the design notes of the
- * repository; callers need not depend on it (kvq_cache_bytes gives the size).
+ * The byte layout of the cache is internal to the library (it is restated, for checking,
+ * by the test oracle); callers need not depend on it: kvq_cache_bytes gives the size.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -154,9 +154,10 @@ int kvq_cache_init(const kvq_config* cfg, void* cache, kvq_stream_t stream);
  *                 must stay the same for every append to a layer.  Ignored otherwise.
  *   flags         KVQ_NO_AUTOFLUSH or 0
  * KIVI: tokens enter the bf16 window; whenever the window would hold R + G tokens its
- * oldest G are quantised as one group ("Quantizing the KV cache": KIVI keeps the most
- * recent tokens in full precision and quantizes them as a group once the window fills;
- * the newest R tokens are kept in full precision).  Keys: per channel over the group's
+ * oldest G are quantised as one group ("Quantizing the KV cache", "Keys and values are
+ * shaped differently" and "Per-channel and per-token grouping": recent tokens wait
+ * unquantised in a window that is packed group by group, and the newest R always stay
+ * unquantised).  Keys: per channel over the group's
  * G tokens; values: per token over each Gv channels; parameters s = (max - min) /
  * (2^b - 1) and min are stored as fp16 (min rounded down, s rounded up), codes are
  * round-half-even((x - min) / s) in fp32.  With KVQ_NO_AUTOFLUSH the groups wait in the

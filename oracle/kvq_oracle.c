@@ -240,8 +240,8 @@ float kvqo_qb_dequant(int code, uint16_t scale, uint16_t zero)
     return p + kvqo_half_to_float(zero);
 }
 
-/* [QC] "Workshop" and "Terms / Per-token": symmetric round-to-nearest with one scale
- * for all of a token's values in a head.  Reading: codes in [-127, 127], scale =
+/* [QC] "Workshop" and "Terms / Per-token": symmetric round-to-nearest, one scale per
+ * token and head shared by its D values.  Reading: codes in [-127, 127], scale =
  * max|x| / 127 in binary32, code = round-half-even(x / scale); an all-zero vector gets
  * scale 0 and zero codes. */
 void kvqo_int8_token(const float* x, int n, float* scale_out, int8_t* codes)
@@ -628,9 +628,9 @@ uint32_t kvqo_append(const kvqo_config* c, uint8_t* img, int l, int seq_begin, i
     return st;
 }
 
-/* Quantise every full group still waiting in the window ([QKV] "quantizes them as a
- * group once the window fills"): while the window holds at least R + G tokens, its
- * oldest G become one packed group. */
+/* Quantise every full group still waiting in the window ([QKV] "Keys and values are
+ * shaped differently": a full window is packed as one group): while the window holds at
+ * least R + G tokens, its oldest G become one packed group. */
 void kvqo_flush(const kvqo_config* c, uint8_t* img, int l)
 {
     if (c->scheme != SCHEME_KIVI) return;

@@ -4,7 +4,7 @@
 // An E4M3 value is exactly an fp16 value (3 mantissa bits, exponents inside fp16's
 // range), so the codes go straight into mma.sync.m16n8k16 (f16 -> f32) after one
 // conversion per code pair.  The key and value scales are per (layer, kv head)
-// ("How the KV cache is quantized": per-tensor or per-head scales), so the query operand
+// ("How the KV cache is quantized": one scale per tensor or head), so the query operand
 // (query * key scale, split into fp16 major + minor parts) is built once per block and
 // stays in registers, and the value scale is applied once to the block's output.
 //

@@ -7,7 +7,7 @@ the Llama 3 8B attention layer the cache pages discuss ("Quantizing the KV cache
 pages describe for real caches:
   * keys have a few outlier channels that are large in every token
     ("Keys and values are shaped differently");
-  * some value tokens are larger overall than others (same section).
+  * a few value tokens have a larger magnitude in all their channels (same section).
 
 Recipe (all normal draws N(0, 1), scaling in fp32, then one round-to-nearest-even
 conversion to bf16 when the workload is bf16):

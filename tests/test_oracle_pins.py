@@ -23,8 +23,8 @@ KiB = 2.0 ** 10
 
 # ----------------------------------------------------------------------------- capacity
 def test_llama3_8b_bytes_per_token():
-    # "Quantizing the KV cache", "In an LLM": Llama 3 8B needs 128 KiB per token in 16-bit,
-    # 16 GiB for a 128k-token conversation; FP8 halves it and 4 bits quarter it.
+    # "Quantizing the KV cache", "In an LLM": at 16 bits a Llama 3 8B token takes 128 KiB of
+    # cache and a 128k-token conversation 16 GiB; FP8 halves that and 4 bits quarter it.
     assert O.kv_bytes(32, 8, 128, 1, 2) == 128 * KiB
     assert O.kv_bytes(32, 8, 128, 128 * 1024, 2) == 16 * GiB
     assert O.kv_bytes(32, 8, 128, 128 * 1024, 1) == 8 * GiB
@@ -50,7 +50,7 @@ def test_widget_24gb_32k_one_user():
     # "Quantizing the KV cache", "Try it": context 32k, 1 user, 24 GB GPU:
     # KV 4.0 GiB, weights 4.5-bit 4.2 GiB, 16-bit 15.0 GiB, total 8.2 GiB, 14.1 GiB to spare.
     kv = O.kv_bytes(32, 8, 128, 32768, 2) / GiB
-    w16 = 16.1e9 / GiB                  # 16.1 GB of bf16 weights ("Workshop")
+    w16 = 16.1e9 / GiB                  # the bf16 weights take 16.1 GB ("Workshop")
     w45 = 16.1e9 * 4.5 / 16 / GiB
     assert round(kv, 1) == 4.0
     assert round(w45, 1) == 4.2
@@ -69,8 +69,8 @@ def test_llama7b_glossary_numbers():
 
 
 def test_half_bit_per_value_overhead_at_group_64():
-    # "Quantizing the KV cache", "Try it" caption: 4- and 2-bit caches carry about half a bit per
-    # value of scales and offsets.  With binary16 scale + offset (32 bits) per group of 64 values,
+    # "Quantizing the KV cache", "Try it" caption: the scales and offsets of 4- and 2-bit caches
+    # cost roughly 0.5 extra bits for each value.  With binary16 scale + offset (32 bits) per group of 64 values,
     # the packed records of the layout hold exactly bits + 0.5 bits per value.
     for bits in (2, 4):
         cfg = O.make_config(scheme=0, batch=1, kv_heads=1, head_dim=128, bits=bits, group_k=64,
@@ -267,8 +267,9 @@ def _kivi_cfg(**kw):
 
 
 def test_residual_window_rule_and_bit_identity():
-    # "Quantizing the KV cache", going deeper: the newest R tokens are kept in full precision;
-    # "... quantizes them as a group once the window fills".  After any sequence of appends the
+    # "Quantizing the KV cache", going deeper: the newest R tokens stay unquantised, and a full
+    # window is packed as one group ("Keys and values are shaped differently").  After any
+    # sequence of appends the
     # window holds the newest tokens bit for bit and at least R of them once n >= R.
     cfg = _kivi_cfg()
     img = O.Image(cfg)
