@@ -131,3 +131,15 @@ def test_host_side_argument_checks_before_any_launch():
 def test_status_strings():
     for code in (0, -1, -2, -3, -4, -5, -6, -99):
         assert isinstance(K.status_string(code), str) and K.status_string(code)
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    # the binding has no fallback: without libkvq.so every entry point raises instead of
+    # computing anything on the host
+    monkeypatch.setattr(N, "_lib", None)
+    monkeypatch.setattr(N._build, "LIB", str(tmp_path / "libkvq.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        N.load()
+    cfg = K.make_config(0, 1, 1, 4, 4, 64, 64, bits=2, group_k=16, group_v=16, residual=0)
+    with pytest.raises(RuntimeError, match="not built"):
+        N.kvq_cache_bytes(cfg, 64)
