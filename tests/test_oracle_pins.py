@@ -562,3 +562,43 @@ def test_value_codes_read_lane_by_lane(bits, D):
                     hi = (word >> (16 + bits * jj)) & lv
                     t = 16 * tile + 2 * i + s
                     assert (lo, hi) == (V[t, ch], V[t + 8, ch]), (tile, lane, w, jj)
+
+
+def test_kivi_attention_brute_force_packed_and_window():
+    # a small KIVI cache (packed groups plus the bf16 window, two query heads per KV head):
+    # softmax attention written out here over keys and values rebuilt from the Q_b rule
+    # ("Per-channel and per-token grouping") for the packed tokens and taken as they are for
+    # the window tokens ("Why values per token": o = sum_t p_t V_t)
+    G, Gv, R, D, n, bits = 16, 16, 24, 64, 70, 2
+    cfg = _kivi_cfg(batch=1, q_heads=4, kv_heads=2, head_dim=D, bits=bits, group_k=G, group_v=Gv,
+                    residual=R, max_tokens=96)
+    img = O.Image(cfg)
+    g = torch.Generator().manual_seed(31)
+    k = (torch.randn(1, n, 2, D, generator=g) * 1.5).to(torch.bfloat16)
+    v = torch.randn(1, n, 2, D, generator=g).to(torch.bfloat16)
+    img.append(0, 0, _bf16_bits(k[:, :50]), _bf16_bits(v[:, :50]))
+    for t in range(50, n):
+        img.append(0, 0, _bf16_bits(k[:, t:t + 1]), _bf16_bits(v[:, t:t + 1]))
+    qn = G * ((n - R) // G)
+    assert img.state(0, 0) == (n, qn)
+    kf, vf = k.float().numpy()[0], v.float().numpy()[0]
+    q = torch.randn(1, 4, D, generator=g).to(torch.bfloat16).float().numpy()
+    scale = 0.17
+    out = img.decode(0, q, scale)
+    for hq in range(4):
+        h = hq // 2
+        K = np.array(kf[:, h], np.float64)
+        V = np.array(vf[:, h], np.float64)
+        for g0 in range(0, qn, G):               # keys: per channel over each group of G tokens
+            for ch in range(D):
+                s, z, codes = O.qb_group(kf[g0:g0 + G, h, ch], bits)
+                K[g0:g0 + G, ch] = [O.qb_dequant(int(c), s, z) for c in codes]
+        for t in range(qn):                      # values: per token over each Gv channels
+            for j in range(D // Gv):
+                s, z, codes = O.qb_group(vf[t, h, j * Gv:(j + 1) * Gv], bits)
+                V[t, j * Gv:(j + 1) * Gv] = [O.qb_dequant(int(c), s, z) for c in codes]
+        sc = [scale * sum(float(q[0, hq, i]) * K[t, i] for i in range(D)) for t in range(n)]
+        e = [math.exp(x - max(sc)) for x in sc]
+        den = sum(e)
+        ref = [sum(e[t] / den * V[t, i] for t in range(n)) for i in range(D)]
+        np.testing.assert_allclose(out[0, hq], ref, rtol=1e-11, atol=1e-13)
