@@ -602,3 +602,34 @@ def test_kivi_attention_brute_force_packed_and_window():
         den = sum(e)
         ref = [sum(e[t] / den * V[t, i] for t in range(n)) for i in range(D)]
         np.testing.assert_allclose(out[0, hq], ref, rtol=1e-11, atol=1e-13)
+
+
+def test_fp8_attention_brute_force():
+    # a small FP8 cache: attention written out here over keys and values rebuilt as
+    # e4m3(x / scale) * scale from the (exhaustively pinned) E4M3 codec, one scale per
+    # (layer, KV head) for keys and one for values ("How the KV cache is quantized")
+    cfg = O.make_config(scheme=2, batch=1, q_heads=4, kv_heads=2, head_dim=32, max_tokens=40,
+                        in_dtype=O.DT_F32)
+    img = O.Image(cfg)
+    rng = np.random.default_rng(7)
+    n = 37
+    k = (rng.standard_normal((1, n, 2, 32)) * 3).astype(np.float32)
+    v = rng.standard_normal((1, n, 2, 32)).astype(np.float32)
+    sc = np.array([[0.02, 0.01], [0.015, 0.008]], np.float32)      # [kv head][K, V]
+    img.append(0, 0, k, v, fp8_scales=sc)
+    q = rng.standard_normal((1, 4, 32)).astype(np.float32)
+    out = img.decode(0, q, 0.25)
+
+    def rebuild(x, s):
+        code = int(O.e4m3_from_float(np.float32(np.float32(x) / np.float32(s))))
+        return float(np.float32(O.e4m3_to_float(code)) * np.float32(s))
+
+    for hq in range(4):
+        h = hq // 2
+        K = [[rebuild(k[0, t, h, i], sc[h, 0]) for i in range(32)] for t in range(n)]
+        V = [[rebuild(v[0, t, h, i], sc[h, 1]) for i in range(32)] for t in range(n)]
+        s = [0.25 * sum(float(q[0, hq, i]) * K[t][i] for i in range(32)) for t in range(n)]
+        e = [math.exp(x - max(s)) for x in s]
+        den = sum(e)
+        ref = [sum(e[t] / den * V[t][i] for t in range(n)) for i in range(32)]
+        np.testing.assert_allclose(out[0, hq], ref, rtol=1e-11, atol=1e-13)
