@@ -229,3 +229,17 @@ def test_fp8_long_context_separate_merge():
     p.assert_same_image()
     out, ref = p.decode(0, p.rand_q(g))
     assert_close(out, ref, what="fp8 long")
+
+
+@pytest.mark.parametrize("max_tokens", [512, 600])
+def test_int8_merge_paths_at_the_boundary(max_tokens):
+    # INT8 rows come in items of 128 tokens: 512 tokens of capacity give four items per
+    # (sequence, kv head), merged by the one-thread-per-output merge; 600 give five, merged
+    # by the warp-per-chunk merge.  Ragged fills leave some items empty.
+    p = Pair("int8", batch=3, q_heads=8, kv_heads=2, head_dim=64, max_tokens=max_tokens, in_dtype="bf16")
+    g = gen(max_tokens)
+    k, v = p.rand_kv(3, max_tokens - 8, g)
+    p.append(0, k, v, n_valid=[max_tokens - 8, 130, 5])
+    p.assert_same_image()
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="int8 merge boundary %d" % max_tokens)
