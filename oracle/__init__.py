@@ -17,7 +17,7 @@ from . import build as _build
 
 _lib = None
 
-SCHEME_KIVI, SCHEME_INT8, SCHEME_FP8 = 0, 1, 2
+SCHEME_KIVI, SCHEME_INT8, SCHEME_FP8, SCHEME_FP8_E5M2, SCHEME_INT4 = 0, 1, 2, 3, 4
 DT_BF16, DT_F32 = 0, 1
 ST_CAPACITY, ST_RING_FULL, ST_NONFINITE = 1, 2, 4
 FLAG_NO_AUTOFLUSH = 1
@@ -43,6 +43,9 @@ def lib():
             "kvqo_half_round": (u16, [f32, C.c_int]),
             "kvqo_e4m3_to_float": (f32, [C.c_uint8]),
             "kvqo_e4m3_from_float": (C.c_uint8, [f32]),
+            "kvqo_e5m2_to_float": (f32, [C.c_uint8]),
+            "kvqo_e5m2_from_float": (C.c_uint8, [f32]),
+            "kvqo_int4_token": (None, [P, C.c_int, P, P]),
             "kvqo_qb_group": (None, [P, C.c_int, C.c_int, C.c_int, P, P, P]),
             "kvqo_qb_dequant": (f32, [C.c_int, u16, u16]),
             "kvqo_int8_token": (None, [P, C.c_int, P, P]),
@@ -53,6 +56,7 @@ def lib():
             "kvqo_flush": (None, [P, P, C.c_int]),
             "kvqo_dequant_token": (None, [P, P, C.c_int, C.c_int, C.c_int, i64, P, P]),
             "kvqo_decode": (None, [P, P, C.c_int, C.c_int, C.c_int, P, f64, P]),
+            "kvqo_decode_head": (None, [P, P, C.c_int, C.c_int, C.c_int, P, f64, P]),
             "kvqo_lse_merge": (None, [C.c_int, C.c_int, P, P, P, P]),
             "kvqo_partial": (None, [P, P, C.c_int, C.c_int, C.c_int, i64, i64, P, f64, P, P, P]),
         }
@@ -108,6 +112,22 @@ def qb_group(x, bits):
 
 def qb_dequant(code, scale_bits, zero_bits):
     return lib().kvqo_qb_dequant(int(code), int(scale_bits), int(zero_bits))
+
+
+def e5m2_from_float(x):
+    return lib().kvqo_e5m2_from_float(float(np.float32(x)))
+
+
+def e5m2_to_float(c):
+    return lib().kvqo_e5m2_to_float(int(c))
+
+
+def int4_token(x):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    s = np.zeros(1, np.float32)
+    codes = np.zeros(x.size, np.int8)
+    lib().kvqo_int4_token(_p(x), x.size, _p(s), _p(codes))
+    return float(s[0]), codes
 
 
 def int8_token(x):
@@ -190,6 +210,14 @@ class Image:
         lib().kvqo_decode(C.byref(self.cfg), _p(self.buf), layer, seq_begin, seq_count, _p(q),
                           float(softmax_scale), _p(out))
         return out
+
+    def decode_head(self, layer, q, softmax_scale, seq, kv_head, out):
+        """Writes the outputs of the query heads of (seq, kv_head) into `out` (float64
+        [batch][q_heads][head_dim], C-contiguous); q as for decode."""
+        q = np.ascontiguousarray(q, dtype=np.float32)
+        assert out.dtype == np.float64 and out.flags["C_CONTIGUOUS"]
+        lib().kvqo_decode_head(C.byref(self.cfg), _p(self.buf), layer, seq, kv_head, _p(q),
+                               float(softmax_scale), _p(out))
 
     def partial(self, layer, seq, hq, t0, t1, qrow, softmax_scale):
         D = self.cfg.head_dim

@@ -36,7 +36,8 @@
  * Configuration, mirroring the library's kvq_config field by field.
  * ---------------------------------------------------------------------------------- */
 typedef struct {
-    int32_t scheme;     /* 0 = KIVI asymmetric, 1 = INT8 symmetric per token, 2 = FP8 E4M3 */
+    int32_t scheme;     /* 0 = KIVI asymmetric, 1 = INT8 symmetric per token, 2 = FP8 E4M3,
+                           3 = FP8 E5M2, 4 = INT4 symmetric per token */
     int32_t layers;
     int32_t batch;
     int32_t q_heads;
@@ -50,7 +51,7 @@ typedef struct {
     int32_t in_dtype;   /* 0 = bf16, 1 = fp32 (inputs K, V and q) */
 } kvqo_config;
 
-enum { SCHEME_KIVI = 0, SCHEME_INT8 = 1, SCHEME_FP8 = 2 };
+enum { SCHEME_KIVI = 0, SCHEME_INT8 = 1, SCHEME_FP8 = 2, SCHEME_FP8_E5M2 = 3, SCHEME_INT4 = 4 };
 enum { DT_BF16 = 0, DT_F32 = 1 };
 enum { ST_CAPACITY = 1u, ST_RING_FULL = 2u, ST_NONFINITE = 4u };
 enum { FLAG_NO_AUTOFLUSH = 1u };
@@ -195,6 +196,51 @@ uint8_t kvqo_e4m3_from_float(float xf)
 }
 
 /* ------------------------------------------------------------------------------------
+ * [QKV] "How the KV cache is quantized": FP8 E5M2 (5 exponent bits, bias 15, 2 fraction
+ * bits, IEEE-style: exponent 31 holds the infinities and NaNs; largest finite 57344,
+ * subnormals m * 2^-16).  Encoding rounds to nearest-even and saturates finite overflow
+ * (and infinities) to +-57344; NaN encodes as 0x7f.
+ * ---------------------------------------------------------------------------------- */
+float kvqo_e5m2_to_float(uint8_t c)
+{
+    int sign = c >> 7, e = (c >> 2) & 31, m = c & 3;
+    double v;
+    if (e == 31) v = m ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)m, -16);
+    else v = ldexp(4.0 + m, e - 17);
+    return (float)(sign ? -v : v);
+}
+
+uint8_t kvqo_e5m2_from_float(float xf)
+{
+    if (isnan(xf)) return 0x7f;
+    uint8_t sign = signbit(xf) ? 0x80 : 0;
+    double ax = fabs((double)xf);
+    if (ax >= 57344.0) return sign | 0x7b;  /* saturate (includes infinity) */
+    if (ax == 0.0) return sign;
+    double q;
+    if (ax < ldexp(1.0, -14)) q = ldexp(1.0, -16);
+    else {
+        int k;
+        frexp(ax, &k);
+        q = ldexp(1.0, (k - 1) - 2);
+    }
+    double y = ax / q, lo = floor(y), hi = ceil(y), pick;
+    double dlo = y - lo, dhi = hi - y;
+    if (dlo < dhi) pick = lo;
+    else if (dhi < dlo) pick = hi;
+    else pick = (fmod(lo, 2.0) == 0.0) ? lo : hi;
+    double r = pick * q;
+    if (r > 57344.0) r = 57344.0;
+    if (r < ldexp(1.0, -14)) return sign | (uint8_t)(r / ldexp(1.0, -16));
+    int k;
+    frexp(r, &k);
+    int e = k - 1;
+    int m = (int)((r / ldexp(1.0, e) - 1.0) * 4.0);
+    return sign | (uint8_t)(((e + 15) << 2) | m);
+}
+
+/* ------------------------------------------------------------------------------------
  * [QKV] "Per-channel and per-token grouping", the Q_b equation:
  *   s = (max x - min x) / (2^b - 1),  Q_b(x) = round((x - min x) / s) * s + min x.
  * Stored parameters are binary16: the offset is min x rounded toward -infinity and the
@@ -262,6 +308,28 @@ void kvqo_int8_token(const float* x, int n, float* scale_out, int8_t* codes)
     *scale_out = s;
 }
 
+/* [GL] "kv cache quantization" (INT4, per-token quantization), with the symmetric
+ * per-token rule of [QC] "Workshop" at 4 bits.  Reading: codes in [-7, 7], scale =
+ * max|x| / 7 in binary32, code = round-half-even(x / scale); an all-zero vector gets
+ * scale 0 and zero codes. */
+void kvqo_int4_token(const float* x, int n, float* scale_out, int8_t* codes)
+{
+    float a = 0.0f;
+    for (int i = 0; i < n; i++) a = fmaxf(a, fabsf(x[i]));
+    float s = a / 7.0f;
+    for (int i = 0; i < n; i++) {
+        int code = 0;
+        if (s != 0.0f) {
+            float r = rintf(x[i] / s);
+            if (r < -7.0f) r = -7.0f;
+            if (r > 7.0f) r = 7.0f;
+            code = (int)r;
+        }
+        codes[i] = (int8_t)code;
+    }
+    *scale_out = s;
+}
+
 /* ------------------------------------------------------------------------------------
  * The cache image.  Restated here from the written layout specification (regions
  * aligned to 256 bytes, little-endian):
@@ -281,7 +349,10 @@ void kvqo_int8_token(const float* x, int n, float* scale_out, int8_t* codes)
  *          slots; token t (qn <= t < n) sits in slot t mod C.
  *   INT8:  per (l, b, h) block over T16 = T rounded up to 16:
  *            K codes int8 [T16][D], V codes int8 [T16][D], K scale f32 [T16], V scale f32 [T16]
- *   FP8:   scale table f32 [layers][kv heads][2] (K, V), then per (l, b, h) block:
+ *   INT4:  per (l, b, h) block: K codes [T16][D / 2] bytes, V codes [T16][D / 2] bytes, K scale
+ *            f32 [T16], V scale f32 [T16]; channel c of a row in byte c / 2, the low four
+ *            bits for even c and the high four for odd c, as a 4-bit two's complement
+ *   FP8 (E4M3 and E5M2): scale table f32 [layers][kv heads][2] (K, V), then per (l, b, h) block:
  *            K codes e4m3 [T16][D], each row in the channel order of fp8_kbyte
  *            V codes e4m3 [T16 / 16 tiles][D][16 tokens], tokens in the order of fp8_vbyte
  * Bits are numbered LSB-first within a byte: bit i is bit (i mod 8) of byte i / 8.
@@ -371,6 +442,10 @@ static layout_t make_layout(const kvqo_config* c)
         pos += up256(units * L.cap * 4 * D);
     } else if (c->scheme == SCHEME_INT8) {
         L.unit = L.t16 * (2 * D + 8);
+        L.data = pos;
+        pos += up256(units * L.unit);
+    } else if (c->scheme == SCHEME_INT4) {
+        L.unit = L.t16 * (D + 8);
         L.data = pos;
         pos += up256(units * L.unit);
     } else {
@@ -539,7 +614,8 @@ uint32_t kvqo_append(const kvqo_config* c, uint8_t* img, int l, int seq_begin, i
     int D = c->head_dim, H = c->kv_heads;
     uint32_t st = 0;
     float* row = (float*)malloc(sizeof(float) * D);
-    if (c->scheme == SCHEME_FP8 && fp8_scales) {
+    int fp8 = c->scheme == SCHEME_FP8 || c->scheme == SCHEME_FP8_E5M2;
+    if (fp8 && fp8_scales) {
         float* tab = (float*)(img + L.scales) + (int64_t)l * H * 2;
         for (int i = 0; i < 2 * H; i++) tab[i] = fp8_scales[i];
     }
@@ -602,6 +678,26 @@ uint32_t kvqo_append(const kvqo_config* c, uint8_t* img, int l, int seq_begin, i
             free(codes);
             s[0] = (int32_t)(n + m);
             s[1] = (int32_t)(n + m);
+        } else if (c->scheme == SCHEME_INT4) {
+            int8_t* codes = (int8_t*)malloc((size_t)D);
+            for (int h = 0; h < H; h++) {
+                uint8_t* base = unit_base(c, &L, img, l, b, h);
+                for (int j = 0; j < m; j++) {
+                    int64_t t = n + j;
+                    for (int kv = 0; kv < 2; kv++) {
+                        float sc;
+                        input_row(c, kv ? v_new : k_new, n_new, bi, j, h, row);
+                        kvqo_int4_token(row, D, &sc, codes);
+                        uint8_t* dst = base + kv * L.t16 * (D / 2) + t * (D / 2);
+                        for (int ch = 0; ch < D; ch += 2)
+                            dst[ch / 2] = (uint8_t)((codes[ch] & 15) | ((codes[ch + 1] & 15) << 4));
+                        memcpy(base + L.t16 * D + kv * L.t16 * 4 + t * 4, &sc, 4);
+                    }
+                }
+            }
+            free(codes);
+            s[0] = (int32_t)(n + m);
+            s[1] = (int32_t)(n + m);
         } else {
             const float* tab = (const float*)(img + L.scales) + (int64_t)l * H * 2;
             for (int h = 0; h < H; h++) {
@@ -613,7 +709,8 @@ uint32_t kvqo_append(const kvqo_config* c, uint8_t* img, int l, int seq_begin, i
                         input_row(c, kv ? v_new : k_new, n_new, bi, j, h, row);
                         for (int ch = 0; ch < D; ch++) {
                             int64_t at = kv ? L.t16 * D + fp8_vbyte(D, t, ch) : t * D + fp8_kbyte(D, ch);
-                            base[at] = kvqo_e4m3_from_float(row[ch] / sc);
+                            float y = row[ch] / sc;
+                            base[at] = c->scheme == SCHEME_FP8 ? kvqo_e4m3_from_float(y) : kvqo_e5m2_from_float(y);
                         }
                     }
                 }
@@ -690,11 +787,28 @@ void kvqo_dequant_token(const kvqo_config* c, const uint8_t* img, int l, int b, 
             kout[ch] = (float)kc[ch] * ks;
             vout[ch] = (float)vc[ch] * vs;
         }
+    } else if (c->scheme == SCHEME_INT4) {
+        const uint8_t* kc = base + t * (D / 2);
+        const uint8_t* vc = base + L.t16 * (D / 2) + t * (D / 2);
+        float ks, vs;
+        memcpy(&ks, base + L.t16 * D + t * 4, 4);
+        memcpy(&vs, base + L.t16 * D + L.t16 * 4 + t * 4, 4);
+        for (int ch = 0; ch < D; ch++) {
+            int kn = (kc[ch / 2] >> (4 * (ch & 1))) & 15, vn = (vc[ch / 2] >> (4 * (ch & 1))) & 15;
+            kout[ch] = (float)(kn >= 8 ? kn - 16 : kn) * ks;
+            vout[ch] = (float)(vn >= 8 ? vn - 16 : vn) * vs;
+        }
     } else {
         const float* tab = (const float*)(img + L.scales) + (int64_t)l * c->kv_heads * 2;
         for (int ch = 0; ch < D; ch++) {
-            kout[ch] = kvqo_e4m3_to_float(base[t * D + fp8_kbyte(D, ch)]) * tab[2 * h];
-            vout[ch] = kvqo_e4m3_to_float(base[L.t16 * D + fp8_vbyte(D, t, ch)]) * tab[2 * h + 1];
+            uint8_t kb = base[t * D + fp8_kbyte(D, ch)], vb = base[L.t16 * D + fp8_vbyte(D, t, ch)];
+            if (c->scheme == SCHEME_FP8) {
+                kout[ch] = kvqo_e4m3_to_float(kb) * tab[2 * h];
+                vout[ch] = kvqo_e4m3_to_float(vb) * tab[2 * h + 1];
+            } else {
+                kout[ch] = kvqo_e5m2_to_float(kb) * tab[2 * h];
+                vout[ch] = kvqo_e5m2_to_float(vb) * tab[2 * h + 1];
+            }
         }
     }
 }
@@ -705,45 +819,50 @@ void kvqo_dequant_token(const kvqo_config* c, const uint8_t* img, int l, int b, 
  * hq / (q_heads / kv_heads) (grouped-query sharing, [QKV] "Two levers").  A sequence
  * with no tokens yields a zero output.  q is [batch][q_heads][head_dim] (binary32 values
  * of the caller's query); out is [batch][q_heads][head_dim]. */
+/* The attention of the gqa query heads that read kv head h of sequence b: every token is
+ * dequantised once (its scores for those query heads, its value row kept for the
+ * weighted sum). */
+void kvqo_decode_head(const kvqo_config* c, const uint8_t* img, int l, int b, int h, const float* q,
+                      double softmax_scale, double* out)
+{
+    int D = c->head_dim, Hq = c->q_heads, gqa = c->q_heads / c->kv_heads;
+    const int32_t* s = state_of(c, (uint8_t*)img, l, b);
+    int64_t n = s[0];
+    float* kr = (float*)malloc(sizeof(float) * D);
+    float* vr = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n * D : 1));
+    double* sc = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * gqa : 1));
+    for (int64_t t = 0; t < n; t++) {
+        kvqo_dequant_token(c, img, l, b, h, t, kr, vr + t * D);
+        for (int g = 0; g < gqa; g++) {
+            const float* qq = q + ((int64_t)b * Hq + h * gqa + g) * D;
+            double acc = 0.0;
+            for (int ch = 0; ch < D; ch++) acc += (double)qq[ch] * (double)kr[ch];
+            sc[t * gqa + g] = softmax_scale * acc;
+        }
+    }
+    for (int g = 0; g < gqa; g++) {
+        double* o = out + ((int64_t)b * Hq + h * gqa + g) * D;
+        for (int ch = 0; ch < D; ch++) o[ch] = 0.0;
+        if (n == 0) continue;
+        double mx = -INFINITY;
+        for (int64_t t = 0; t < n; t++) mx = fmax(mx, sc[t * gqa + g]);
+        double den = 0.0;
+        for (int64_t t = 0; t < n; t++) den += exp(sc[t * gqa + g] - mx);
+        for (int64_t t = 0; t < n; t++) {
+            double p = exp(sc[t * gqa + g] - mx) / den;
+            for (int ch = 0; ch < D; ch++) o[ch] += p * (double)vr[t * D + ch];
+        }
+    }
+    free(sc);
+    free(vr);
+    free(kr);
+}
+
 void kvqo_decode(const kvqo_config* c, const uint8_t* img, int l, int seq_begin, int seq_count,
                  const float* q, double softmax_scale, double* out)
 {
-    int D = c->head_dim, Hq = c->q_heads, gqa = c->q_heads / c->kv_heads;
-    float* kr = (float*)malloc(sizeof(float) * D);
-    float* vr = (float*)malloc(sizeof(float) * D);
-    for (int b = seq_begin; b < seq_begin + seq_count; b++) {
-        const int32_t* s = state_of(c, (uint8_t*)img, l, b);
-        int64_t n = s[0];
-        for (int h = 0; h < c->kv_heads; h++) {
-            double* sc = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * gqa : 1));
-            for (int64_t t = 0; t < n; t++) {
-                kvqo_dequant_token(c, img, l, b, h, t, kr, vr);
-                for (int g = 0; g < gqa; g++) {
-                    const float* qq = q + ((int64_t)b * Hq + h * gqa + g) * D;
-                    double acc = 0.0;
-                    for (int ch = 0; ch < D; ch++) acc += (double)qq[ch] * (double)kr[ch];
-                    sc[t * gqa + g] = softmax_scale * acc;
-                }
-            }
-            for (int g = 0; g < gqa; g++) {
-                double* o = out + ((int64_t)b * Hq + h * gqa + g) * D;
-                for (int ch = 0; ch < D; ch++) o[ch] = 0.0;
-                if (n == 0) continue;
-                double mx = -INFINITY;
-                for (int64_t t = 0; t < n; t++) mx = fmax(mx, sc[t * gqa + g]);
-                double den = 0.0;
-                for (int64_t t = 0; t < n; t++) den += exp(sc[t * gqa + g] - mx);
-                for (int64_t t = 0; t < n; t++) {
-                    kvqo_dequant_token(c, img, l, b, h, t, kr, vr);
-                    double p = exp(sc[t * gqa + g] - mx) / den;
-                    for (int ch = 0; ch < D; ch++) o[ch] += p * (double)vr[ch];
-                }
-            }
-            free(sc);
-        }
-    }
-    free(kr);
-    free(vr);
+    for (int b = seq_begin; b < seq_begin + seq_count; b++)
+        for (int h = 0; h < c->kv_heads; h++) kvqo_decode_head(c, img, l, b, h, q, softmax_scale, out);
 }
 
 /* Merge of partial softmax results over disjoint token chunks by log-sum-exp: chunk i

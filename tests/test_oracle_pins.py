@@ -633,3 +633,123 @@ def test_fp8_attention_brute_force():
         den = sum(e)
         ref = [sum(e[t] / den * V[t][i] for t in range(n)) for i in range(32)]
         np.testing.assert_allclose(out[0, hq], ref, rtol=1e-11, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- FP8 E5M2
+def test_e5m2_decode_all_codes():
+    # "How the KV cache is quantized": FP8 as E4M3 or E5M2
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e5m2).float().numpy()
+    got = np.array([O.e5m2_to_float(c) for c in range(256)], np.float32)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])        # infinities included
+
+
+def test_e5m2_encode_exhaustive_bf16():
+    # every finite bfloat16 value, clamped to +-57344 first because the cache saturates while
+    # torch's conversion does not; torch rounds to nearest-even
+    pats = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    x = pats.float()
+    x = x[torch.isfinite(x)]
+    ref = x.clamp(-57344, 57344).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    got = np.array([O.e5m2_from_float(float(v)) for v in x.numpy()], np.uint8)
+    assert np.array_equal(got, ref)
+    assert O.e5m2_from_float(float("inf")) == 0x7B and O.e5m2_from_float(float("-inf")) == 0xFB
+    assert O.e5m2_from_float(float("nan")) == 0x7F
+    # E5M2 is the upper byte of binary16: every code decodes to the binary16 with that high byte
+    for c in range(256):
+        h = np.array([c << 8], np.uint16).view(np.float16)[0]
+        v = O.e5m2_to_float(c)
+        assert (np.isnan(v) and np.isnan(h)) or v == float(h)
+
+
+def test_e5m2_attention_brute_force():
+    # a small E5M2 cache: attention written out here over keys and values rebuilt as
+    # e5m2(x / scale) * scale from the exhaustively pinned codec
+    cfg = O.make_config(scheme=3, batch=1, q_heads=4, kv_heads=2, head_dim=32, max_tokens=40,
+                        in_dtype=O.DT_F32)
+    img = O.Image(cfg)
+    rng = np.random.default_rng(8)
+    n = 35
+    k = (rng.standard_normal((1, n, 2, 32)) * 3).astype(np.float32)
+    v = rng.standard_normal((1, n, 2, 32)).astype(np.float32)
+    sc = np.array([[0.0003, 0.0001], [0.0002, 0.00005]], np.float32)   # [kv head][K, V]
+    img.append(0, 0, k, v, fp8_scales=sc)
+    q = rng.standard_normal((1, 4, 32)).astype(np.float32)
+    out = img.decode(0, q, 0.25)
+
+    def rebuild(x, s):
+        code = int(O.e5m2_from_float(np.float32(np.float32(x) / np.float32(s))))
+        return float(np.float32(O.e5m2_to_float(code)) * np.float32(s))
+
+    for hq in range(4):
+        h = hq // 2
+        K = [[rebuild(k[0, t, h, i], sc[h, 0]) for i in range(32)] for t in range(n)]
+        V = [[rebuild(v[0, t, h, i], sc[h, 1]) for i in range(32)] for t in range(n)]
+        s = [0.25 * sum(float(q[0, hq, i]) * K[t][i] for i in range(32)) for t in range(n)]
+        e = [math.exp(x - max(s)) for x in s]
+        den = sum(e)
+        ref = [sum(e[t] / den * V[t][i] for t in range(n)) for i in range(32)]
+        np.testing.assert_allclose(out[0, hq], ref, rtol=1e-11, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- INT4
+def test_int4_golden_and_invariants():
+    for vals, scale, codes in _golden("int4_cases.txt"):
+        x = np.array([float(v) for v in vals.split()], np.float32)
+        s, c = O.int4_token(x)
+        assert s == float(scale)
+        assert list(c) == [int(v) for v in codes.split()]
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        x = (rng.standard_normal(64) * rng.uniform(0.01, 100)).astype(np.float32)
+        s, c = O.int4_token(x)
+        assert np.abs(c).max() == 7 and c.min() >= -7
+        assert np.all(np.abs(x - c.astype(np.float64) * s) <= s / 2 * (1 + 1e-6))
+
+
+def test_int4_block_layout_golden():
+    cfg = O.make_config(scheme=4, batch=1, q_heads=1, kv_heads=1, head_dim=32, max_tokens=16,
+                        in_dtype=O.DT_F32)
+    img = O.Image(cfg)
+    K = np.zeros((1, 1, 1, 32), np.float32)
+    K[0, 0, 0, :8] = [1, -2, 7, -7, 0, 3, -1, 5]
+    img.append(0, 0, K, -K)
+    reg = img.regions()
+    assert reg["unit"] == 16 * (32 + 8)
+    blk = img.buf[reg["data"]:reg["data"] + reg["unit"]]
+    rows = _golden("layout_int4.txt")
+    assert len(rows) >= 15
+    for off, byte in rows:
+        assert blk[int(off)] == int(byte, 16), off
+    kt, vt = img.dequant_token(0, 0, 0, 0)
+    assert np.array_equal(kt, K[0, 0, 0]) and np.array_equal(vt, -K[0, 0, 0])
+
+
+def test_int4_attention_brute_force():
+    # a small INT4 cache: attention over keys and values rebuilt from the per-token rule
+    cfg = O.make_config(scheme=4, batch=1, q_heads=4, kv_heads=2, head_dim=32, max_tokens=40,
+                        in_dtype=O.DT_F32)
+    img = O.Image(cfg)
+    rng = np.random.default_rng(9)
+    n = 39
+    k = (rng.standard_normal((1, n, 2, 32)) * 2).astype(np.float32)
+    v = rng.standard_normal((1, n, 2, 32)).astype(np.float32)
+    img.append(0, 0, k, v)
+    q = rng.standard_normal((1, 4, 32)).astype(np.float32)
+    out = img.decode(0, q, 0.3)
+
+    def rebuild(x):
+        s, c = O.int4_token(x)
+        return c.astype(np.float32) * np.float32(s)
+
+    for hq in range(4):
+        h = hq // 2
+        K = [rebuild(k[0, t, h]).astype(np.float64) for t in range(n)]
+        V = [rebuild(v[0, t, h]).astype(np.float64) for t in range(n)]
+        s = [0.3 * sum(float(q[0, hq, i]) * K[t][i] for i in range(32)) for t in range(n)]
+        e = [math.exp(x - max(s)) for x in s]
+        den = sum(e)
+        ref = [sum(e[t] / den * V[t][i] for t in range(n)) for i in range(32)]
+        np.testing.assert_allclose(out[0, hq], ref, rtol=1e-11, atol=1e-13)
