@@ -2,14 +2,20 @@
 
 One step = the whole hot path over one batch: append one new bf16 token per sequence
 (quantising and packing a full group whenever the window fills) and run single-query
-decode attention over the packed cache.  Default workload: KIVI 2-bit keys/values,
-Llama-3-8B attention layer shape (32 query / 8 KV heads, head_dim 128), batch 8,
-context 4096, groups of 32, 128-token bf16 window.
+decode attention over the packed cache, for every layer of the workload.
 
-Timing: steps are captured in a CUDA graph and replayed; consecutive steps rotate over
-cache replicas whose total size exceeds the L2 cache, so every step reads its cache from
-HBM.  The dominant kernel (decode attention) is also timed alone for the roofline.
-`--impl reference` times the CPU oracle (tests' reference implementation) instead.
+The headline workload (`--workload`, default the KIVI 2-bit Llama-3-8B layer: 32 query /
+8 KV heads, head_dim 128, batch 8, context 4096, groups of 32, 128-token bf16 window) gives
+the line's `value`; the other workloads of the suite (`--suite`) are measured the same way
+and reported under `workloads`.
+
+Timing: steps are captured in a CUDA graph; consecutive steps rotate over cache replicas
+whose total size exceeds the L2 cache, so every step reads its cache from HBM.  The step
+graph (K steps) is replayed `--replays` times and the median replay gives `value` and
+`ms_per_step`; the decode kernels alone (the roofline's kernel: decode + merge) are timed
+by replaying a K-launch decode graph for at least `--decode-seconds`, median again.  Every
+replay is bracketed by CUDA events on the launching stream.  The end-to-end leg drives the
+public C ABI from pinned host buffers.  `--impl reference` times the CPU oracle instead.
 
 Prints one JSON line (rank 0).
 """
@@ -29,6 +35,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("quantised-cache decode attention tokens/s and achieved HBM GB/s (% of peak), 1 GB300")
 L2_BYTES = 129 * 2 ** 20
+# the timed workloads (the tiny INT8 one is a correctness case, checked by the tests)
+SUITE = ("kivi2_llama3_8b", "kivi4_128k", "fp8_32layer", "serve_mix")
 
 
 def peaks():
@@ -161,25 +169,33 @@ def max_over_ranks(values, world, device="cpu"):
     return t.tolist()
 
 
+def host_cores():
+    return len(os.sched_getaffinity(0))
+
+
 # ---------------------------------------------------------------------------- GPU arm
-def run_gpu(args, w, rank, world):
+def run_gpu(args, w, world, all_layers, nsteps, sampler_on):
+    """Fill the workload's caches, then time the step graph, the decode graph and the
+    end-to-end leg.  Returns a dict of raw timings and byte counts (this rank)."""
     import torch
     import quantised_kv_cache_kvq_gb300 as K
     from quantised_kv_cache_kvq_gb300 import workloads as W
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    K.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
     lens0 = [int(x) for x in W.context_lengths(w).tolist()]
-    layers = w.layers if args.all_layers else 1
+    layers = w.layers if all_layers else 1
     per_cache = layers * decode_bytes(w, lens0)
     # replicas rotated per step so that consecutive steps read their caches from HBM
     reps = max(1, math.ceil(4 * L2_BYTES / per_cache)) if args.replicas <= 0 else args.replicas
     reps = max(reps, 2) if per_cache < 4 * L2_BYTES else reps
-    total_steps = args.warmup + args.steps
-    e2e_steps = min(args.steps, 200)
-    appends_per_rep = math.ceil((total_steps + e2e_steps) / reps) + 1
-    max_tokens = max(lens0) + appends_per_rep + 64
+    e2e_runs, e2e_steps = 5, min(nsteps, 200)
+    # step replays grow every context by about nsteps / reps tokens each: keep the growth
+    # within 2% of the mean context (at least 5 replays)
+    mean0 = sum(lens0) / len(lens0)
+    replays = min(args.replays, max(5, int(0.02 * mean0 * reps / nsteps)))
+    total_steps = args.warmup + nsteps * replays + e2e_steps * e2e_runs
+    appends_per_rep = math.ceil(total_steps / reps) + 1
+    max_tokens = max(lens0) + appends_per_rep + 16
     cfg = K.make_config(w.scheme, layers, w.batch, w.q_heads, w.kv_heads, w.head_dim, max_tokens,
                         bits=w.bits, group_k=w.group_k, group_v=w.group_v, residual=w.residual,
                         in_dtype=w.in_dtype)
@@ -205,45 +221,63 @@ def run_gpu(args, w, rank, world):
         caches.append(c)
     torch.cuda.synchronize()
     t_fill = time.perf_counter() - t_fill
+
+    def check_status(phase):
+        status = 0
+        for c in caches:
+            status |= c.status(stream=None)
+        if status:
+            raise RuntimeError("%s: device status word %#x after the %s" % (w.name, status, phase))
+
+    check_status("fill")
     ws = caches[0].workspace
     # per-step inputs: one new token per sequence (shared by the layers) and the step's queries
-    kn, vn = W.kv_tokens(w, 0, 0, w.batch, max(lens0), total_steps, device=dev, tag="steps")
+    nin = args.warmup + nsteps + e2e_steps
+    kn, vn = W.kv_tokens(w, 0, 0, w.batch, max(lens0), nin, device=dev, tag="steps")
     k_steps = kn.permute(1, 0, 2, 3).contiguous().unsqueeze(2)   # [step][batch][1][H][D]
     v_steps = vn.permute(1, 0, 2, 3).contiguous().unsqueeze(2)
     del kn, vn
     qdt = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
     g = torch.Generator(device=dev)
     g.manual_seed(w.seed * 7919 + 17)
-    q_steps = (torch.randn(total_steps, w.batch, w.q_heads, w.head_dim, generator=g, device=dev)
-               * w.q_mult).to(qdt)
+    q_steps = (torch.randn(nin, w.batch, w.q_heads, w.head_dim, generator=g, device=dev) * w.q_mult).to(qdt)
     outs = [torch.empty(w.batch, w.q_heads, w.head_dim, dtype=torch.float32, device=dev) for _ in range(reps)]
     scale = w.scale
     stream = torch.cuda.Stream(dev)
+    # the inputs were made on the default stream: the timed work runs on `stream`
+    stream.wait_stream(torch.cuda.current_stream())
+    visits = [0] * reps          # steps appended to each replica so far
 
-    def step(i):
-        c = caches[i % reps]
+    def step(i, c):
         for layer in range(layers):
             K.kvq_quantize_append(cfg, c.cache, layer, 0, w.batch, k_steps[i], v_steps[i], 1, fp8_scales=fp8,
                                   stream=stream)
-            K.kvq_decode_attention(cfg, c.cache, layer, q_steps[i], scale, outs[i % reps], ws, stream=stream)
+            K.kvq_decode_attention(cfg, c.cache, layer, q_steps[i], scale, outs[caches.index(c)], ws,
+                                   stream=stream)
 
-    launches_per_step = 3 * layers  # per layer: append (one kernel for a one-token append), decode, merge
-    # warm-up (eager), then the timed steps as one graph
+    def lengths(r):
+        return [n + visits[r] for n in lens0]
+
+    # warm-up (eager), then the timed steps as one graph of nsteps steps
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            step(i)
+            step(i, caches[i % reps])
+            visits[i % reps] += 1
     stream.synchronize()
+    check_status("warm-up steps")
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        for i in range(args.warmup, total_steps):
-            step(i)
-    # decode-only graph over the same rotation, for the dominant kernel's duration
+        for i in range(nsteps):
+            step(args.warmup + i, caches[i % reps])
+    launches_per_step = 3 * layers   # per layer: append (one kernel for one token), decode, merge
+    # decode-only graph over the same rotation: the roofline's kernels alone
     dgraph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(dgraph, stream=stream):
-        for i in range(args.steps):
+        for i in range(nsteps):
             c = caches[i % reps]
             for layer in range(layers):
-                K.kvq_decode_attention(cfg, c.cache, layer, q_steps[i], scale, outs[i % reps], ws, stream=stream)
+                K.kvq_decode_attention(cfg, c.cache, layer, q_steps[args.warmup + i], scale, outs[i % reps], ws,
+                                       stream=stream)
 
     def barrier():
         if world > 1:
@@ -251,53 +285,60 @@ def run_gpu(args, w, rank, world):
             dist.barrier()
         torch.cuda.synchronize()
 
-    sampler = ClockSampler(dev.index)
-    with sampler:
-        time.sleep(0.3)
-        barrier()
-        # graphs replay on the current stream: make it the stream the events are recorded on
+    def replay(gr):
         with torch.cuda.stream(stream):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            graph.replay()
+            gr.replay()
             e1.record(stream)
+        return e0, e1
+
+    sampler = ClockSampler(dev.index) if sampler_on else None
+    if sampler:
+        sampler.__enter__()
+    try:
+        time.sleep(0.3 if sampler else 0.0)
         barrier()
-        step_ms = e0.elapsed_time(e1)
-        # dominant kernel alone (same replicas, L2-cold by rotation)
-        with torch.cuda.stream(stream):
-            d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            d0.record(stream)
-            dgraph.replay()
-            d1.record(stream)
-        stream.synchronize()
-        decode_ms = d0.elapsed_time(d1)
-        time.sleep(0.3)
-    status = 0
-    for c in caches:
-        status |= c.status()
-    if status:
-        raise RuntimeError("device status word %#x after the benchmark" % status)
+        step_ms, step_bytes = [], []
+        for rep_i in range(replays):
+            before = [list(lengths(r)) for r in range(reps)]
+            e0, e1 = replay(graph)
+            for i in range(nsteps):
+                visits[i % reps] += 1
+            stream.synchronize()
+            step_ms.append(e0.elapsed_time(e1))
+            nb = 0
+            seen = [0] * reps
+            for i in range(nsteps):
+                r = i % reps
+                seen[r] += 1
+                nb += layers * decode_bytes(w, [n + seen[r] for n in before[r]])
+            step_bytes.append(nb)
+        barrier()
+        # decode-only replays (the cache does not change): at least --decode-seconds
+        dec_bytes = sum(layers * decode_bytes(w, lengths(i % reps)) for i in range(nsteps))
+        dec_ms = []
+        t_end = time.perf_counter() + args.decode_seconds
+        while len(dec_ms) < replays or time.perf_counter() < t_end:
+            e0, e1 = replay(dgraph)
+            stream.synchronize()
+            dec_ms.append(e0.elapsed_time(e1))
+        time.sleep(0.3 if sampler else 0.0)
+    finally:
+        if sampler:
+            sampler.__exit__(None, None, None)
+    check_status("timed steps")
 
-    # bytes of the timed steps (every replica's sequences grow by one token per visit)
-    def lengths_after(visits):
-        return [n + visits for n in lens0]
-
-    def visits(r, steps_done):
-        return steps_done // reps + (1 if r < steps_done % reps else 0)
-
-    bytes_steps = 0
-    for i in range(args.warmup, total_steps):
-        r = i % reps
-        bytes_steps += layers * decode_bytes(w, lengths_after(visits(r, i) + 1))
-    bytes_decode = sum(layers * decode_bytes(w, lengths_after(visits(i % reps, total_steps)))
-                       for i in range(args.steps))
-
-    # end to end through the C ABI with host buffers: per step copy the new token and the
-    # queries from pinned host memory, append, decode every layer, copy the outputs back.
-    # A step's keys, values and queries sit side by side in one pinned row (each part at a
-    # 256-byte offset), so a step makes one host-to-device copy into a device row whose
-    # views are the library's inputs.
-    parts = [k_steps[:e2e_steps], v_steps[:e2e_steps], q_steps[:e2e_steps]]
+    # end to end through the C ABI with host buffers: per step the new token and the queries
+    # come from pinned host memory (one copy per step: keys, values and queries side by side
+    # in one row, each part at a 256-byte offset), then the append and decode of every layer,
+    # then a copy of the step's result (the last layer's outputs) back to pinned host
+    # memory.  Captured as one graph of
+    # e2e_steps steps in which the copies run on a second stream: the inputs of step i + 1
+    # arrive and the outputs of step i - 1 leave while step i computes (two device input
+    # rows and two output buffers, reused every other step).
+    base = args.warmup + nsteps
+    parts = [k_steps[base:base + e2e_steps], v_steps[base:base + e2e_steps], q_steps[base:base + e2e_steps]]
     sizes = [t[0].numel() * t.element_size() for t in parts]
     offs = [0]
     for n in sizes[:-1]:
@@ -306,48 +347,89 @@ def run_gpu(args, w, rank, world):
     hin = torch.zeros(e2e_steps, row_bytes, dtype=torch.uint8).pin_memory()
     for t, o, n in zip(parts, offs, sizes):
         hin[:, o:o + n].copy_(t.reshape(e2e_steps, -1).view(torch.uint8).cpu())
-    din = torch.empty(row_bytes, dtype=torch.uint8, device=dev)
-    dk, dv, dq = (din[o:o + n].view(t.dtype).view(t.shape[1:]) for t, o, n in zip(parts, offs, sizes))
-    hout = torch.empty(e2e_steps, layers, w.batch, w.q_heads, w.head_dim, dtype=torch.float32).pin_memory()
-    hin_rows = [hin[i] for i in range(e2e_steps)]
-    hout_rows = [[hout[i, layer] for layer in range(layers)] for i in range(e2e_steps)]
-    barrier()
-    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        x0.record(stream)
+    din = [torch.empty(row_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    views = [[d[o:o + n].view(t.dtype).view(t.shape[1:]) for t, o, n in zip(parts, offs, sizes)] for d in din]
+    hout = torch.empty(e2e_steps, w.batch, w.q_heads, w.head_dim, dtype=torch.float32).pin_memory()
+    dout = [torch.empty(layers, w.batch, w.q_heads, w.head_dim, dtype=torch.float32, device=dev) for _ in range(2)]
+    copy_stream = torch.cuda.Stream(dev)
+    egraph = torch.cuda.CUDAGraph()
+    e2e_start = [visits[r] for r in range(reps)]
+    with torch.cuda.graph(egraph, stream=stream):
+        copy_stream.wait_stream(stream)
+        ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
+        ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
+        ev_out = [torch.cuda.Event() for _ in range(e2e_steps)]
+        with torch.cuda.stream(copy_stream):
+            din[0].copy_(hin[0], non_blocking=True)
+            ev_in[0].record(copy_stream)
         for i in range(e2e_steps):
             c = caches[i % reps]
-            din.copy_(hin_rows[i], non_blocking=True)
+            dk, dv, dq = views[i % 2]
+            stream.wait_event(ev_in[i])
+            if i >= 2:
+                stream.wait_event(ev_out[i - 2])     # outputs of step i - 2 have left
             for layer in range(layers):
                 K.kvq_quantize_append(cfg, c.cache, layer, 0, w.batch, dk, dv, 1, fp8_scales=fp8, stream=stream)
-                K.kvq_decode_attention(cfg, c.cache, layer, dq, scale, outs[0], ws, stream=stream)
-                hout_rows[i][layer].copy_(outs[0], non_blocking=True)
-        x1.record(stream)
+                K.kvq_decode_attention(cfg, c.cache, layer, dq, scale, dout[i % 2][layer], ws, stream=stream)
+            ev_done[i].record(stream)
+            with torch.cuda.stream(copy_stream):
+                if i + 1 < e2e_steps:
+                    if i >= 1:
+                        copy_stream.wait_event(ev_done[i - 1])   # input row of step i - 1 is free
+                    din[(i + 1) % 2].copy_(hin[i + 1], non_blocking=True)
+                    ev_in[i + 1].record(copy_stream)
+                copy_stream.wait_event(ev_done[i])
+                hout[i].copy_(dout[i % 2][layers - 1], non_blocking=True)
+                ev_out[i].record(copy_stream)
+        stream.wait_stream(copy_stream)
+    e2e_ms = []
     barrier()
-    e2e_ms = x0.elapsed_time(x1)
+    for run in range(e2e_runs):
+        e0, e1 = replay(egraph)
+        stream.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+        for i in range(e2e_steps):
+            visits[i % reps] += 1
+    barrier()
+    # the last run's outputs came back to the host: check them against the device results of
+    # the same calls (the output buffers of the last two steps)
+    last = e2e_steps - 1
+    if not torch.equal(hout[last], dout[last % 2][layers - 1].cpu()):
+        raise RuntimeError("end-to-end outputs did not come back to the host")
     h2d = row_bytes
-    d2h = layers * outs[0].numel() * 4
-
-    step_ms, decode_ms, e2e_ms = max_over_ranks([step_ms, decode_ms, e2e_ms], world, dev)
-    return dict(step_ms=step_ms, decode_ms=decode_ms, e2e_ms=e2e_ms, e2e_steps=e2e_steps,
-                bytes_steps=bytes_steps, bytes_decode=bytes_decode, reps=reps, layers=layers,
-                cache_mb=per_cache / 1e6, launches=launches_per_step * args.steps,
-                clocks=sampler.summary(), h2d=h2d, d2h=d2h, max_tokens=max_tokens, fill_s=t_fill,
-                mean_context=sum(lens0) / len(lens0))
+    d2h = w.batch * w.q_heads * w.head_dim * 4
+    del egraph, graph, dgraph
+    # the job is as slow as its slowest rank
+    step_med, dec_med, e2e_med = max_over_ranks(
+        [statistics.median(step_ms), statistics.median(dec_ms), statistics.median(e2e_ms)], world, dev)
+    res = dict(step_ms=step_med, step_ms_all=step_ms,
+               step_bytes=statistics.median(step_bytes), decode_ms=dec_med,
+               decode_replays=len(dec_ms), dec_bytes=dec_bytes, e2e_ms=e2e_med,
+               e2e_steps=e2e_steps, reps=reps, layers=layers, cache_mb=per_cache / 1e6,
+               launches=(launches_per_step * nsteps * replays + 2 * layers * nsteps * len(dec_ms)
+                         + launches_per_step * e2e_steps * e2e_runs),
+               clocks=sampler.summary() if sampler else None, h2d=h2d,
+               d2h=d2h, max_tokens=max_tokens, fill_s=t_fill, mean_context=sum(lens0) / len(lens0),
+               nsteps=nsteps, e2e_start=e2e_start)
+    caches.clear()
+    del ws, outs, k_steps, v_steps, q_steps, hin, hout, din, dout
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------- CPU oracle
 def oracle_setup(w, nseq):
     import numpy as np
+    import torch
     import oracle as O
     from quantised_kv_cache_kvq_gb300 import workloads as W
     lens = [int(x) for x in W.context_lengths(w).tolist()[:nseq]]
     n0 = max(lens)
     kw = dict(scheme=w.scheme, layers=1, batch=nseq, q_heads=w.q_heads, kv_heads=w.kv_heads,
-              head_dim=w.head_dim, bits=w.bits, group_k=w.group_k, group_v=w.group_v,
+              head_dim=w.head_dim, bits=w.bits if w.scheme == 0 else 8, group_k=w.group_k, group_v=w.group_v,
               residual=w.residual, max_tokens=n0 + 4096, in_dtype=0 if w.in_dtype == "bf16" else 1)
     img = O.Image(O.make_config(**kw))
-    import torch
     k, v = W.kv_tokens(w, 0, 0, nseq, 0, n0, device="cpu", tag="cpu")
     to = (lambda t: t.view(torch.int16).numpy().view(np.uint16)) if w.in_dtype == "bf16" else (lambda t: t.numpy())
     sc = W.fp8_scales(w, k, v).numpy() if w.scheme == 2 else None
@@ -357,52 +439,107 @@ def oracle_setup(w, nseq):
     return img, q, to(kn), to(vn), sc
 
 
-def oracle_steps(w, img, q, kn, vn, sc, nsteps, seqs_per_step, threads, t_index):
-    """nsteps oracle steps; each appends one token to every sequence and decodes
-    `seqs_per_step` of them (one thread per sequence).  Returns decoded sequences."""
-    nseq = q.shape[0]
-    done = 0
-    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-        for s in range(nsteps):
-            j = (t_index + s) % kn.shape[1]
-            img.append(0, 0, kn[:, j:j + 1], vn[:, j:j + 1], fp8_scales=sc)
-            seqs = [(t_index + s + i) % nseq for i in range(seqs_per_step)]
-            list(ex.map(lambda b: img.decode(0, q, w.scale, seq_begin=b, seq_count=1), seqs))
-            done += seqs_per_step
-    return done
-
-
-def run_oracle(w, steps, warmup, budget_s, adapt_steps=False):
-    """Time the oracle on a bounded sample of the workload.  Returns (tokens/s, seconds,
-    threads, sequences decoded per step, sequences in the image, steps run)."""
+def run_oracle(w, budget_s, max_steps=None, warmup=1):
+    """Time the oracle on a bounded sample of the workload: the first min(batch, 8)
+    sequences of one layer; each step appends one token to every sampled sequence and
+    decodes all of them, one task per (sequence, kv head) on a pool of every host core.
+    After `warmup` untimed steps, steps run until `budget_s` seconds have passed (at most
+    `max_steps`).  Returns a dict."""
+    import numpy as np
     nseq = min(w.batch, 8)
-    cores = len(os.sched_getaffinity(0))
+    cores = host_cores()
     img, q, kn, vn, sc = oracle_setup(w, nseq)
-    threads = min(cores, nseq)
-    t = time.perf_counter()
-    oracle_steps(w, img, q, kn, vn, sc, max(1, warmup), 1, 1, 0)
-    per_seq = (time.perf_counter() - t) / max(1, warmup)
-    if adapt_steps:
-        steps = int(max(1, min(steps, budget_s / max(1e-9, per_seq * nseq / threads))))
-    spp = int(max(1, min(nseq, budget_s / max(1e-9, steps * per_seq) * threads)))
-    t = time.perf_counter()
-    done = oracle_steps(w, img, q, kn, vn, sc, steps, spp, threads, warmup)
-    el = time.perf_counter() - t
-    return done / el, el, threads, spp, nseq, steps
+    out = np.zeros((nseq, w.q_heads, w.head_dim))
+    tasks = [(b, h) for b in range(nseq) for h in range(w.kv_heads)]
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        for i in range(warmup):     # untimed
+            img.append(0, 0, kn[:, i:i + 1], vn[:, i:i + 1], fp8_scales=sc)
+            list(ex.map(lambda t: img.decode_head(0, q, w.scale, t[0], t[1], out), tasks))
+        steps, t0 = 0, time.perf_counter()
+        while True:
+            j = (warmup + steps) % kn.shape[1]
+            img.append(0, 0, kn[:, j:j + 1], vn[:, j:j + 1], fp8_scales=sc)
+            list(ex.map(lambda t: img.decode_head(0, q, w.scale, t[0], t[1], out), tasks))
+            steps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or (max_steps is not None and steps >= max_steps):
+                break
+    return {"tokens_per_s": steps * nseq / el, "seconds": el, "steps": steps, "nseq": nseq, "cores": cores,
+            "tasks": len(tasks)}
+
+
+def cpu_record(w, res, layers):
+    return {"value": res["tokens_per_s"] / layers, "unit": "tokens/s", "cores": res["cores"], "kind": "oracle",
+            "sample": "%d oracle steps on the first %d sequences of one layer (%.1f s): each appends one token "
+                      "to every sequence and decodes all of them, %d (sequence, kv head) tasks on %d host "
+                      "threads%s" % (res["steps"], res["nseq"], res["seconds"], res["tasks"], res["cores"],
+                                     "; divided by the %d layers a token needs" % layers if layers > 1 else "")}
+
+
+# ---------------------------------------------------------------------------- records
+def workload_config(w, layers):
+    ragged = w.context[0] != w.context[1]
+    return {"workload": w.name, "scheme": ["kivi", "int8", "fp8"][w.scheme], "bits": w.bits,
+            "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads, "head_dim": w.head_dim,
+            "context": list(w.context) if ragged else w.context[0], "group_k": w.group_k,
+            "group_v": w.group_v, "residual": w.residual, "layers": layers}
+
+
+def gpu_record(w, r, world, peak, peak_kind):
+    tokens = w.batch * r["nsteps"] * world
+    value = tokens / (r["step_ms"] / 1e3)
+    launches = r["nsteps"] * r["layers"]                 # decode calls in the decode-only graph
+    dec_avg_ms = r["decode_ms"] / launches
+    achieved = (r["dec_bytes"] / launches) / (dec_avg_ms / 1e3) / 1e9
+    step_gbs = r["step_bytes"] / (r["step_ms"] / 1e3) / 1e9
+    traffic = profiled_traffic(w.name, w.scheme) if r["layers"] == 1 else None
+    cfg = workload_config(w, r["layers"])
+    cfg.update({"steps_per_replay": r["nsteps"], "replicas": r["reps"],
+                "cache_mb_per_replica": round(r["cache_mb"], 2), "mean_context": round(r["mean_context"], 1),
+                "fill_s": round(r["fill_s"], 1),
+                "l2": "inputs larger than L2: %d cache replica(s) rotated per step (%.0f MB > 129 MB)"
+                      % (r["reps"], r["reps"] * r["cache_mb"]),
+                "timing": "CUDA graph of the steps replayed %d times (median), decode graph replayed %d "
+                          "times (median); CUDA events on the launch stream"
+                          % (len(r["step_ms_all"]), r["decode_replays"])})
+    rec = {
+        "value": value, "unit": "tokens/s", "ms_per_step": r["step_ms"] / r["nsteps"],
+        "hbm_gbs": step_gbs, "hbm_pct_of_peak": 100.0 * step_gbs / peak, "config": cfg,
+        "roofline": {"kernel": "kvq decode attention (decode kernel + merge)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind, "traffic": traffic,
+                     "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of both kernels, from "
+                                        "profiles/k_decode_%s.md (same kernel sources)" % w.name)
+                     if traffic is not None else None,
+                     "avg_launch_us": 1e3 * dec_avg_ms, "bytes_per_launch": r["dec_bytes"] / launches},
+        "e2e": {"value": w.batch * r["e2e_steps"] * world / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"],
+                "how": "public C ABI (kvq_quantize_append, kvq_decode_attention) in one CUDA graph per run, "
+                       "inputs copied from pinned host memory and outputs copied back every step on a "
+                       "second stream; median of 5 runs"},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    return rec
 
 
 # ---------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="kivi2_llama3_8b")
+    ap.add_argument("--workload", default="kivi2_llama3_8b", help="the headline workload")
+    ap.add_argument("--suite", default="all",
+                    help="other workloads to report under `workloads`: all, none, or a comma list")
     ap.add_argument("--replicas", type=int, default=0, help="cache replicas (0: enough to exceed 4x L2)")
-    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work per run")
+    ap.add_argument("--replays", type=int, default=20, help="timed replays of the step graph (median)")
+    ap.add_argument("--decode-seconds", type=float, default=1.0,
+                    help="minimum duration of the decode-only replays (median)")
+    ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle work per workload")
     ap.add_argument("--all-layers", action="store_true",
-                    help="time every layer of a multi-layer workload in each step (default: one layer)")
+                    help="time every layer of the headline workload in each step (default: one layer)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -411,12 +548,12 @@ def main():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     peak, peak_kind = peaks()
-    ragged = w.context[0] != w.context[1]
-    config = {"workload": w.name, "scheme": ["kivi", "int8", "fp8"][w.scheme], "bits": w.bits,
-              "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads, "head_dim": w.head_dim,
-              "context": list(w.context) if ragged else w.context[0], "group_k": w.group_k,
-              "group_v": w.group_v, "residual": w.residual,
-              "layers": w.layers if args.all_layers else 1}
+    if args.suite == "all":
+        suite = [n for n in SUITE if n != w.name]
+    elif args.suite == "none":
+        suite = []
+    else:
+        suite = [n for n in args.suite.split(",") if n and n != w.name]
 
     if args.impl == "reference":
         if rank != 0:
@@ -424,17 +561,17 @@ def main():
         import __graft_entry__  # noqa: F401  (oracle build)
         from oracle import build as ob
         ob.build()
-        tps, el, threads, spp, nseq, _ = run_oracle(w, args.steps, args.warmup, args.cpu_budget)
-        sample = ("%d steps; each appends one token to %d sequences and decodes %d of them "
-                  "(%d KV heads, contexts of the workload's first %d sequences, one layer)"
-                  % (args.steps, nseq, spp, w.kv_heads, nseq))
-        line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                 "sample": sample},
-                "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        # each of the K timed steps is a bounded oracle step of the workload: one token
+        # appended to every sampled sequence and all of them decoded
+        res = run_oracle(w, budget_s=1e9, max_steps=args.steps, warmup=args.warmup)
+        layers = w.layers if args.all_layers else 1
+        cpu = cpu_record(w, res, layers)
+        line = {"impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * res["seconds"] / res["steps"], "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_config(w, layers),
+                "cpu_baseline": cpu,
+                "e2e": {"value": cpu["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
 
@@ -444,48 +581,54 @@ def main():
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     import __graft_entry__
     __graft_entry__.build()
-    r = run_gpu(args, w, rank, world)
+    import quantised_kv_cache_kvq_gb300 as K
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    K.load()
+    layers = w.layers if args.all_layers else 1
+    r = run_gpu(args, w, world, args.all_layers, args.steps, sampler_on=True)
+    others = {}
+    for name in suite:
+        ow = W.WORKLOADS[name]
+        osteps = max(args.steps, ow.steps)
+        try:
+            others[name] = (ow, run_gpu(args, ow, world, ow.layers > 1, osteps, sampler_on=True))
+        except Exception as exc:     # the other lines stand without it; the error is reported
+            others[name] = (ow, {"error": str(exc)})
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
     if rank != 0:
         return
-    tokens = w.batch * args.steps * world
-    value = tokens / (r["step_ms"] / 1e3)
-    launches = args.steps * r["layers"]                 # decode calls in the decode-only graph
-    dec_avg_ms = r["decode_ms"] / launches
-    achieved = (r["bytes_decode"] / launches) / (dec_avg_ms / 1e3) / 1e9
-    step_gbs = r["bytes_steps"] / (r["step_ms"] / 1e3) / 1e9
-    cpu = None
+    head = gpu_record(w, r, world, peak, peak_kind)
     try:
-        tps, el, threads, spp, nseq, ns = run_oracle(w, 8, 1, args.cpu_budget, adapt_steps=True)
-        cpu = {"value": tps / r["layers"], "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": "%d oracle steps of the same workload on %d sequences, each appending one token "
-                         "to all and decoding %d of them (%.1f s)%s"
-                         % (ns, nseq, spp, el, "; one layer timed, divided by the %d layers a token "
-                            "needs" % r["layers"] if r["layers"] > 1 else "")}
+        cpu = cpu_record(w, run_oracle(w, args.cpu_budget), layers)
     except Exception as exc:  # the GPU number stands without it
         cpu = {"value": None, "unit": "tokens/s", "cores": 0, "kind": "oracle", "sample": "failed: %s" % exc}
-    cfg = dict(config)
-    cfg.update({"replicas": r["reps"], "cache_mb_per_replica": round(r["cache_mb"], 2),
-                "mean_context": round(r["mean_context"], 1), "fill_s": round(r["fill_s"], 1),
-                "l2": "inputs larger than L2: %d cache replica(s) rotated per step (%.0f MB > 129 MB)"
-                      % (r["reps"], r["reps"] * r["cache_mb"]),
-                "timing": "CUDA graph of the timed steps, CUDA events on the launch stream",
-                "parallelism": "replicas" if world > 1 else "single"})
+    head["config"]["parallelism"] = "replicas" if world > 1 else "single"
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": r["step_ms"] / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
-        "hbm_gbs": step_gbs, "hbm_pct_of_peak": 100.0 * step_gbs / peak,
-        "roofline": {"kernel": "kvq decode attention (split-context kernel + merge)", "bound": "hbm",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": profiled_traffic(w.name, w.scheme),
-                     "avg_launch_us": 1e3 * dec_avg_ms,
-                     "bytes_per_launch": r["bytes_decode"] / launches},
-        "cpu_baseline": cpu,
-        "e2e": {"value": w.batch * r["e2e_steps"] * world / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"]},
-        "gpu_launches": r["launches"],
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": head["config"],
+        "hbm_gbs": head["hbm_gbs"], "hbm_pct_of_peak": head["hbm_pct_of_peak"], "roofline": head["roofline"],
+        "cpu_baseline": cpu, "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+        "gpu_launches_counts": "every launch of the library's kernels in all timed regions of this line "
+                               "(step, decode-only and end-to-end replays of every workload)",
         "clocks": r["clocks"],
     }
+    wl = {}
+    for name, (ow, orr) in others.items():
+        if "error" in orr:
+            wl[name] = {"error": orr["error"]}
+            continue
+        rec = gpu_record(ow, orr, world, peak, peak_kind)
+        try:
+            rec["cpu_baseline"] = cpu_record(ow, run_oracle(ow, args.cpu_budget), orr["layers"])
+        except Exception as exc:
+            rec["cpu_baseline"] = {"value": None, "unit": "tokens/s", "cores": 0, "kind": "oracle",
+                                   "sample": "failed: %s" % exc}
+        line["gpu_launches"] += rec["gpu_launches"]
+        wl[name] = rec
+    if wl:
+        line["workloads"] = wl
     print(json.dumps(line))
 
 

@@ -2,7 +2,7 @@
  * kvq.h -- C ABI of the GB300 quantised KV cache library (libkvq.so).
  *
  * The library stores attention keys and values in a packed low-bit cache and runs
- * single-query decode attention over it on one GPU (sm_103a).  Three cache schemes:
+ * single-query decode attention over it on one GPU (sm_103a).  Five cache schemes:
  *
  *   KVQ_SCHEME_KIVI      asymmetric b-bit (b = 2, 4, 8): keys quantised per channel over
  *                        groups of G tokens, values per token over groups of Gv channels,
@@ -16,10 +16,18 @@
  *   KVQ_SCHEME_FP8_E4M3  E4M3 codes with one fp32 scale per (layer, KV head) for keys and
  *                        one for values ("Quantizing the KV cache", "How the KV cache is
  *                        quantized", FP8 KV cache).
+ *   KVQ_SCHEME_FP8_E5M2  the same with E5M2 codes (same section: FP8 as E4M3 or E5M2).
+ *   KVQ_SCHEME_INT4      symmetric round-to-nearest at 4 bits, one fp32 scale per (head,
+ *                        token), codes in [-7, 7] (the glossary "kv cache quantization":
+ *                        INT4 and per-token quantization).
  *
  * Memory ownership: the caller allocates every buffer (the cache, the decode workspace,
- * inputs and outputs) in device memory; the library allocates nothing and keeps no
- * global state.  All device work is enqueued asynchronously on the caller's stream; no
+ * inputs and outputs) in device memory, and every entry point that takes a workspace
+ * allocates nothing.  The one exception is kvq_decode_attention_noalloc, which keeps its
+ * scratch in a fixed array of KVQ_NOALLOC_SCRATCH_BYTES on every GPU that loads the
+ * library (with a small host-side record of that array's address per device); see its
+ * declaration below.  The library also remembers, per device, the SM count and the
+ * resident decode blocks per SM it sizes its decode grid by.  All device work is enqueued asynchronously on the caller's stream; no
  * call synchronises except kvq_read_status.  Pointers marked "device" must be device
  * (or managed) memory; the cache must be 256-byte aligned, every other device pointer
  * 16-byte aligned.
@@ -55,12 +63,14 @@ typedef struct CUstream_st* kvq_stream_t;
 enum kvq_scheme {
     KVQ_SCHEME_KIVI = 0,
     KVQ_SCHEME_INT8 = 1,
-    KVQ_SCHEME_FP8_E4M3 = 2
+    KVQ_SCHEME_FP8_E4M3 = 2,
+    KVQ_SCHEME_FP8_E5M2 = 3,
+    KVQ_SCHEME_INT4 = 4
 };
 
 enum kvq_dtype {
     KVQ_DTYPE_BF16 = 0, /* bfloat16 inputs (required for KIVI: the window stores them as is) */
-    KVQ_DTYPE_F32 = 1   /* fp32 inputs (INT8 and FP8 schemes) */
+    KVQ_DTYPE_F32 = 1   /* fp32 inputs (INT8, INT4 and FP8 schemes) */
 };
 
 enum kvq_bytes_mode {
@@ -98,9 +108,10 @@ enum kvq_status_bits {
  *   batch       number of sequences (>= 1)
  *   q_heads     query heads; q_heads / kv_heads must be 1, 2, 4 or 8
  *   kv_heads    key/value heads
- *   head_dim    channels per head: 64, 128 or 256 (KIVI); 32, 64, 128 or 256 (INT8, FP8)
- *   bits        KIVI: 2, 4 or 8; INT8 and FP8: 8 (the formula mode uses it as the
- *               bits per value, and accepts 16 for an unquantised reference size)
+ *   head_dim    channels per head: 64, 128 or 256 (KIVI); 32, 64, 128 or 256 (INT8, INT4, FP8)
+ *   bits        KIVI: 2, 4 or 8; the other schemes fix their code width and ignore it (the
+ *               formula mode uses it as the bits per value, and accepts 16 for an
+ *               unquantised reference size)
  *   group_k     KIVI G: tokens per key group, a multiple of 16 in [16, 128]
  *   group_v     KIVI Gv: channels per value group, a multiple of 16 dividing head_dim
  *   residual    KIVI R: newest tokens kept in the bf16 window (>= 0)
@@ -149,9 +160,10 @@ int kvq_cache_init(const kvq_config* cfg, void* cache, kvq_stream_t stream);
  *   n_valid       device int32 [seq_count] or NULL: sequence i appends its first
  *                 n_valid[i] rows (0..n_new), the rest of its rows are ignored
  *   fp8_scales    FP8 only, device fp32 [kv_heads][2] = (key scale, value scale) of this
- *                 layer: codes are e4m3(x / scale), round-to-nearest-even, saturating at
- *                 +-448.  The scales are also stored in the cache for decoding, so they
- *                 must stay the same for every append to a layer.  Ignored otherwise.
+ *                 layer: codes are e4m3(x / scale) (saturating at +-448) or e5m2(x /
+ *                 scale) (saturating at +-57344), round-to-nearest-even, NaN to 0x7f.  The
+ *                 scales are also stored in the cache for decoding, so they must stay the
+ *                 same for every append to a layer.  Ignored otherwise.
  *   flags         KVQ_NO_AUTOFLUSH or 0
  * KIVI: tokens enter the bf16 window; whenever the window would hold R + G tokens its
  * oldest G are quantised as one group ("Quantizing the KV cache", "Keys and values are
@@ -164,7 +176,8 @@ int kvq_cache_init(const kvq_config* cfg, void* cache, kvq_stream_t stream);
  * window (which holds R + G tokens) until kvq_flush_group; an append that would overflow
  * it sets KVQ_STATUS_RING_FULL and leaves that sequence unchanged.
  * INT8: each token's key and value per head get scale = max|x| / 127 and codes
- * round-half-even(x / scale).  An append past max_tokens sets KVQ_STATUS_CAPACITY and
+ * round-half-even(x / scale) in [-127, 127]; INT4 the same with max|x| / 7 and codes in
+ * [-7, 7], two per byte (even channel in the low four bits).  An append past max_tokens sets KVQ_STATUS_CAPACITY and
  * leaves that sequence unchanged.  Appends of at most 16 tokens run as one kernel.
  */
 int kvq_quantize_append(const kvq_config* cfg, void* cache, int32_t layer, int32_t seq_begin,
@@ -175,16 +188,30 @@ int kvq_quantize_append(const kvq_config* cfg, void* cache, int32_t layer, int32
 /*
  * kvq_flush_group -- KIVI: quantise every full group waiting in the window of every
  * sequence of `layer`: while a window holds at least R + G tokens, its oldest G tokens
- * become one packed group.  A no-op for the other schemes and for caches appended with
- * automatic flushing.
+ * become one packed group.  This is the window rule of "Quantizing the KV cache": a full
+ * window of recent keys is quantised together as one group ("Keys and values are shaped
+ * differently"), and the newest R tokens stay in full precision ("Per-channel and
+ * per-token grouping", residual length R; "KIVI: A Tuning-Free Asymmetric 2bit
+ * Quantization for KV Cache", "How It Works").  The group's codes and parameters are
+ * those of kvq_quantize_append.  A no-op for the other schemes and for caches appended
+ * with automatic flushing.  Enqueued on `stream`; host argument errors as for
+ * kvq_quantize_append.
  */
 int kvq_flush_group(const kvq_config* cfg, void* cache, int32_t layer, kvq_stream_t stream);
 
 /*
  * kvq_workspace_bytes -- device scratch needed by kvq_decode_attention for this
  * configuration: the per-chunk partial softmax results of the split context, plus a
- * 256-byte header holding the decode status word.
+ * 256-byte header holding the decode status word.  The pages define no split of the
+ * context: splitting a sequence's tokens into chunks that run in parallel and merging
+ * their partial softmax results by log-sum-exp is this library's design for long
+ * contexts (the merge is exact: the chunks' partials give the unsplit softmax).  Host
+ * arithmetic only, no GPU needed: the size is an upper bound that holds for decode grids
+ * of up to KVQ_MAX_DECODE_BLOCKS blocks (the decode uses fewer on smaller GPUs).
+ * out_bytes (host) receives the size.  Returns KVQ_OK, KVQ_ERR_ARG or
+ * KVQ_ERR_UNSUPPORTED.
  */
+#define KVQ_MAX_DECODE_BLOCKS 2048
 int kvq_workspace_bytes(const kvq_config* cfg, uint64_t* out_bytes);
 
 /*
@@ -198,8 +225,17 @@ int kvq_workspace_bytes(const kvq_config* cfg, uint64_t* out_bytes);
  *               decode status word (sticky; clear it with a memset to restart)
  * Every cache byte is read once per step for all the query heads that share it.  The
  * context is split into chunks processed in parallel; their partial results are merged
- * by log-sum-exp.  Calls that overlap on the GPU must not share a workspace.
+ * by log-sum-exp.  The split follows the token counts held in the cache: one wave of
+ * blocks, each taking an equal share of the bytes the step reads.  Calls that overlap on
+ * the GPU must not share a workspace.
+ * Self-test of the bounded waits: when bytes 8..15 of the workspace hold
+ * KVQ_SELFTEST_WAIT_MAGIC (little-endian uint64), every decode block makes its first
+ * staging wait on a barrier that nothing completes.  The wait gives up after its limit
+ * (about one second), the block sets KVQ_STATUS_TIMEOUT, waits for its copy in flight and
+ * leaves empty partial results (the outputs are then 0); the GPU stays usable.  A zeroed
+ * workspace header decodes normally.
  */
+#define KVQ_SELFTEST_WAIT_MAGIC 0x4b56515449434b31ull
 int kvq_decode_attention(const kvq_config* cfg, const void* cache, int32_t layer, const void* q,
                          float softmax_scale, float* out, void* workspace,
                          uint64_t workspace_bytes, kvq_stream_t stream);
@@ -214,8 +250,10 @@ int kvq_decode_attention(const kvq_config* cfg, const void* cache, int32_t layer
  *   library holds in device memory on every GPU that loads it, until the process exits.
  *   Configurations whose kvq_workspace_bytes exceeds it are rejected with
  *   KVQ_ERR_WORKSPACE before anything is enqueued.  The call allocates nothing.
- *   The first call on a device looks the array's device address up (once per device, with
- *   that device current); make that first call before any stream capture.
+ *   The first call on a device looks the array's device address up (with that device
+ *   current) and remembers it for the device's current CUDA context; a later call in a
+ *   new context (after cudaDeviceReset, for example) looks it up again.  Make the first
+ *   call in each context before any stream capture.
  *   Every call on a device shares the one array and it keeps the previous call's
  *   contents: calls that overlap on the GPU (different streams, or threads) race and
  *   corrupt each other's results; serialise them.  Each call clears the array's status
@@ -228,7 +266,13 @@ int kvq_decode_attention_noalloc(const kvq_config* cfg, const void* cache, int32
 
 /*
  * kvq_read_status -- OR of the status words of `cache` and `workspace` (either may be
- * NULL) into *out (host).  Synchronises `stream` to read them.
+ * NULL) into *out (host).  Synchronises `stream` to read them.  The pages define no error
+ * reporting; the status bits name the conditions the pages' method leaves open on a
+ * device: a sequence past its capacity, a window that must not be flushed yet
+ * ("Quantizing the KV cache", "Keys and values are shaped differently": recent tokens
+ * wait in a window of fixed size) and a non-finite value reaching the Q_b quantiser
+ * ("Per-channel and per-token grouping", whose min, max and scale are then undefined).
+ * Returns KVQ_OK, KVQ_ERR_ARG (out is NULL) or KVQ_ERR_CUDA.
  */
 int kvq_read_status(const void* cache, const void* workspace, uint32_t* out, kvq_stream_t stream);
 
@@ -238,7 +282,9 @@ int kvq_read_status(const void* cache, const void* workspace, uint32_t* out, kvq
 int kvq_sequence_lengths(const kvq_config* cfg, const void* cache, int32_t layer, int32_t* n_out,
                          int32_t* qn_out, kvq_stream_t stream);
 
-/* kvq_status_string -- a static description of a KVQ_ERR_* code. */
+/* kvq_status_string -- a static, NUL-terminated description of a KVQ_ERR_* code (never
+ * NULL; unknown codes get "unknown status").  No counterpart on the pages: it only names
+ * this library's host-side error codes. */
 const char* kvq_status_string(int code);
 
 #ifdef __cplusplus

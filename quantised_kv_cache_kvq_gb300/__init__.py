@@ -9,7 +9,8 @@ import math
 
 from ._native import (  # noqa: F401
     EXPORTS, KVQ_BYTES_FORMULA, KVQ_BYTES_LAYOUT, KVQ_DTYPE_BF16, KVQ_DTYPE_F32,
-    KVQ_NO_AUTOFLUSH, KVQ_SCHEME_FP8_E4M3, KVQ_SCHEME_INT8, KVQ_SCHEME_KIVI,
+    KVQ_NO_AUTOFLUSH, KVQ_SCHEME_FP8_E4M3, KVQ_SCHEME_FP8_E5M2, KVQ_SCHEME_INT4, KVQ_SCHEME_INT8,
+    KVQ_SCHEME_KIVI,
     KVQ_STATUS_CAPACITY, KVQ_STATUS_NONFINITE, KVQ_STATUS_RING_FULL, KVQ_STATUS_TIMEOUT,
     KvqConfig, KvqError, kvq_cache_bytes, kvq_cache_init, kvq_decode_attention,
     kvq_decode_attention_noalloc,
@@ -17,14 +18,15 @@ from ._native import (  # noqa: F401
     kvq_workspace_bytes, library_path, load, status_string,
 )
 
-_SCHEMES = {"kivi": KVQ_SCHEME_KIVI, "int8": KVQ_SCHEME_INT8, "fp8": KVQ_SCHEME_FP8_E4M3}
+_SCHEMES = {"kivi": KVQ_SCHEME_KIVI, "int8": KVQ_SCHEME_INT8, "fp8": KVQ_SCHEME_FP8_E4M3,
+            "fp8e5m2": KVQ_SCHEME_FP8_E5M2, "int4": KVQ_SCHEME_INT4}
 
 
 def make_config(scheme, layers, batch, q_heads, kv_heads, head_dim, max_tokens, bits=None,
                 group_k=32, group_v=32, residual=0, in_dtype="bf16") -> KvqConfig:
     s = _SCHEMES[scheme] if isinstance(scheme, str) else int(scheme)
     if bits is None:
-        bits = 8 if s != KVQ_SCHEME_KIVI else 2
+        bits = {KVQ_SCHEME_KIVI: 2, KVQ_SCHEME_INT4: 4}.get(s, 8)
     c = KvqConfig()
     c.scheme, c.layers, c.batch, c.q_heads, c.kv_heads = s, layers, batch, q_heads, kv_heads
     c.head_dim, c.bits, c.group_k, c.group_v, c.residual = head_dim, bits, group_k, group_v, residual

@@ -6,7 +6,7 @@ import os
 
 from . import build as _build
 
-KVQ_SCHEME_KIVI, KVQ_SCHEME_INT8, KVQ_SCHEME_FP8_E4M3 = 0, 1, 2
+KVQ_SCHEME_KIVI, KVQ_SCHEME_INT8, KVQ_SCHEME_FP8_E4M3, KVQ_SCHEME_FP8_E5M2, KVQ_SCHEME_INT4 = 0, 1, 2, 3, 4
 KVQ_DTYPE_BF16, KVQ_DTYPE_F32 = 0, 1
 KVQ_BYTES_FORMULA, KVQ_BYTES_LAYOUT = 0, 1
 KVQ_NO_AUTOFLUSH = 1
@@ -21,6 +21,8 @@ EXPORTS = (
     "kvq_sequence_lengths", "kvq_status_string",
 )
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
+KVQ_MAX_DECODE_BLOCKS = 2048
+KVQ_SELFTEST_WAIT_MAGIC = 0x4b56515449434b31
 
 
 class KvqConfig(C.Structure):

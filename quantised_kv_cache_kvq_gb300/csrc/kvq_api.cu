@@ -2,6 +2,7 @@
 // layout, the decode plan, and kernel launches on the caller's stream.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "kvq_decode.cuh"
 #include "kvq_internal.cuh"
@@ -15,7 +16,7 @@ int make_layout(const kvq_config* c, int64_t max_tokens, Layout* out) {
     if (!c || !out) return KVQ_ERR_ARG;
     Layout lo;
     std::memset(&lo, 0, sizeof lo);
-    if (c->scheme < 0 || c->scheme > 2) return KVQ_ERR_ARG;
+    if (c->scheme < 0 || c->scheme > 4) return KVQ_ERR_ARG;
     if (c->layers < 1 || c->batch < 1 || c->kv_heads < 1 || c->q_heads < c->kv_heads) return KVQ_ERR_ARG;
     if (c->q_heads % c->kv_heads != 0) return KVQ_ERR_ARG;
     if (max_tokens < 1 || max_tokens > (int64_t)1 << 30) return KVQ_ERR_ARG;
@@ -62,8 +63,8 @@ int make_layout(const kvq_config* c, int64_t max_tokens, Layout* out) {
         pos += align256(units * lo.C * 4 * (int64_t)D);
     } else {
         if (!pow2_in(D, 32, 256)) return KVQ_ERR_UNSUPPORTED;
-        if (c->scheme == KVQ_SCHEME_INT8) {
-            lo.unit = (int64_t)lo.T16 * (2 * D + 8);
+        if (is_rows(c->scheme)) {
+            lo.unit = (int64_t)lo.T16 * ((c->scheme == KVQ_SCHEME_INT8 ? 2 * D : D) + 8);
             lo.data_off = pos;
             pos += align256(units * lo.unit);
         } else {
@@ -79,86 +80,120 @@ int make_layout(const kvq_config* c, int64_t max_tokens, Layout* out) {
     return KVQ_OK;
 }
 
-// Decode blocks resident per SM for `smem` bytes of dynamic shared memory: 4 by the
-// kernel's register bound, fewer when 228 KiB of shared memory per SM (1 KiB of it
-// reserved per block) does not hold 4.
+// Decode blocks resident per SM for `smem` bytes of dynamic shared memory, as used to
+// choose between one and two staging buffers: 4 by the kernels' register bound, fewer
+// when 228 KiB of shared memory per SM (1 KiB of it reserved per block) does not hold 4.
+// The grid itself is sized on the device by the occupancy calculator (decode_blocks).
 static int resident_blocks(int64_t smem) {
     const int64_t r = (228 * 1024) / (smem + 1024);
     return r < 4 ? static_cast<int>(r) : 4;
 }
 
+static int64_t ceil16(int64_t bytes) { return (bytes + 15) / 16; }
+
 int make_plan(const Layout& lo, DecodePlan* p) {
     std::memset(p, 0, sizeof *p);
     p->NT = lo.gqa > 4 ? 2 : 1;
-    const int64_t units = (int64_t)lo.B * lo.H;
+    p->NSTAGE = 1;
     if (lo.scheme == KVQ_SCHEME_KIVI) {
         p->CHR = 64;
-        p->NRC = (lo.C + p->CHR - 1) / p->CHR;
         // a warp takes W tokens (a multiple of 16, at least 64) and a block 4 warps, with 4 * W
         // a whole number of groups: W = 16 * (G / gcd(G, 64)) scaled up to 64 or more
         int gg = lo.G, hh = 64;
         while (hh) { const int t = gg % hh; gg = hh; hh = t; }
         const int wstep = 16 * (lo.G / gg);
-        const int W = wstep * ((64 + wstep - 1) / wstep);
-        p->W = W;
-        p->CH = 4 * W;
-        // chunks per item (capacity-based; items beyond a sequence's length exit at once):
-        // as many as make the items fit one wave of resident blocks, so the per-block setup
-        // and combine are paid once per block of a wave and no wave runs part-empty.  At
-        // most 32 chunks per item.
-        const int64_t packed = (int64_t)lo.NG * lo.G;
-        const int64_t chunks = (packed + p->CH - 1) / p->CH;
-        p->CPI = 1;
-        p->NSTAGE = 1;
-        const int res1 = resident_blocks(decode_smem(lo, *p).total);
-        const int64_t slots = (int64_t)kNumSMs * res1;
-        int64_t cpi = (units * chunks + slots - 1) / slots;
-        cpi = cpi < 1 ? 1 : (cpi > 32 ? 32 : cpi);
-        p->CPI = static_cast<int>(cpi);
-        // double-buffer the chunks of multi-chunk items when that costs no resident block
-        if (cpi > 1) {
-            p->NSTAGE = 2;
-            if (resident_blocks(decode_smem(lo, *p).total) < res1) p->NSTAGE = 1;
-        }
-        p->NQ = static_cast<int>((chunks + cpi - 1) / cpi);
-    } else if (lo.scheme == KVQ_SCHEME_FP8_E4M3) {
-        // FP8 on the tensor cores: warps of W = 32 tokens, chunks of 128, as many chunks
-        // per item as make the items fit one wave, double-buffered when that costs no
-        // resident block
-        p->CHR = 0;
-        p->NRC = 0;
+        p->W = wstep * ((64 + wstep - 1) / wstep);
+        p->CH = 4 * p->W;
+        p->cpt0 = ceil16((lo.rec + lo.G - 1) / lo.G);      // group record bytes per token
+        p->cpt1 = ceil16(4 * (int64_t)lo.D);                // bf16 key and value row
+    } else if (is_fp8(lo.scheme)) {
+        p->CHR = 16;
         p->W = 32;
         p->CH = 4 * p->W;
-        const int64_t chunks = (lo.T + p->CH - 1) / p->CH;
-        p->CPI = 1;
-        p->NSTAGE = 1;
-        const int res1 = resident_blocks(decode_smem(lo, *p).total);
-        const int64_t slots = (int64_t)kNumSMs * res1;
-        int64_t cpi = (units * chunks + slots - 1) / slots;
-        cpi = cpi < 1 ? 1 : (cpi > 64 ? 64 : cpi);
-        p->CPI = static_cast<int>(cpi);
-        if (cpi > 1) {
-            p->NSTAGE = 2;
-            if (resident_blocks(decode_smem(lo, *p).total) < res1) p->NSTAGE = 1;
-        }
-        p->NQ = static_cast<int>((chunks + cpi - 1) / cpi);
+        p->cpt0 = ceil16(2 * (int64_t)lo.D);
+        p->cpt1 = 1;
     } else {
         p->CHR = 128;
-        p->NRC = (lo.T + p->CHR - 1) / p->CHR;
-        p->CH = 0;
-        p->W = 0;
-        p->CPI = 1;
-        p->NSTAGE = 1;
-        p->NQ = 0;
+        p->CH = 16;
+        p->W = 4;
+        p->cpt0 = 1;
+        p->cpt1 = ceil16((lo.scheme == KVQ_SCHEME_INT8 ? 2 * (int64_t)lo.D : lo.D) + 8);
     }
-    p->S = p->NRC + p->NQ;
-    if ((int64_t)p->S * units > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;   // one block per (item, unit)
-    const int64_t slots = units * p->S * lo.gqa;
+    // double-buffer the packed chunks when that costs no resident block
+    if (!is_rows(lo.scheme)) {
+        const int res1 = resident_blocks(decode_smem(lo, *p).total);
+        p->NSTAGE = 2;
+        if (resident_blocks(decode_smem(lo, *p).total) < res1) p->NSTAGE = 1;
+    }
+    // slots: block j writes slot j + part * units + unit (cost ranges) or 2 j + part (whole
+    // blocks per unit, used only when 2 units <= NB), j < NB <= KVQ_MAX_DECODE_BLOCKS
+    const int64_t units = (int64_t)lo.B * lo.H;
+    p->nslot = KVQ_MAX_DECODE_BLOCKS + (2 * units > KVQ_MAX_DECODE_BLOCKS ? 2 * units : KVQ_MAX_DECODE_BLOCKS);
+    const int64_t slots = p->nslot * lo.gqa;
     p->ws_o_off = 256;
     p->ws_ml_off = align256(p->ws_o_off + slots * lo.D * 4);
     p->ws_total = align256(p->ws_ml_off + slots * 8);
     p->smem = decode_smem(lo, *p).total;
     if (p->smem > 227 * 1024) return KVQ_ERR_UNSUPPORTED;
+    p->NB = KVQ_MAX_DECODE_BLOCKS;   // the launcher lowers it to one wave on the device
+    p->inv_nb = 1.0f / p->NB;
+    p->inv_cc0 = 1.0f / static_cast<float>(p->CH * p->cpt0);
+    p->inv_cc1 = 1.0f / static_cast<float>(p->CHR * p->cpt1);
+    return KVQ_OK;
+}
+
+// Streaming multiprocessors of `device`, read once per device.
+int device_sm_count(int device) {
+    static std::mutex mu;
+    static int sms[64] = {};
+    if (device < 0 || device >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (sms[device] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+        sms[device] = v;
+    }
+    return sms[device];
+}
+
+// One wave of resident blocks of kernel `fn` with `smem` bytes of dynamic shared memory on
+// the current device (SM count times the occupancy calculator's blocks per SM), at most
+// KVQ_MAX_DECODE_BLOCKS; remembered per (device, kernel, shared memory).  Also raises the
+// kernel's dynamic shared-memory limit the first time it needs more than 48 KiB.
+int decode_blocks(const void* fn, int threads, int64_t smem, int* nb) {
+    struct Entry { int dev; const void* fn; int64_t smem; int nb; };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int used = 0, next = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache[i].dev == dev && cache[i].fn == fn && cache[i].smem == smem) {
+                *nb = cache[i].nb;
+                return KVQ_OK;
+            }
+    }
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, static_cast<size_t>(smem)) !=
+            cudaSuccess ||
+        per_sm < 1)
+        return KVQ_ERR_CUDA;
+    const int sms = device_sm_count(dev);
+    if (sms < 1) return KVQ_ERR_CUDA;
+    int64_t n = (int64_t)sms * per_sm;
+    if (n > KVQ_MAX_DECODE_BLOCKS) n = KVQ_MAX_DECODE_BLOCKS;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry& e = used < 64 ? cache[used++] : cache[next++ % 64];
+    e.dev = dev;
+    e.fn = fn;
+    e.smem = smem;
+    e.nb = static_cast<int>(n);
+    *nb = e.nb;
     return KVQ_OK;
 }
 
@@ -214,7 +249,7 @@ int kvq_cache_init(const kvq_config* cfg, void* cache, kvq_stream_t stream) {
     if (!aligned(cache, 256)) return KVQ_ERR_ALIGN;
     // header, status and the per-sequence counts; the FP8 scale table too (unset scales
     // read as zero until the first append of a layer)
-    const int64_t clear = lo.scheme == KVQ_SCHEME_FP8_E4M3 ? lo.data_off : lo.state_off + kvq::align256((int64_t)lo.L * lo.B * 16);
+    const int64_t clear = kvq::is_fp8(lo.scheme) ? lo.data_off : lo.state_off + kvq::align256((int64_t)lo.L * lo.B * 16);
     if (cudaMemsetAsync(cache, 0, static_cast<size_t>(clear), reinterpret_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return KVQ_ERR_CUDA;
@@ -236,7 +271,7 @@ int kvq_quantize_append(const kvq_config* cfg, void* cache, int32_t layer, int32
     if (flags & ~static_cast<uint32_t>(KVQ_NO_AUTOFLUSH)) return KVQ_ERR_ARG;
     if (seq_count == 0 || n_new == 0) return KVQ_OK;
     if (!k_new || !v_new) return KVQ_ERR_ARG;
-    if (lo.scheme == KVQ_SCHEME_FP8_E4M3 && !fp8_scales) return KVQ_ERR_ARG;
+    if (kvq::is_fp8(lo.scheme) && !fp8_scales) return KVQ_ERR_ARG;
     if (!aligned(cache, 256) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
         (n_valid && !aligned(n_valid, 4)) || (fp8_scales && !aligned(fp8_scales, 4)))
         return KVQ_ERR_ALIGN;

@@ -13,9 +13,10 @@
 //    differently"; "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache",
 //    "How It Works").  The window keeps the newest tokens in bf16 and quantises the
 //    oldest G as a group whenever it would reach R + G tokens.
-//  * INT8 per-token symmetric ("Quantising the Cache", "Workshop"): scale = max|x| / 127.
-//  * FP8 E4M3 with a per-(layer, KV head) scale ("Quantizing the KV cache", "How the KV
-//    cache is quantized").
+//  * INT8 per-token symmetric ("Quantising the Cache", "Workshop"): scale = max|x| / 127;
+//    INT4 the same at 4 bits (the glossary "kv cache quantization"): scale = max|x| / 7.
+//  * FP8 E4M3 or E5M2 with a per-(layer, KV head) scale ("Quantizing the KV cache", "How the
+//    KV cache is quantized").
 #include <cuda_fp8.h>
 
 #include "kvq_internal.cuh"
@@ -270,7 +271,7 @@ __device__ __forceinline__ uint32_t ring_write_row(const Layout& lo, uint8_t* ca
     return bad;
 }
 
-// INT8 / FP8: quantise one token row of (l, b, h) at absolute position t; one warp.
+// INT8 / INT4 / FP8: quantise one token row of (l, b, h) at absolute position t; one warp.
 __device__ __forceinline__ uint32_t quantise_row(const Layout& lo, uint8_t* cache, int l, int b,
                                                  int h, int64_t t, const void* src_k,
                                                  const void* src_v, int64_t row,
@@ -305,11 +306,41 @@ __device__ __forceinline__ uint32_t quantise_row(const Layout& lo, uint8_t* cach
             }
             if (lane == 0)
                 reinterpret_cast<float*>(base + 2 * (int64_t)lo.T16 * D)[(int64_t)kv * lo.T16 + t] = s;
+        } else if (lo.scheme == KVQ_SCHEME_INT4) {
+            // two channels per byte: lane takes channel pairs (2p, 2p + 1), p = lane + 32 e
+            const int ppl = (D / 2 + 31) / 32;   // pairs per lane (1..4)
+            float x[8];
+            float a = 0.0f;
+            for (int e = 0; e < ppl; ++e) {
+                const int pr = lane + 32 * e;
+                x[2 * e] = pr < D / 2 ? load_input(src, row + 2 * pr, lo.dtype) : 0.0f;
+                x[2 * e + 1] = pr < D / 2 ? load_input(src, row + 2 * pr + 1, lo.dtype) : 0.0f;
+                bad |= nonfinite(x[2 * e]) | nonfinite(x[2 * e + 1]);
+                a = fmaxf(a, fmaxf(fabsf(x[2 * e]), fabsf(x[2 * e + 1])));
+            }
+            for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+            const float s = __fdiv_rn(a, 7.0f);
+            uint8_t* codes4 = base + (int64_t)kv * lo.T16 * (D / 2) + t * (D / 2);
+            for (int e = 0; e < ppl; ++e) {
+                const int pr = lane + 32 * e;
+                if (pr >= D / 2) continue;
+                int c2[2] = {0, 0};
+                if (s != 0.0f) {
+                    for (int u = 0; u < 2; ++u) {
+                        int code = __float2int_rn(__fdiv_rn(x[2 * e + u], s));
+                        c2[u] = code < -7 ? -7 : (code > 7 ? 7 : code);
+                    }
+                }
+                codes4[pr] = static_cast<uint8_t>((c2[0] & 15) | ((c2[1] & 15) << 4));
+            }
+            if (lane == 0)
+                reinterpret_cast<float*>(base + (int64_t)lo.T16 * D)[(int64_t)kv * lo.T16 + t] = s;
         } else {
             // keys: channel r of 16-channel block kb at quarter (r mod 8) / 2 of the row,
             // byte 4 kb + 2 (r / 8) + (r mod 2) of it; values: tiles of 16 tokens stored
             // [channel][16], token tt at byte 4 ((tt mod 8) / 2) + 2 (tt mod 2) + tt / 8
             const float s = fp8_scales[2 * h + kv];
+            const __nv_fp8_interpretation_t fmt = lo.scheme == KVQ_SCHEME_FP8_E4M3 ? __NV_E4M3 : __NV_E5M2;
             const int tt = static_cast<int>(t % 16);
             uint8_t* vtile = base + (int64_t)lo.T16 * D + (t - tt) * D + 4 * ((tt % 8) / 2) + 2 * (tt % 2) + tt / 8;
             uint8_t* krow = base + t * D;
@@ -317,7 +348,7 @@ __device__ __forceinline__ uint32_t quantise_row(const Layout& lo, uint8_t* cach
                 float x = load_input(src, row + c, lo.dtype);
                 bad |= nonfinite(x);
                 const uint8_t code = static_cast<uint8_t>(
-                    __nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3));
+                    __nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, fmt));
                 const int r = c % 16;
                 if (kv == 0)
                     krow[((r % 8) / 2) * (D / 4) + 4 * (c / 16) + 2 * (r / 8) + (r % 2)] = code;
@@ -392,7 +423,7 @@ __global__ void __launch_bounds__(kThreads) k_append_small(AppendArgs a) {
         for (int64_t t = first + warp; t < (int64_t)n + m; t += nwarps)
             bad |= ring_write_row(lo, a.cache, a.layer, b, h, t, n, a.k_new, a.v_new, a.n_new, bi, lane);
     } else {
-        if (lo.scheme == KVQ_SCHEME_FP8_E4M3 && bi == 0 && h == 0)
+        if (is_fp8(lo.scheme) && bi == 0 && h == 0)
             for (int i = threadIdx.x; i < 2 * lo.H; i += blockDim.x)
                 reinterpret_cast<float*>(a.cache + lo.scales_off)[(int64_t)a.layer * lo.H * 2 + i] = a.fp8_scales[i];
         for (int j = warp; j < m; j += nwarps)
@@ -475,7 +506,7 @@ __global__ void __launch_bounds__(kThreads) k_append_rows(AppendArgs a) {
 // Bulk appends, step 3: new per-sequence counts and status bits (and the FP8 scale table).
 __global__ void k_append_commit(AppendArgs a) {
     const Layout& lo = a.lo;
-    if (lo.scheme == KVQ_SCHEME_FP8_E4M3 && blockIdx.x == 0)
+    if (is_fp8(lo.scheme) && blockIdx.x == 0)
         for (int i = threadIdx.x; i < 2 * lo.H; i += blockDim.x)
             reinterpret_cast<float*>(a.cache + lo.scales_off)[(int64_t)a.layer * lo.H * 2 + i] = a.fp8_scales[i];
     const int bi = blockIdx.x * blockDim.x + threadIdx.x;

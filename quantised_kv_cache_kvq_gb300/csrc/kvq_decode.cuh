@@ -5,9 +5,12 @@
 // head, o = sum_t p_t * Vhat_t with p = softmax_t(softmax_scale * q . Khat_t) over all
 // cached tokens of the sequence; query head hq reads KV head hq / gqa.
 //
-// Work split: a block handles one (sequence, kv head, chunk of tokens) item and leaves
-// the chunk's partial softmax (m, l, o[D]) for all gqa query heads of the kv head, so
-// every cache byte is read once per step.  k_merge combines the chunks by log-sum-exp.
+// Work split: the grid is one wave of resident blocks.  The layer's work is measured by
+// the real token counts in the cache state (the bytes each token reads), and block j takes
+// a contiguous 1/NB of it: runs of chunks of one or more (sequence, kv head) units.  For
+// every part of a unit it touches (the packed tokens, the rows) a block leaves one partial
+// softmax (m, l, o[D]) for all gqa query heads of the kv head, so every cache byte is read
+// once per step.  k_merge combines a unit's partials by log-sum-exp.
 //
 // Packed KIVI chunks (runs of group records) are staged into shared memory by one bulk
 // asynchronous copy, then both contractions run on the tensor cores with operands built
@@ -49,45 +52,441 @@ struct DecodeArgs {
     uint8_t* ws;
 };
 
-struct ItemRange {
-    int64_t t0, t1;
-};
-
-// Token range of work item `item` of a unit with n cached tokens, qn of them packed.
-__host__ __device__ inline ItemRange item_range(const Layout& lo, const DecodePlan& p, int item,
-                                                int64_t n, int64_t qn) {
-    ItemRange r;
-    if (item < p.NRC) {
-        const int64_t base = lo.scheme == KVQ_SCHEME_KIVI ? qn : 0;
-        r.t0 = base + (int64_t)item * p.CHR;
-        r.t1 = r.t0 + p.CHR < n ? r.t0 + p.CHR : n;
+// ------------------------------------------------------------------------ scheduling
+// Tokens of the two parts of a unit holding n tokens, qn of them packed: part 0 (KIVI
+// groups, FP8 tiles) and part 1 (KIVI window, INT8 or INT4 rows).
+__host__ __device__ __forceinline__ void unit_parts(const Layout& lo, int64_t n, int64_t qn, int64_t& n0,
+                                                    int64_t& n1) {
+    if (lo.scheme == KVQ_SCHEME_KIVI) {
+        n0 = qn;
+        n1 = n - qn;
+    } else if (is_fp8(lo.scheme)) {
+        n0 = n;
+        n1 = 0;
     } else {
-        const int64_t span = (int64_t)p.CPI * p.CH;
-        r.t0 = (int64_t)(item - p.NRC) * span;
-        r.t1 = r.t0 + span < qn ? r.t0 + span : qn;
+        n0 = 0;
+        n1 = n;
     }
+}
+
+// The scheduling arithmetic below divides by multiplying with binary32 reciprocals made
+// on the host (integer division and binary64 arithmetic are long or slow on the GPU).  A
+// block boundary or a chunk index may then differ a little from the exact quotient, which
+// only moves work between neighbouring blocks: the decode and the merge call these same
+// functions with the same arguments, block ranges are nondecreasing in j with
+// range_lo(C, 0) = 0 and range_lo(C, nb) = C, and block j's chunks end where block j + 1's
+// begin, so every chunk is taken by exactly one block.
+
+// First cost position of block j of nb over a total cost C: about ceil(C j / nb).
+__host__ __device__ __forceinline__ int64_t range_lo(int64_t C, int64_t j, int64_t nb, float inv_nb) {
+    if (j >= nb) return C;
+    const int64_t r = static_cast<int64_t>(ceilf(static_cast<float>(C) * (static_cast<float>(j) * inv_nb)));
+    return r < C ? r : C;
+}
+
+// Chunks [k_lo, k_hi) of a part whose chunk k starts at cost position base + k * cc (nch
+// chunks, inv_cc = 1 / cc) that start inside the block range [lo, hi), up to the rounding
+// described above.
+__host__ __device__ __forceinline__ void chunks_in(int64_t base, int64_t nch, float inv_cc, int64_t lo, int64_t hi,
+                                                   int64_t& k_lo, int64_t& k_hi) {
+    k_lo = lo > base ? static_cast<int64_t>(ceilf(static_cast<float>(lo - base) * inv_cc)) : 0;
+    k_hi = hi > base ? static_cast<int64_t>(ceilf(static_cast<float>(hi - base) * inv_cc)) : 0;
+    if (k_lo > nch) k_lo = nch;
+    if (k_hi > nch) k_hi = nch;
+}
+
+// Tokens n, qn of sequence b in this layer's state.
+__device__ __forceinline__ int2 seq_state(const DecodeArgs& a, int b) {
+    return *reinterpret_cast<const int2*>(state_ptr(a.lo, a.cache, a.layer, b));
+}
+
+// Scheduling costs of one unit's packed part and row part for a sequence with state st.
+__device__ __forceinline__ void part_costs(const DecodeArgs& a, int2 st, int64_t& c0, int64_t& c1) {
+    int64_t n0, n1;
+    unit_parts(a.lo, st.x, st.y, n0, n1);
+    c0 = n0 * a.plan.cpt0;
+    c1 = n1 * a.plan.cpt1;
+}
+
+__device__ __forceinline__ int64_t warp_scan64(int64_t v) {   // inclusive
+    const int lane = threadIdx.x & 31;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+// Block-wide inclusive scan of one int64 per thread over a tile of kDecodeThreads values;
+// returns the thread's inclusive prefix within the tile and sets *tile_total.  Two block
+// barriers; `scratch` holds NW int64.
+__device__ __forceinline__ int64_t block_scan64(int64_t v, int64_t* scratch, int64_t* tile_total) {
+    constexpr int NW = kDecodeThreads / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t inc = warp_scan64(v);
+    if (lane == 31) scratch[warp] = inc;
+    __syncthreads();
+    int64_t woff = 0, tot = 0;
+    for (int w = 0; w < NW; ++w) {
+        if (w < warp) woff += scratch[w];
+        tot += scratch[w];
+    }
+    __syncthreads();
+    *tile_total = tot;
+    return inc + woff;
+}
+
+// The layer's work in cost order: first the packed parts of every unit (sequence-major,
+// then kv head), then the row parts of every unit.  Keeping the two apart means a block
+// never interleaves a unit's bf16 window with packed groups.  C0 is the packed total, C
+// the whole.  block_range finds this block's range [lo, hi) and the (part, sequence) at
+// position lo with the cost P before that sequence in its part; part = 2 when the range
+// is empty.  Whole block; `scratch` holds at least 16 int64 of shared memory and `sst` B
+// int2 when B <= kDecodeThreads (the sequences' states, kept for the walk).
+struct BlockRange {
+    int64_t C0, C, lo, hi, P;
+    int part, b;
+};
+__device__ inline BlockRange block_range(const DecodeArgs& a, int64_t* scratch, int2* sst, int blk) {
+    const int tid = threadIdx.x;
+    const int B = a.lo.B, H = a.lo.H;
+    BlockRange r;
+    int64_t f0 = 0, f1 = 0, C0 = 0, C1 = 0;
+    for (int base = 0; base < B; base += kDecodeThreads) {
+        const int b = base + tid;
+        int2 st = make_int2(0, 0);
+        if (b < B) st = seq_state(a, b);
+        if (B <= kDecodeThreads && b < B) sst[b] = st;
+        int64_t c0, c1;
+        part_costs(a, st, c0, c1);
+        c0 *= H;
+        c1 *= H;
+        if (base == 0) {
+            f0 = c0;
+            f1 = c1;
+        }
+        int64_t t0, t1;
+        block_scan64(c0, scratch, &t0);
+        block_scan64(c1, scratch, &t1);
+        C0 += t0;
+        C1 += t1;
+    }
+    r.C0 = C0;
+    r.C = C0 + C1;
+    r.lo = range_lo(r.C, blk, a.plan.NB, a.plan.inv_nb);
+    r.hi = range_lo(r.C, blk + 1, a.plan.NB, a.plan.inv_nb);
+    r.part = 2;
+    r.b = B;
+    r.P = 0;
+    if (r.lo >= r.hi) return r;
+    // the part holding lo, then the sequence within it
+    const int part = r.lo < C0 ? 0 : 1;
+    const int64_t pos = part ? r.lo - C0 : r.lo;
+    if (tid == 0) scratch[8] = -1;
+    int64_t run = 0;
+    for (int base = 0; base < B; base += kDecodeThreads) {
+        const int b = base + tid;
+        int64_t c;
+        if (base == 0) {
+            c = part ? f1 : f0;
+        } else {
+            int64_t c0 = 0, c1 = 0;
+            if (b < B) part_costs(a, seq_state(a, b), c0, c1);
+            c = H * (part ? c1 : c0);
+        }
+        int64_t tile;
+        const int64_t inc = block_scan64(c, scratch, &tile) + run;
+        const int64_t exc = inc - c;
+        if (c > 0 && exc <= pos && pos < inc) {
+            scratch[8] = b;
+            scratch[9] = exc;
+        }
+        __syncthreads();
+        const int64_t found = scratch[8];
+        __syncthreads();
+        if (found >= 0) {
+            r.part = part;
+            r.b = static_cast<int>(found);
+            r.P = scratch[9];
+            break;
+        }
+        run += tile;
+    }
+    __syncthreads();
     return r;
 }
 
-// The work of one decode block.  Blocks are numbered item-major over the units (sequence,
-// kv head): first every unit's packed items (the long ones; a unit's last, possibly
-// partial, item last), then the window or row items.  The blocks left over for a second
-// wave of resident blocks are then the short ones.
-struct BlockWork {
-    int item, h, b;
+// The unit-aligned split, used when the batch has at most half as many units as the grid
+// has blocks.  A unit of cost U > 0 gets k = 1 + floor(U NB' / C) whole blocks (NB' = NB
+// minus the number of non-empty units, so that sum k <= NB), units in order (sequence-
+// major, then kv head) on consecutive blocks.  The unit's N chunks (packed part, then rows)
+// are shared by count: block r of k takes chunks [N r / k, N (r + 1) / k), so that no
+// block holds a chunk more than another (a cost split can give one block three chunk
+// starts where the next gets two).  No
+// block then spans two units, and block j's partial results go to slots 2 j + part.  (The
+// cost-range slots j + part B H + unit would collide here: a unit's rows can end on a
+// block a few blocks before the next unit's packed part begins.)  unit_plan finds this
+// block's unit (b = B when it has none) and r, k.
+struct UnitPlan {
+    int b, h, r, k;
+    int64_t n0, n1;
 };
-__device__ __forceinline__ BlockWork block_work(const Layout& lo, const DecodePlan& p) {
-    const uint32_t units = static_cast<uint32_t>(lo.B) * static_cast<uint32_t>(lo.H);
-    const uint32_t k = blockIdx.x / units, u = blockIdx.x - k * units;
-    BlockWork w;
-    w.item = static_cast<int>(k) < p.NQ ? p.NRC + static_cast<int>(k) : static_cast<int>(k) - p.NQ;
-    w.b = static_cast<int>(u / static_cast<uint32_t>(lo.H));
-    w.h = static_cast<int>(u) - w.b * lo.H;
-    return w;
+// 1 + floor(U nbp / C) in binary32, scaled down by 1e-6 so that the rounding never makes it
+// exceed the exact value (the error of the few binary32 operations is below 3e-7): the
+// sum over the units then stays within NB.
+__device__ __forceinline__ int unit_blocks(int64_t U, int64_t C, int64_t nbp) {
+    if (U <= 0) return 0;
+    const float x = static_cast<float>(U) * (static_cast<float>(nbp) / static_cast<float>(C)) * 0.999999f;
+    return 1 + static_cast<int>(x);
 }
-// Grid of the decode kernels: one block per (item, unit).
-inline dim3 decode_grid(const DecodeArgs& a) {
-    return dim3(static_cast<unsigned>((int64_t)a.plan.S * a.lo.B * a.lo.H));
+__device__ inline UnitPlan unit_plan(const DecodeArgs& a, int64_t* scratch, int2* sst, int blk) {
+    const int tid = threadIdx.x;
+    const int B = a.lo.B, H = a.lo.H;
+    UnitPlan up;
+    up.b = B;
+    if (B <= 32) {
+        // one warp, a sequence per lane, one block barrier
+        if (tid < 32) {
+            const int b = tid;
+            int2 st = make_int2(0, 0);
+            if (b < B) st = seq_state(a, b);
+            sst[b] = st;
+            int64_t c0, c1;
+            part_costs(a, st, c0, c1);
+            const int64_t U = b < B ? c0 + c1 : 0;
+            int64_t C = H * U, live = U > 0 ? H : 0;
+            for (int o = 16; o > 0; o >>= 1) {
+                C += __shfl_xor_sync(0xffffffffu, C, o);
+                live += __shfl_xor_sync(0xffffffffu, live, o);
+            }
+            const int64_t nbp = a.plan.NB - live;
+            const int k = C > 0 ? unit_blocks(U, C, nbp) : 0;
+            const int64_t inc = warp_scan64((int64_t)H * k), exc = inc - (int64_t)H * k;
+            const bool mine = k > 0 && exc <= blk && blk < inc;
+            const unsigned m = __ballot_sync(0xffffffffu, mine);
+            if (tid == 0) scratch[8] = m ? static_cast<int64_t>(__ffs(m) - 1) : -1;
+            if (mine) {
+                scratch[9] = exc;
+                scratch[10] = k;
+            }
+        }
+        __syncthreads();
+        const int64_t found = scratch[8];
+        if (found >= 0) {
+            up.b = static_cast<int>(found);
+            up.k = static_cast<int>(scratch[10]);
+            const int off = blk - static_cast<int>(scratch[9]);
+            up.h = off / up.k;
+            up.r = off - up.h * up.k;
+            const int2 st = sst[up.b];
+            unit_parts(a.lo, st.x, st.y, up.n0, up.n1);
+        }
+        return up;
+    }
+    int64_t C = 0, live = 0, fU = 0;
+    for (int base = 0; base < B; base += kDecodeThreads) {
+        const int b = base + tid;
+        int2 st = make_int2(0, 0);
+        if (b < B) st = seq_state(a, b);
+        if (B <= kDecodeThreads && b < B) sst[b] = st;
+        int64_t c0, c1;
+        part_costs(a, st, c0, c1);
+        if (base == 0) fU = c0 + c1;
+        int64_t t0, t1;
+        block_scan64(H * (c0 + c1), scratch, &t0);
+        block_scan64(c0 + c1 > 0 ? H : 0, scratch, &t1);
+        C += t0;
+        live += t1;
+    }
+    if (C == 0) return up;
+    const int64_t nbp = a.plan.NB - live;
+    int64_t run = 0;
+    if (tid == 0) scratch[8] = -1;
+    for (int base = 0; base < B; base += kDecodeThreads) {
+        const int b = base + tid;
+        int64_t U = fU;
+        if (base != 0 || B > kDecodeThreads) {
+            int64_t c0 = 0, c1 = 0;
+            if (b < B) part_costs(a, B <= kDecodeThreads ? sst[b] : seq_state(a, b), c0, c1);
+            U = c0 + c1;
+        }
+        if (b >= B) U = 0;
+        const int k = unit_blocks(U, C, nbp);
+        int64_t tile;
+        const int64_t inc = block_scan64((int64_t)H * k, scratch, &tile) + run;
+        const int64_t exc = inc - (int64_t)H * k;
+        if (k > 0 && exc <= blk && blk < inc) {
+            scratch[8] = b;
+            scratch[9] = exc;
+            scratch[10] = k;
+        }
+        __syncthreads();
+        const int64_t found = scratch[8];
+        if (found >= 0) break;
+        run += tile;
+        __syncthreads();
+    }
+    __syncthreads();
+    const int64_t found = scratch[8];
+    if (found >= 0) {
+        up.b = static_cast<int>(found);
+        up.k = static_cast<int>(scratch[10]);
+        const int off = blk - static_cast<int>(scratch[9]);
+        up.h = off / up.k;
+        up.r = off - up.h * up.k;
+        const int2 st = B <= kDecodeThreads ? sst[up.b] : seq_state(a, up.b);
+        unit_parts(a.lo, st.x, st.y, up.n0, up.n1);
+    }
+    __syncthreads();
+    return up;
+}
+
+// Calls fn(part, b, h, slot, t0, t1) for every run of chunks of one part of one unit that
+// this block takes, in cost order (whole block, uniform).  The run's partial result goes
+// to slot j + part * B H + unit: unique, because block ranges are contiguous in cost order.
+// fn returns false once the block cannot go on (a bounded wait gave up); the remaining runs
+// then get empty partials via dead(slot).
+template <typename F, typename E>
+__device__ void for_each_segment(const DecodeArgs& a, int64_t* scratch, int2* sst, F&& fn, E&& dead) {
+    const Layout& lo = a.lo;
+    const int64_t units = (int64_t)lo.B * lo.H;
+    if (a.plan.unit_aligned) {
+        const UnitPlan up = unit_plan(a, scratch, sst, blockIdx.x);
+        grid_launch_dependents();   // the merge may start its own planning; it waits for this grid
+        if (up.b >= lo.B) return;
+        const int64_t nc0 = (up.n0 + a.plan.CH - 1) / a.plan.CH, nc1 = (up.n1 + a.plan.CHR - 1) / a.plan.CHR;
+        const int64_t N = nc0 + nc1;
+        const int64_t clo = N * up.r / up.k, chi = N * (up.r + 1) / up.k;
+        bool go = true;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            const int64_t nt = part ? up.n1 : up.n0, gs = part ? a.plan.CHR : a.plan.CH;
+            if (nt > 0) {
+                const int64_t off = part ? nc0 : 0, nch = part ? nc1 : nc0;
+                int64_t k_lo = clo - off, k_hi = chi - off;
+                k_lo = k_lo < 0 ? 0 : (k_lo > nch ? nch : k_lo);
+                k_hi = k_hi < 0 ? 0 : (k_hi > nch ? nch : k_hi);
+                if (k_lo < k_hi) {
+                    const int64_t slot = 2 * (int64_t)blockIdx.x + part;   // one unit per block
+                    const int64_t t1 = k_hi * gs < nt ? k_hi * gs : nt;
+                    __syncthreads();   // the previous run is done with shared memory
+                    if (go)
+                        go = fn(part, up.b, up.h, slot, k_lo * gs, t1);
+                    else
+                        dead(slot);
+                }
+            }
+        }
+        return;
+    }
+    const BlockRange r = block_range(a, scratch, sst, blockIdx.x);
+    grid_launch_dependents();   // the merge may start its own planning; it waits for this grid
+    bool live = true;
+    for (int part = r.part; part < 2; ++part) {
+        const int64_t gs = part ? a.plan.CHR : a.plan.CH, cpt = part ? a.plan.cpt1 : a.plan.cpt0;
+        const float inv_cc = part ? a.plan.inv_cc1 : a.plan.inv_cc0;
+        // cost position of the part's first sequence considered, in the whole order
+        int64_t P = (part ? r.C0 : 0) + (part == r.part ? r.P : 0);
+        if (P >= r.hi) break;
+        for (int b = part == r.part ? r.b : 0; b < lo.B && P < r.hi; ++b) {
+            const int2 st = lo.B <= kDecodeThreads ? sst[b] : seq_state(a, b);
+            int64_t n0, n1;
+            unit_parts(lo, st.x, st.y, n0, n1);
+            const int64_t nt = part ? n1 : n0;
+            const int64_t U = nt * cpt;
+            if (U == 0) continue;
+            // the first head whose cost range reaches lo (a reciprocal estimate, made exact)
+            int h0 = 0;
+            if (r.lo > P) {
+                h0 = static_cast<int>(static_cast<float>(r.lo - P) / static_cast<float>(U));
+                h0 = h0 < 0 ? 0 : (h0 > lo.H - 1 ? lo.H - 1 : h0);
+                while (h0 > 0 && P + h0 * U > r.lo) --h0;
+                while (h0 + 1 < lo.H && P + (h0 + 1) * U <= r.lo) ++h0;
+            }
+            for (int h = h0; h < lo.H && P + h * U < r.hi; ++h) {
+                int64_t k_lo, k_hi;
+                chunks_in(P + h * U, (nt + gs - 1) / gs, inv_cc, r.lo, r.hi, k_lo, k_hi);
+                if (k_lo < k_hi) {
+                    const int64_t slot = blockIdx.x + part * units + (int64_t)b * lo.H + h;
+                    const int64_t t1 = k_hi * gs < nt ? k_hi * gs : nt;
+                    __syncthreads();   // the previous run is done with shared memory
+                    if (live)
+                        live = fn(part, b, h, slot, k_lo * gs, t1);
+                    else
+                        dead(slot);
+                }
+            }
+            P += (int64_t)lo.H * U;
+        }
+    }
+}
+
+// The layer's totals and one sequence's prefixes, as the decode's split uses them: C0 the
+// packed total, C the whole, P0 and P1 the packed and row costs of the sequences before
+// b (cost-range split); live the non-empty units and K the first block of sequence b
+// (unit-aligned split).
+struct SplitCtx {
+    int64_t C0, C, P0, P1, live, K;
+};
+
+// The partial-result slots of unit u (sequence b = u / H, kv head h = u % H, state st):
+// the decode blocks that may have taken chunks of the unit, by the same arithmetic as the
+// decode's split; cand[i] is the block's slot, or -1 when the block took no chunk of the
+// unit (in the cost-range split the range is widened by two blocks on each side for the
+// rounding of that arithmetic).  Written by the block's `nthreads` threads (no barrier);
+// returns the list's length (at most 2 KVQ_MAX_DECODE_BLOCKS).
+__device__ inline int unit_candidates(const DecodeArgs& a, int u, int2 st, const SplitCtx& x, int* cand,
+                                      int nthreads) {
+    const Layout& lo = a.lo;
+    const int h = u % lo.H;
+    const int tid = threadIdx.x;
+    const int64_t units = (int64_t)lo.B * lo.H;
+    const int NB = a.plan.NB;
+    int64_t n0, n1;
+    unit_parts(lo, st.x, st.y, n0, n1);
+    int total = 0;
+    if (a.plan.unit_aligned) {
+        // the unit's k blocks from K + h k; block r takes chunks starting in its share
+        const int64_t U = n0 * a.plan.cpt0 + n1 * a.plan.cpt1;
+        const int k = x.C > 0 ? unit_blocks(U, x.C, NB - x.live) : 0;
+        const int64_t K = x.K + (int64_t)h * k;
+        const int64_t nc0 = (n0 + a.plan.CH - 1) / a.plan.CH, nc1 = (n1 + a.plan.CHR - 1) / a.plan.CHR;
+        const int64_t N = nc0 + nc1;
+        for (int i = tid; i < 2 * k; i += nthreads) {
+            const int part = i / k, r = i - part * k;
+            const int64_t clo = N * r / k, chi = N * (r + 1) / k;
+            const int64_t lo_c = part ? nc0 : 0, hi_c = part ? N : nc0;
+            const bool any = (clo > lo_c ? clo : lo_c) < (chi < hi_c ? chi : hi_c);
+            cand[i] = any ? static_cast<int>(2 * (K + r) + part) : -1;
+        }
+        return 2 * k;
+    }
+    const int64_t C0 = x.C0, C = x.C;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+        const int64_t nt = part ? n1 : n0, gs = part ? a.plan.CHR : a.plan.CH;
+        const int64_t cpt = part ? a.plan.cpt1 : a.plan.cpt0;
+        if (nt > 0 && C > 0) {
+            const int64_t base = (part ? C0 + x.P1 : x.P0) + (int64_t)h * nt * cpt;
+            const int64_t nch = (nt + gs - 1) / gs;
+            const float inv_cc = part ? a.plan.inv_cc1 : a.plan.inv_cc0;
+            const float per = static_cast<float>(NB) / static_cast<float>(C);
+            int j0 = static_cast<int>(static_cast<float>(base) * per) - 2;
+            int j1 = static_cast<int>(static_cast<float>(base + (nch - 1) * gs * cpt) * per) + 2;
+            j0 = j0 < 0 ? 0 : j0;
+            j1 = j1 > NB - 1 ? NB - 1 : j1;
+            const int count = j1 - j0 + 1;
+            for (int i = tid; i < count; i += nthreads) {
+                const int j = j0 + i;
+                int64_t k_lo, k_hi;
+                chunks_in(base, nch, inv_cc, range_lo(C, j, NB, a.plan.inv_nb), range_lo(C, j + 1, NB, a.plan.inv_nb),
+                          k_lo, k_hi);
+                cand[total + i] = k_lo < k_hi ? static_cast<int>(j + part * units + u) : -1;
+            }
+            total += count;
+        }
+    }
+    return total;
 }
 
 __device__ __forceinline__ float load_q(const void* q, int64_t idx, int dtype) {
@@ -120,29 +519,46 @@ __device__ __forceinline__ void bulk_copy_pieces(uint8_t* dst, const uint8_t* sr
     }
 }
 
-// All threads wait for the staged bytes; on a timeout the decode status gets
-// KVQ_STATUS_TIMEOUT, the block waits once more (bounded) for its copies and returns false.
-__device__ __forceinline__ bool wait_staged(uint64_t* bar, uint8_t* ws) {
-    bool ok = mbar_wait_bounded(bar, 0, kWaitLimit);
+// Staging barriers: bit s of `phase` is the parity the next completion of barrier s
+// carries (items take the bits and return them updated, or -1 once a wait gave up).  All
+// threads wait; on a timeout the decode status gets KVQ_STATUS_TIMEOUT, the block waits
+// once more (bounded) for the copy and false is returned.  With kSelfTestBit set in
+// `phase` (the workspace self-test, see kvq_decode_attention) the wait is made on a
+// barrier that nothing completes, so it gives up, and the real copy is then waited for.
+__device__ __forceinline__ bool wait_stage(uint64_t* bars, int s, uint32_t& phase, uint8_t* ws) {
+    const uint32_t par = (phase >> s) & 1u;
+    bool ok = mbar_wait_bounded(bars + ((phase & kSelfTestBit) ? kSelfTestBar : s), par, kWaitLimitNs);
     ok = __syncthreads_and(ok);
     if (!ok) {
         if (threadIdx.x == 0) atomicOr(reinterpret_cast<uint32_t*>(ws), KVQ_STATUS_TIMEOUT);
-        mbar_wait_bounded(bar, 0, kWaitLimit);
-        __syncthreads();
+        mbar_wait_bounded(bars + s, par, kWaitLimitNs);
+        return false;
     }
-    return ok;
+    phase ^= 1u << s;
+    return true;
+}
+// After a timeout: a bounded wait for a copy still armed on barrier s.
+__device__ __forceinline__ void drain_stage(uint64_t* bars, int s, uint32_t phase) {
+    mbar_wait_bounded(bars + s, (phase >> s) & 1u, kWaitLimitNs);
 }
 
-// Partial-result slots of the workspace.
-__device__ __forceinline__ int64_t slot_index(const DecodeArgs& a, int b, int h, int item, int head) {
-    return (((int64_t)b * a.lo.H + h) * a.plan.S + item) * a.lo.gqa + head;
+// The workspace self-test word (bytes 8..15 of the workspace header).
+__device__ __forceinline__ uint32_t selftest_bits(const DecodeArgs& a) {
+    return *reinterpret_cast<const unsigned long long*>(a.ws + 8) == KVQ_SELFTEST_WAIT_MAGIC ? kSelfTestBit : 0u;
 }
 
-// An item without tokens (or whose chunks never arrived) leaves an empty partial: m = -inf,
-// l = 0, so the merge gives it weight 0 without reading the cache state.
-__device__ __forceinline__ void empty_partial(const DecodeArgs& a, int b, int h, int item) {
+// Partial-result slots of the workspace: slot * gqa + head.
+__device__ __forceinline__ float* slot_o(const DecodeArgs& a, int64_t slot, int head) {
+    return reinterpret_cast<float*>(a.ws + a.plan.ws_o_off) + (slot * a.lo.gqa + head) * a.lo.D;
+}
+__device__ __forceinline__ float* slot_ml(const DecodeArgs& a, int64_t slot, int head) {
+    return reinterpret_cast<float*>(a.ws + a.plan.ws_ml_off) + 2 * (slot * a.lo.gqa + head);
+}
+
+// An empty partial: m = -inf, l = 0, so the merge gives it weight 0.
+__device__ __forceinline__ void empty_partial(const DecodeArgs& a, int64_t slot) {
     if (threadIdx.x < a.lo.gqa) {
-        float* ml = reinterpret_cast<float*>(a.ws + a.plan.ws_ml_off) + 2 * slot_index(a, b, h, item, threadIdx.x);
+        float* ml = slot_ml(a, slot, threadIdx.x);
         ml[0] = -INFINITY;
         ml[1] = 0.0f;
     }
@@ -156,359 +572,6 @@ __device__ __forceinline__ void load_query(const DecodeArgs& a, int b, int h, fl
         qs[i] = load_q(a.q, base + i, lo.dtype) * a.qscale;
 }
 
-// Softmax over the chunk: per-head max (from per-warp maxima in red[warp][head]), then
-// p = 2^(s - max) in place and l = sum p.  Leaves max and l in hstat[0..31], [32..63].
-__device__ __forceinline__ void chunk_softmax(const Layout& lo, float* sc, int ntok, int sc_stride,
-                                              float* red, float* hstat) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid < lo.gqa) {
-        float m = -INFINITY;
-        for (int w = 0; w < 4; ++w) m = fmaxf(m, red[w * 32 + tid]);
-        hstat[tid] = m;
-    }
-    __syncthreads();
-    for (int hh = 0; hh < lo.gqa; ++hh) {
-        const float m = hstat[hh];
-        float part = 0.0f;
-        for (int t = tid; t < ntok; t += blockDim.x) {
-            const float p = exp2f(sc[hh * sc_stride + t] - m);
-            sc[hh * sc_stride + t] = p;
-            part += p;
-        }
-        part = warp_sum(part);
-        if (lane == 0) red[warp * 32 + hh] = part;
-    }
-    __syncthreads();
-    if (tid < lo.gqa) {
-        float l = 0.0f;
-        for (int w = 0; w < 4; ++w) l += red[w * 32 + tid];
-        hstat[32 + tid] = l;
-    }
-    __syncthreads();
-}
-
-// ------------------------------------------------------------------------ row path
-// Tokens held as whole rows: the bf16 window of a KIVI cache, or INT8 rows.
-template <int D>
-__device__ void rows_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& so, int b, int h,
-                          int item, int64_t t0, int64_t t1) {
-    const Layout& lo = a.lo;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int cnt = static_cast<int>(t1 - t0);
-    const int CHR = a.plan.CHR;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + so.bar);
-    float* red = reinterpret_cast<float*>(smem + so.red);
-    float* hstat = reinterpret_cast<float*>(smem + so.hstat);
-    float* qs = reinterpret_cast<float*>(smem + so.qs);
-    float* sc = reinterpret_cast<float*>(smem + so.sc);
-    uint8_t* data = smem + so.data;
-    const int64_t u = unit_index(lo, a.layer, b, h);
-
-    if (tid == 0) mbar_init(bar, 1);
-    __syncthreads();
-    if (tid == 0) {
-        if (lo.scheme == KVQ_SCHEME_KIVI) {
-            const uint8_t* ring = a.cache + lo.ring_off + u * lo.C * (int64_t)(4 * D);
-            const int s0 = static_cast<int>(t0 % lo.C);
-            const int first = cnt < lo.C - s0 ? cnt : lo.C - s0;
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * 4 * D);
-            bulk_copy_pieces(data, ring + (int64_t)s0 * 4 * D, static_cast<uint32_t>(first) * 4 * D, bar);
-            if (cnt > first)
-                bulk_copy_pieces(data + (int64_t)first * 4 * D, ring, static_cast<uint32_t>(cnt - first) * 4 * D, bar);
-        } else {
-            // INT8 rows (FP8 has its own tensor-core path)
-            const uint8_t* unit = a.cache + lo.data_off + u * lo.unit;
-            const uint32_t cb = static_cast<uint32_t>(cnt) * D;
-            const uint32_t sb = static_cast<uint32_t>((cnt + 3) / 4 * 4) * 4;
-            mbar_arrive_expect_tx(bar, 2 * cb + 2 * sb);
-            bulk_copy_pieces(data, unit + t0 * D, cb, bar);
-            bulk_copy_pieces(data + (int64_t)CHR * D, unit + (int64_t)lo.T16 * D + t0 * D, cb, bar);
-            const uint8_t* scales = unit + 2 * (int64_t)lo.T16 * D;
-            bulk_copy_pieces(data + 2 * (int64_t)CHR * D, scales + 4 * t0, sb, bar);
-            bulk_copy_pieces(data + 2 * (int64_t)CHR * D + 4 * CHR, scales + 4 * (int64_t)lo.T16 + 4 * t0, sb, bar);
-        }
-    }
-    load_query(a, b, h, qs);
-    if (!wait_staged(bar, a.ws)) {
-        empty_partial(a, b, h, item);
-        return;
-    }
-
-    auto kval = [&](int i, int c) -> float {
-        if (lo.scheme == KVQ_SCHEME_KIVI)
-            return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(data + (int64_t)i * 4 * D)[c]);
-        return static_cast<float>(reinterpret_cast<const int8_t*>(data)[i * D + c]) *
-               reinterpret_cast<const float*>(data + 2 * (int64_t)CHR * D)[i];
-    };
-    auto vval = [&](int i, int c) -> float {
-        if (lo.scheme == KVQ_SCHEME_KIVI)
-            return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(data + (int64_t)i * 4 * D + 2 * D)[c]);
-        return static_cast<float>(reinterpret_cast<const int8_t*>(data + (int64_t)CHR * D)[i * D + c]) *
-               reinterpret_cast<const float*>(data + 2 * (int64_t)CHR * D + 4 * CHR)[i];
-    };
-
-    // scores: a warp per token, lanes over channels, one reduction per head
-    constexpr int CPL = (D + 31) / 32;
-    float hmax[8];
-#pragma unroll
-    for (int hh = 0; hh < 8; ++hh) hmax[hh] = -INFINITY;
-    for (int i = warp; i < cnt; i += 4) {
-        float kv[CPL];
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) kv[j] = kval(i, lane + 32 * j);
-#pragma unroll
-        for (int hh = 0; hh < 8; ++hh) {
-            if (hh >= lo.gqa) break;
-            float acc = 0.0f;
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) acc = fmaf(qs[hh * D + lane + 32 * j], kv[j], acc);
-            acc = warp_sum(acc);
-            if (lane == 0) sc[hh * CHR + i] = acc;
-            hmax[hh] = fmaxf(hmax[hh], acc);
-        }
-    }
-#pragma unroll
-    for (int hh = 0; hh < 8; ++hh)
-        if (lane == 0 && hh < lo.gqa) red[warp * 32 + hh] = hmax[hh];
-    __syncthreads();
-    chunk_softmax(lo, sc, cnt, CHR, red, hstat);
-
-    // values: a thread per channel
-    for (int c = tid; c < D; c += blockDim.x) {
-        float o[8];
-#pragma unroll
-        for (int hh = 0; hh < 8; ++hh) o[hh] = 0.0f;
-        for (int i = 0; i < cnt; ++i) {
-            const float v = vval(i, c);
-#pragma unroll
-            for (int hh = 0; hh < 8; ++hh)
-                if (hh < lo.gqa) o[hh] = fmaf(sc[hh * CHR + i], v, o[hh]);
-        }
-#pragma unroll
-        for (int hh = 0; hh < 8; ++hh)
-            if (hh < lo.gqa)
-                reinterpret_cast<float*>(a.ws + a.plan.ws_o_off)[slot_index(a, b, h, item, hh) * D + c] = o[hh];
-    }
-    if (tid < lo.gqa) {
-        float* ml = reinterpret_cast<float*>(a.ws + a.plan.ws_ml_off) + 2 * slot_index(a, b, h, item, tid);
-        ml[0] = hstat[tid];
-        ml[1] = hstat[32 + tid];
-    }
-}
-
-// Combine the 4 warps' partials of one work item (comb[warp][head][D] = o, cml[warp][head]
-// = (m, l)) into the item's workspace slots.  Called by the whole block after a barrier.
-// A warp without tokens leaves m = -inf, l = 0 and its o unwritten; it gets weight 0 and
-// its o is never read.
-template <int D>
-__device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* comb, const float* cml,
-                                              float* red, int b, int h, int item) {
-    const int tid = threadIdx.x;
-    const int gqa = a.lo.gqa;
-    float* wgt = red;   // [head][4 warps]
-    if (tid < gqa) {
-        float M = -INFINITY, l = 0.0f;
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, cml[2 * (w * gqa + tid)]);
-        for (int w = 0; w < 4; ++w) {
-            const float* mlw = cml + 2 * (w * gqa + tid);
-            const float wt = mlw[1] > 0.0f ? fast_exp2(mlw[0] - M) : 0.0f;
-            wgt[tid * 4 + w] = wt;
-            l = fmaf(mlw[1], wt, l);
-        }
-        float* ml = reinterpret_cast<float*>(a.ws + a.plan.ws_ml_off) + 2 * slot_index(a, b, h, item, tid);
-        ml[0] = M;
-        ml[1] = l;
-    }
-    __syncthreads();
-    // the item's gqa slots are consecutive: gqa * D floats, four per thread and step
-    float4* wso = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.ws + a.plan.ws_o_off) +
-                                            slot_index(a, b, h, item, 0) * D);
-    for (int i = tid; i < gqa * D / 4; i += blockDim.x) {
-        const int head = (4 * i) / D;
-        float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float wt = wgt[head * 4 + w];
-            if (wt != 0.0f) {
-                const float4 v = reinterpret_cast<const float4*>(comb + w * gqa * D)[i];
-                o.x = fmaf(v.x, wt, o.x);
-                o.y = fmaf(v.y, wt, o.y);
-                o.z = fmaf(v.z, wt, o.z);
-                o.w = fmaf(v.w, wt, o.w);
-            }
-        }
-        wso[i] = o;
-    }
-}
-
-// ------------------------------------------------------------------------ window path
-// The bf16 window of a KIVI cache.  Keys and queries are exact bf16 values, so the scores
-// go straight to the tensor cores (no conversion, no operand split): rows = 16 tokens,
-// columns = up to 8 query heads.  Each warp takes one 16-token tile and keeps its own
-// softmax partial; P.V runs on the tensor cores too, with V^T fragments read from the
-// token-major rows by ldmatrix.trans and p split into bf16 major and minor parts.  The
-// block then combines its 4 warps.
-template <int D, int NT>
-__device__ void window_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& so, int b, int h,
-                            int item, int64_t t0, int64_t t1) {
-    constexpr int KSTEPS = D / 16;
-    constexpr int MTV = D / 16;
-    const Layout& lo = a.lo;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
-    const int cnt = static_cast<int>(t1 - t0);
-    const int gqa = lo.gqa;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + so.bar);
-    float* red = reinterpret_cast<float*>(smem + so.red);
-    float* comb = reinterpret_cast<float*>(smem + so.sc);       // [warp][head][D]
-    float* cml = comb + 4 * gqa * D;                            // [warp][head][m, l]
-    float* pw = reinterpret_cast<float*>(smem + so.pw);         // [warp][16 tokens][8 heads]
-    uint8_t* data = smem + so.data;
-    const int64_t u = unit_index(lo, a.layer, b, h);
-
-    if (tid == 0) mbar_init(bar, 1);
-    __syncthreads();
-    if (tid == 0) {
-        const uint8_t* ring = a.cache + lo.ring_off + u * lo.C * (int64_t)(4 * D);
-        const int s0 = static_cast<int>(t0 % lo.C);
-        const int first = cnt < lo.C - s0 ? cnt : lo.C - s0;
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * 4 * D);
-        bulk_copy_pieces(data, ring + (int64_t)s0 * 4 * D, static_cast<uint32_t>(first) * 4 * D, bar);
-        if (cnt > first)
-            bulk_copy_pieces(data + (int64_t)first * 4 * D, ring, static_cast<uint32_t>(cnt - first) * 4 * D, bar);
-    }
-    // query operand: column g = head g (zero beyond gqa), k = channel pairs (2t, 2t+1) and
-    // (2t+8, 2t+9) of each 16-channel step, straight from the caller's bf16 query
-    uint32_t bq[KSTEPS][2];
-    {
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            reinterpret_cast<const uint16_t*>(a.q) + ((int64_t)b * lo.Hq + (int64_t)h * gqa + g) * D);
-#pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks) {
-            bq[ks][0] = g < gqa ? qrow[(16 * ks + 2 * tig) / 2] : 0u;
-            bq[ks][1] = g < gqa ? qrow[(16 * ks + 8 + 2 * tig) / 2] : 0u;
-        }
-    }
-    const bool ok = wait_staged(bar, a.ws);
-    const int tok0 = 16 * warp;
-    const int ntok = cnt - tok0 < 0 ? 0 : (cnt - tok0 > 16 ? 16 : cnt - tok0);
-    float oacc[MTV][NT][4];
-#pragma unroll
-    for (int mt = 0; mt < MTV; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.0f;
-    float mh = -INFINITY, lh = 0.0f;      // this lane's head (lane < gqa): max and sum
-    if (ok && ntok > 0) {
-        // scores: rows g, g + 8 of the tile (tokens beyond the window read as zero rows)
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        const uint8_t* r0 = data + (int64_t)(tok0 + g) * 4 * D;
-        const uint8_t* r1 = data + (int64_t)(tok0 + g + 8) * 4 * D;
-        const bool v0 = g < ntok, v1 = g + 8 < ntok;
-#pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks) {
-            uint32_t af[4];
-            af[0] = v0 ? *reinterpret_cast<const uint32_t*>(r0 + 2 * (16 * ks + 2 * tig)) : 0u;
-            af[1] = v1 ? *reinterpret_cast<const uint32_t*>(r1 + 2 * (16 * ks + 2 * tig)) : 0u;
-            af[2] = v0 ? *reinterpret_cast<const uint32_t*>(r0 + 2 * (16 * ks + 8 + 2 * tig)) : 0u;
-            af[3] = v1 ? *reinterpret_cast<const uint32_t*>(r1 + 2 * (16 * ks + 8 + 2 * tig)) : 0u;
-            mma_16816_bf16(acc, af, bq[ks][0], bq[ks][1]);
-        }
-        // lane (g, t) holds heads 2t, 2t+1 for tokens g and g + 8
-        float sc[2][2];
-        sc[0][0] = v0 ? acc[0] * a.qscale : -INFINITY;
-        sc[0][1] = v0 ? acc[1] * a.qscale : -INFINITY;
-        sc[1][0] = v1 ? acc[2] * a.qscale : -INFINITY;
-        sc[1][1] = v1 ? acc[3] * a.qscale : -INFINITY;
-        float m0 = fmaxf(sc[0][0], sc[1][0]), m1 = fmaxf(sc[0][1], sc[1][1]);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
-            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
-        }
-        float* pt = pw + warp * 16 * 8;
-        const float p00 = v0 ? fast_exp2(sc[0][0] - m0) : 0.0f, p01 = v0 ? fast_exp2(sc[0][1] - m1) : 0.0f;
-        const float p10 = v1 ? fast_exp2(sc[1][0] - m0) : 0.0f, p11 = v1 ? fast_exp2(sc[1][1] - m1) : 0.0f;
-        pt[g * 8 + 2 * tig] = p00;
-        pt[g * 8 + 2 * tig + 1] = p01;
-        pt[(g + 8) * 8 + 2 * tig] = p10;
-        pt[(g + 8) * 8 + 2 * tig + 1] = p11;
-        float l0 = p00 + p10, l1 = p01 + p11;
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-        }
-        // lane hh (< gqa) keeps head hh's max and sum: heads 2t, 2t+1 live in lanes t
-        const int src = (lane < 8 ? lane : 0) >> 1;
-        const float mm0 = __shfl_sync(0xffffffffu, m0, src), mm1 = __shfl_sync(0xffffffffu, m1, src);
-        const float ll0 = __shfl_sync(0xffffffffu, l0, src), ll1 = __shfl_sync(0xffffffffu, l1, src);
-        mh = (lane & 1) ? mm1 : mm0;
-        lh = (lane & 1) ? ll1 : ll0;
-        // value rows past the window's end hold stale bytes: zero them (their p is 0,
-        // and a stale pattern could read as NaN)
-        if (ntok < 16) {
-            for (int i = ntok + (lane >> 4); i < 16; i += 2) {
-                uint4* vr = reinterpret_cast<uint4*>(data + (int64_t)(tok0 + i) * 4 * D + 2 * D);
-                for (int e = lane & 15; e < D / 8; e += 16) vr[e] = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        __syncwarp();
-        // values on the tensor cores: A = the 16 x 16 (channels x tokens) tile of V^T, read
-        // from the token-major bf16 rows by ldmatrix.trans; B = p (k = tokens, column
-        // 2h + part) split into bf16 major and minor parts, from the warp's p table
-        uint32_t b0[NT], b1[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int head = 4 * nt + (g >> 1);
-            const float p0 = pt[(2 * tig) * 8 + head], p1 = pt[(2 * tig + 1) * 8 + head];
-            const float p2 = pt[(2 * tig + 8) * 8 + head], p3 = pt[(2 * tig + 9) * 8 + head];
-            const __nv_bfloat162 m01 = __floats2bfloat162_rn(p0, p1), m23 = __floats2bfloat162_rn(p2, p3);
-            const float2 f01 = __bfloat1622float2(m01), f23 = __bfloat1622float2(m23);
-            const __nv_bfloat162 r01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
-            const __nv_bfloat162 r23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
-            const uint32_t um01 = *reinterpret_cast<const uint32_t*>(&m01), um23 = *reinterpret_cast<const uint32_t*>(&m23);
-            const uint32_t ur01 = *reinterpret_cast<const uint32_t*>(&r01), ur23 = *reinterpret_cast<const uint32_t*>(&r23);
-            b0[nt] = (g & 1) ? ur01 : um01;
-            b1[nt] = (g & 1) ? ur23 : um23;
-        }
-        // ldmatrix rows: lane l addresses token (l mod 8) + 8 (l / 16), channels from
-        // 16 q + 8 ((l / 8) mod 2): the four 8 x 8 blocks land as a0..a3
-        const uint32_t vrow = smem_addr(data) + (tok0 + (lane & 7) + 8 * (lane >> 4)) * 4 * D + 2 * D +
-                              2 * 8 * ((lane >> 3) & 1);
-#pragma unroll
-        for (int q = 0; q < MTV; ++q) {
-            uint32_t af[4];
-            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(af[0]), "=r"(af[1]), "=r"(af[2]), "=r"(af[3])
-                         : "r"(vrow + 32 * q)
-                         : "memory");
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_16816_bf16(oacc[q][nt], af, b0[nt], b1[nt]);
-        }
-    }
-    // warp partial into shared memory, then the 4 warps combined
-    float* cw = comb + warp * gqa * D;
-    const bool wlive = ok && ntok > 0;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int head = 4 * nt + tig;
-        if (head < gqa && wlive) {
-#pragma unroll
-            for (int mt = 0; mt < MTV; ++mt) {
-                const int c0 = 16 * mt + g;
-                cw[head * D + c0] = oacc[mt][nt][0] + oacc[mt][nt][1];
-                cw[head * D + c0 + 8] = oacc[mt][nt][2] + oacc[mt][nt][3];
-            }
-        }
-    }
-    if (lane < gqa) {
-        cml[2 * (warp * gqa + lane)] = wlive ? mh : -INFINITY;
-        cml[2 * (warp * gqa + lane) + 1] = wlive ? lh : 0.0f;
-    }
-    __syncthreads();
-    combine_warps<D>(a, comb, cml, red, b, h, item);
-}
-
-// ------------------------------------------------------------------------ packed path
 // Loads from the staged chunk by 32-bit shared-window address.  They are volatile so the
 // compiler keeps them after the barrier waits (volatile asm with a memory clobber) that
 // make the bulk copies visible, and before the barrier that frees the stage.
@@ -544,6 +607,399 @@ __device__ __forceinline__ void lds_words(uint32_t a, uint32_t (&w)[N]) {
     }
 }
 
+// ------------------------------------------------------------------------ row path (INT8, INT4)
+// Per-token rows, CHR tokens per chunk: a warp per token for the scores, a thread per
+// channel for the values, and a running softmax (per-head max M and sum L in shared memory,
+// per-thread outputs in registers) across the chunks of the run.  INT4 rows hold two
+// channels per byte (even channel in the low four bits, two's complement).
+template <int D>
+__device__ __forceinline__ int rows_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64_t slot, int64_t t0,
+                                      int64_t t1, uint32_t phase) {
+    const SmemOffsets so = decode_smem(a.lo, a.plan);
+    constexpr int CPL = (D + 31) / 32;              // channels per lane (scores)
+    constexpr int CPT = (D + kDecodeThreads - 1) / kDecodeThreads;   // channels per thread (values)
+    const Layout& lo = a.lo;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int CHR = a.plan.CHR, gqa = lo.gqa;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + so.bar);
+    float* red = reinterpret_cast<float*>(smem + so.red);
+    float* hstat = reinterpret_cast<float*>(smem + so.hstat);    // M[32], L[32], alpha[32]
+    float* qs = reinterpret_cast<float*>(smem + so.qs);
+    float* sc = reinterpret_cast<float*>(smem + so.sc);
+    uint8_t* data = smem + so.data;
+    const int64_t u = unit_index(lo, a.layer, b, h);
+    const uint8_t* unit = a.cache + lo.data_off + u * lo.unit;
+    const bool int4 = lo.scheme == KVQ_SCHEME_INT4;
+    const int RB = int4 ? D / 2 : D;                 // code bytes per row
+
+    load_query(a, b, h, qs);
+    if (tid < 32) {
+        hstat[tid] = -INFINITY;
+        hstat[32 + tid] = 0.0f;
+    }
+    float o[CPT][8];
+#pragma unroll
+    for (int x = 0; x < CPT; ++x)
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh) o[x][hh] = 0.0f;
+
+    for (int64_t c0 = t0; c0 < t1; c0 += CHR) {
+        const int cnt = static_cast<int>(t1 - c0 < CHR ? t1 - c0 : CHR);
+        __syncthreads();    // the previous chunk is done with the stage
+        if (tid == 0) {
+            const uint32_t cb = static_cast<uint32_t>(cnt) * RB;
+            const uint32_t sb = static_cast<uint32_t>((cnt + 3) / 4 * 4) * 4;
+            mbar_arrive_expect_tx(bars, 2 * cb + 2 * sb);
+            bulk_copy_pieces(data, unit + c0 * RB, cb, bars);
+            bulk_copy_pieces(data + (int64_t)CHR * D, unit + (int64_t)lo.T16 * RB + c0 * RB, cb, bars);
+            const uint8_t* scales = unit + 2 * (int64_t)lo.T16 * RB;
+            bulk_copy_pieces(data + 2 * (int64_t)CHR * D, scales + 4 * c0, sb, bars);
+            bulk_copy_pieces(data + 2 * (int64_t)CHR * D + 4 * CHR, scales + 4 * (int64_t)lo.T16 + 4 * c0, sb, bars);
+        }
+        if (!wait_stage(bars, 0, phase, a.ws)) {
+            empty_partial(a, slot);
+            return -1;
+        }
+        const int8_t* kc = reinterpret_cast<const int8_t*>(data);
+        const int8_t* vc = reinterpret_cast<const int8_t*>(data + (int64_t)CHR * D);
+        const float* ks = reinterpret_cast<const float*>(data + 2 * (int64_t)CHR * D);
+        const float* vs = ks + CHR;
+        // the integer code of channel c of row i (a sign-extended nibble for INT4)
+        auto code = [&](const int8_t* rows, int i, int c) -> int {
+            if (!int4) return rows[i * D + c];
+            const uint32_t byte = static_cast<uint8_t>(rows[i * (D / 2) + c / 2]);
+            return static_cast<int>(byte << ((c & 1) ? 24 : 28)) >> 28;
+        };
+        // scores: a warp per token, lanes over channels, one reduction per head
+        float hmax[8];
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh) hmax[hh] = -INFINITY;
+        for (int i = warp; i < cnt; i += 4) {
+            float kv[CPL];
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                const int c = lane + 32 * j;
+                kv[j] = c < D ? static_cast<float>(code(kc, i, c)) * ks[i] : 0.0f;
+            }
+#pragma unroll
+            for (int hh = 0; hh < 8; ++hh) {
+                if (hh >= gqa) break;
+                float acc = 0.0f;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    const int c = lane + 32 * j;
+                    if (c < D) acc = fmaf(qs[hh * D + c], kv[j], acc);
+                }
+                acc = warp_sum(acc);
+                if (lane == 0) sc[hh * CHR + i] = acc;
+                hmax[hh] = fmaxf(hmax[hh], acc);
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh)
+            if (lane == 0 && hh < gqa) red[warp * 32 + hh] = hmax[hh];
+        __syncthreads();
+        // running max per head, the rescale factor of what came before, p in place
+        if (tid < gqa) {
+            float m = hstat[tid];
+            for (int w = 0; w < 4; ++w) m = fmaxf(m, red[w * 32 + tid]);
+            hstat[64 + tid] = hstat[tid] > -INFINITY ? fast_exp2(hstat[tid] - m) : 0.0f;
+            hstat[tid] = m;
+        }
+        __syncthreads();
+        for (int hh = 0; hh < gqa; ++hh) {
+            const float m = hstat[hh];
+            float part = 0.0f;
+            for (int t = tid; t < cnt; t += blockDim.x) {
+                const float p = fast_exp2(sc[hh * CHR + t] - m);
+                sc[hh * CHR + t] = p;
+                part += p;
+            }
+            part = warp_sum(part);
+            if (lane == 0) red[warp * 32 + hh] = part;
+        }
+        __syncthreads();
+        if (tid < gqa) {
+            float l = 0.0f;
+            for (int w = 0; w < 4; ++w) l += red[w * 32 + tid];
+            hstat[32 + tid] = fmaf(hstat[32 + tid], hstat[64 + tid], l);
+        }
+        // values: a thread per channel
+#pragma unroll
+        for (int x = 0; x < CPT; ++x) {
+            const int c = tid + kDecodeThreads * x;
+            if (c < D) {
+#pragma unroll
+                for (int hh = 0; hh < 8; ++hh)
+                    if (hh < gqa) o[x][hh] *= hstat[64 + hh];
+                for (int i = 0; i < cnt; ++i) {
+                    const float v = static_cast<float>(code(vc, i, c)) * vs[i];
+#pragma unroll
+                    for (int hh = 0; hh < 8; ++hh)
+                        if (hh < gqa) o[x][hh] = fmaf(sc[hh * CHR + i], v, o[x][hh]);
+                }
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int x = 0; x < CPT; ++x) {
+        const int c = tid + kDecodeThreads * x;
+        if (c < D) {
+#pragma unroll
+            for (int hh = 0; hh < 8; ++hh)
+                if (hh < gqa) slot_o(a, slot, hh)[c] = o[x][hh];
+        }
+    }
+    if (tid < gqa) {
+        float* ml = slot_ml(a, slot, tid);
+        ml[0] = hstat[tid];
+        ml[1] = hstat[32 + tid];
+    }
+    return static_cast<int>(phase);
+}
+
+// Combine the 4 warps' partials of one run (comb[warp][head][D] = o, cml[warp][head] =
+// (m, l)) into the workspace slot.  Called by the whole block after a barrier.  A warp
+// without tokens leaves m = -inf, l = 0 and its o unwritten; it gets weight 0 and its o is
+// never read.
+template <int D>
+__device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* comb, const float* cml,
+                                              float* red, int64_t slot) {
+    const int tid = threadIdx.x;
+    const int gqa = a.lo.gqa;
+    float* wgt = red;   // [head][4 warps]
+    if (tid < gqa) {
+        float M = -INFINITY, l = 0.0f;
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, cml[2 * (w * gqa + tid)]);
+        for (int w = 0; w < 4; ++w) {
+            const float* mlw = cml + 2 * (w * gqa + tid);
+            const float wt = mlw[1] > 0.0f ? fast_exp2(mlw[0] - M) : 0.0f;
+            wgt[tid * 4 + w] = wt;
+            l = fmaf(mlw[1], wt, l);
+        }
+        float* ml = slot_ml(a, slot, tid);
+        ml[0] = M;
+        ml[1] = l;
+    }
+    __syncthreads();
+    // the slot's gqa heads are consecutive: gqa * D floats, four per thread and step
+    float4* wso = reinterpret_cast<float4*>(slot_o(a, slot, 0));
+    for (int i = tid; i < gqa * D / 4; i += blockDim.x) {
+        const int head = (4 * i) / D;
+        float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float wt = wgt[head * 4 + w];
+            if (wt != 0.0f) {
+                const float4 v = reinterpret_cast<const float4*>(comb + w * gqa * D)[i];
+                o.x = fmaf(v.x, wt, o.x);
+                o.y = fmaf(v.y, wt, o.y);
+                o.z = fmaf(v.z, wt, o.z);
+                o.w = fmaf(v.w, wt, o.w);
+            }
+        }
+        wso[i] = o;
+    }
+}
+
+// ------------------------------------------------------------------------ window path
+// The bf16 window of a KIVI cache, CHR = 64 tokens per chunk.  Keys and queries are exact
+// bf16 values, so the scores go straight to the tensor cores (no conversion, no operand
+// split): rows = 16 tokens, columns = up to 8 query heads.  Each warp takes one 16-token
+// tile of every chunk and keeps its own running softmax (max and sum per head, rescaled
+// output); P.V runs on the tensor cores too, with V^T fragments read from the
+// token-major rows by ldmatrix.trans and p split into bf16 major and minor parts.  The
+// block then combines its 4 warps.
+template <int D, int NT>
+__device__ __forceinline__ int window_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64_t slot,
+                                        int64_t t0, int64_t t1, uint32_t phase) {
+    const SmemOffsets so = decode_smem(a.lo, a.plan);
+    constexpr int KSTEPS = D / 16;
+    constexpr int MTV = D / 16;
+    const Layout& lo = a.lo;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+    const int gqa = lo.gqa, CHR = a.plan.CHR;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + so.bar);
+    float* red = reinterpret_cast<float*>(smem + so.red);
+    float* comb = reinterpret_cast<float*>(smem + so.sc);       // [warp][head][D]
+    float* cml = comb + 4 * gqa * D;                            // [warp][head][m, l]
+    float* pw = reinterpret_cast<float*>(smem + so.pw);         // [warp][16 tokens][8 heads]
+    uint8_t* data = smem + so.data;
+    const int64_t u = unit_index(lo, a.layer, b, h);
+    const uint8_t* ring = a.cache + lo.ring_off + u * lo.C * (int64_t)(4 * D);
+    // the window's tokens follow the packed ones: part-1 token i is absolute token qn + i
+    const int64_t qn = seq_state(a, b).y;
+
+    // query operand: column g = head g (zero beyond gqa), k = channel pairs (2t, 2t+1) and
+    // (2t+8, 2t+9) of each 16-channel step: the caller's bf16 query rows, staged once in
+    // shared memory (rows gqa..7 zero) and read per tile
+    uint32_t* qw = reinterpret_cast<uint32_t*>(smem + so.qs);   // [8 heads][D / 2] words
+    {
+        const uint32_t* qsrc = reinterpret_cast<const uint32_t*>(
+            reinterpret_cast<const uint16_t*>(a.q) + ((int64_t)b * lo.Hq + (int64_t)h * gqa) * D);
+        for (int i = tid; i < 8 * D / 2; i += blockDim.x) qw[i] = i < gqa * D / 2 ? qsrc[i] : 0u;
+    }
+    const uint32_t qlane = smem_addr(qw) + (g * (D / 2) + tig) * 4;
+    float oacc[MTV][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < MTV; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.0f;
+    // running max of heads 2 tig, 2 tig + 1 (the lane's score columns) and the lane's
+    // partial sums of their p
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.0f, lB = 0.0f;
+    for (int64_t c0 = t0; c0 < t1; c0 += CHR) {
+        const int cnt = static_cast<int>(t1 - c0 < CHR ? t1 - c0 : CHR);
+        __syncthreads();    // the previous chunk is done with the stage
+        if (tid == 0) {
+            const int C = lo.C;
+            const int s0 = static_cast<int>((qn + c0) % C);
+            const int first = cnt < C - s0 ? cnt : C - s0;
+            mbar_arrive_expect_tx(bars, static_cast<uint32_t>(cnt) * 4 * D);
+            bulk_copy_pieces(data, ring + (int64_t)s0 * 4 * D, static_cast<uint32_t>(first) * 4 * D, bars);
+            if (cnt > first)
+                bulk_copy_pieces(data + (int64_t)first * 4 * D, ring, static_cast<uint32_t>(cnt - first) * 4 * D, bars);
+        }
+        if (!wait_stage(bars, 0, phase, a.ws)) {
+            empty_partial(a, slot);
+            return -1;
+        }
+        const int tok0 = 16 * warp;
+        const int ntok = cnt - tok0 < 0 ? 0 : (cnt - tok0 > 16 ? 16 : cnt - tok0);
+        if (ntok > 0) {
+            // scores: rows g, g + 8 of the tile (tokens beyond the window read as zero rows)
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint8_t* r0 = data + (int64_t)(tok0 + g) * 4 * D;
+            const uint8_t* r1 = data + (int64_t)(tok0 + g + 8) * 4 * D;
+            const bool v0 = g < ntok, v1 = g + 8 < ntok;
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                uint32_t af[4];
+                af[0] = v0 ? *reinterpret_cast<const uint32_t*>(r0 + 2 * (16 * ks + 2 * tig)) : 0u;
+                af[1] = v1 ? *reinterpret_cast<const uint32_t*>(r1 + 2 * (16 * ks + 2 * tig)) : 0u;
+                af[2] = v0 ? *reinterpret_cast<const uint32_t*>(r0 + 2 * (16 * ks + 8 + 2 * tig)) : 0u;
+                af[3] = v1 ? *reinterpret_cast<const uint32_t*>(r1 + 2 * (16 * ks + 8 + 2 * tig)) : 0u;
+                mma_16816_bf16(acc, af, lds32(qlane + 32 * ks), lds32(qlane + 32 * ks + 16));
+            }
+            // lane (g, t) holds heads 2t, 2t+1 for tokens g and g + 8
+            float sc[2][2];
+            sc[0][0] = v0 ? acc[0] * a.qscale : -INFINITY;
+            sc[0][1] = v0 ? acc[1] * a.qscale : -INFINITY;
+            sc[1][0] = v1 ? acc[2] * a.qscale : -INFINITY;
+            sc[1][1] = v1 ? acc[3] * a.qscale : -INFINITY;
+            float m0 = fmaxf(sc[0][0], sc[1][0]), m1 = fmaxf(sc[0][1], sc[1][1]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+            }
+            // new running maxima (finite: the tile has a token) and the factors that
+            // rescale what the warp accumulated before
+            const float MA = fmaxf(mA, m0), MB = fmaxf(mB, m1);
+            const float aA = mA > -INFINITY ? fast_exp2(mA - MA) : 0.0f;
+            const float aB = mB > -INFINITY ? fast_exp2(mB - MB) : 0.0f;
+            mA = MA;
+            mB = MB;
+            float* pt = pw + warp * 16 * 8;
+            const float p00 = v0 ? fast_exp2(sc[0][0] - MA) : 0.0f, p01 = v0 ? fast_exp2(sc[0][1] - MB) : 0.0f;
+            const float p10 = v1 ? fast_exp2(sc[1][0] - MA) : 0.0f, p11 = v1 ? fast_exp2(sc[1][1] - MB) : 0.0f;
+            pt[g * 8 + 2 * tig] = p00;
+            pt[g * 8 + 2 * tig + 1] = p01;
+            pt[(g + 8) * 8 + 2 * tig] = p10;
+            pt[(g + 8) * 8 + 2 * tig + 1] = p11;
+            lA = fmaf(lA, aA, p00 + p10);
+            lB = fmaf(lB, aB, p01 + p11);
+            // the value accumulators of lane (g, t) hold head 4 nt + t: its factor comes
+            // from lane (4 nt + t) / 2 of the score layout
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hv = 4 * nt + tig;
+                const float xa = __shfl_sync(0xffffffffu, aA, hv >> 1);
+                const float xb = __shfl_sync(0xffffffffu, aB, hv >> 1);
+                const float f = (hv & 1) ? xb : xa;
+#pragma unroll
+                for (int mt = 0; mt < MTV; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) oacc[mt][nt][e] *= f;
+            }
+            // value rows past the window's end hold stale bytes: zero them (their p is 0,
+            // and a stale pattern could read as NaN)
+            if (ntok < 16) {
+                for (int i = ntok + (lane >> 4); i < 16; i += 2) {
+                    uint4* vr = reinterpret_cast<uint4*>(data + (int64_t)(tok0 + i) * 4 * D + 2 * D);
+                    for (int e = lane & 15; e < D / 8; e += 16) vr[e] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            __syncwarp();
+            // values on the tensor cores: A = the 16 x 16 (channels x tokens) tile of V^T, read
+            // from the token-major bf16 rows by ldmatrix.trans; B = p (k = tokens, column
+            // 2h + part) split into bf16 major and minor parts, from the warp's p table
+            uint32_t b0[NT], b1[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int head = 4 * nt + (g >> 1);
+                const float p0 = pt[(2 * tig) * 8 + head], p1 = pt[(2 * tig + 1) * 8 + head];
+                const float p2 = pt[(2 * tig + 8) * 8 + head], p3 = pt[(2 * tig + 9) * 8 + head];
+                const __nv_bfloat162 m01 = __floats2bfloat162_rn(p0, p1), m23 = __floats2bfloat162_rn(p2, p3);
+                const float2 f01 = __bfloat1622float2(m01), f23 = __bfloat1622float2(m23);
+                const __nv_bfloat162 r01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
+                const __nv_bfloat162 r23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
+                const uint32_t um01 = *reinterpret_cast<const uint32_t*>(&m01), um23 = *reinterpret_cast<const uint32_t*>(&m23);
+                const uint32_t ur01 = *reinterpret_cast<const uint32_t*>(&r01), ur23 = *reinterpret_cast<const uint32_t*>(&r23);
+                b0[nt] = (g & 1) ? ur01 : um01;
+                b1[nt] = (g & 1) ? ur23 : um23;
+            }
+            // ldmatrix rows: lane l addresses token (l mod 8) + 8 (l / 16), channels from
+            // 16 q + 8 ((l / 8) mod 2): the four 8 x 8 blocks land as a0..a3
+            const uint32_t vrow = smem_addr(data) + (tok0 + (lane & 7) + 8 * (lane >> 4)) * 4 * D + 2 * D +
+                                  2 * 8 * ((lane >> 3) & 1);
+#pragma unroll
+            for (int q = 0; q < MTV; ++q) {
+                uint32_t af[4];
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(af[0]), "=r"(af[1]), "=r"(af[2]), "=r"(af[3])
+                             : "r"(vrow + 32 * q)
+                             : "memory");
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_16816_bf16(oacc[q][nt], af, b0[nt], b1[nt]);
+            }
+        }
+    }
+    // warp partial into shared memory, then the 4 warps combined
+    float* cw = comb + warp * gqa * D;
+    const bool wlive = mA > -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int head = 4 * nt + tig;
+        if (head < gqa && wlive) {
+#pragma unroll
+            for (int mt = 0; mt < MTV; ++mt) {
+                const int c0 = 16 * mt + g;
+                cw[head * D + c0] = oacc[mt][nt][0] + oacc[mt][nt][1];
+                cw[head * D + c0 + 8] = oacc[mt][nt][2] + oacc[mt][nt][3];
+            }
+        }
+    }
+    // lane hh (< gqa) keeps head hh's max and sum: heads 2t, 2t+1 live in lanes t
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        lA += __shfl_xor_sync(0xffffffffu, lA, off);
+        lB += __shfl_xor_sync(0xffffffffu, lB, off);
+    }
+    const int src = (lane < 8 ? lane : 0) >> 1;
+    const float mm0 = __shfl_sync(0xffffffffu, mA, src), mm1 = __shfl_sync(0xffffffffu, mB, src);
+    const float ll0 = __shfl_sync(0xffffffffu, lA, src), ll1 = __shfl_sync(0xffffffffu, lB, src);
+    if (lane < gqa) {
+        cml[2 * (warp * gqa + lane)] = wlive ? ((lane & 1) ? mm1 : mm0) : -INFINITY;
+        cml[2 * (warp * gqa + lane) + 1] = wlive ? ((lane & 1) ? ll1 : ll0) : 0.0f;
+    }
+    __syncthreads();
+    combine_warps<D>(a, comb, cml, red, slot);
+    return static_cast<int>(phase);
+}
+
+// ------------------------------------------------------------------------ packed path
 // 2^k as a float for -126 <= k <= 127 (exact).
 __device__ __forceinline__ float exp2i(int k) { return __int_as_float((127 + k) << 23); }
 // 2^k as an fp16 pair for -14 <= k <= 15 (exact).
@@ -587,8 +1043,9 @@ __device__ __forceinline__ uint32_t split_mul(__half2 s, uint32_t x, uint32_t y)
 // accumulated rescaled by the exact power of two, when a larger scale arrives); the code
 // position p is fixed per accumulator element, so 2^(24 - p) is applied at the end.
 template <int D, int BITS, int NT>
-__device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& so, int b, int h,
-                            int item, int64_t t0, int64_t t1) {
+__device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64_t slot,
+                                        int64_t t0, int64_t t1, uint32_t phase) {
+    const SmemOffsets so = decode_smem(a.lo, a.plan);
     constexpr int CPW = 32 / BITS;          // key channels per 32-bit word
     constexpr int HPW = CPW / 2;            // code pairs per word (keys and values)
     constexpr int NPAIR = D / 8;            // code pairs per thread per token row
@@ -630,10 +1087,6 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         mbar_arrive_expect_tx(bar, bytes);
         bulk_copy_pieces(smem + so.data + sj * stage_bytes, src_groups + (int64_t)j * gpc * rec, bytes, bar);
     };
-    if (tid == 0) {
-        for (int s2 = 0; s2 < nstage; ++s2) mbar_init(bars + s2, 1);
-    }
-    __syncthreads();
     if (tid == 0) {
         for (int j = 0; j < nstage && j < nch; ++j) issue(j);
     }
@@ -746,20 +1199,16 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         for (int mt = 0; mt < MTV; ++mt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.0f;
     }
     int Ev = 15;
-    bool live = true;
     // the warp's tokens start W * warp tokens into every chunk: group g0 of the chunk's
     // records, offset ti0 in it (a group may be shared by two warps)
     const int g0 = (warp * W) / G, ti0 = (warp * W) % G;
     for (int j = 0; j < nch; ++j) {
         const int sj = nstage == 2 ? (j & 1) : 0;                       // stage of chunk j
-        const uint32_t par = nstage == 2 ? ((j >> 1) & 1) : (j & 1);    // its barrier phase
-        bool ok = mbar_wait_bounded(bars + sj, par, kWaitLimit);
-        ok = __syncthreads_and(ok);
-        if (!ok) {
-            if (tid == 0) atomicOr(reinterpret_cast<uint32_t*>(a.ws), KVQ_STATUS_TIMEOUT);
-            mbar_wait_bounded(bars + sj, par, kWaitLimit);
-            live = false;
-            break;
+        if (!wait_stage(bars, sj, phase, a.ws)) {
+            // the next chunk's copy may already be armed on the other stage
+            if (nstage == 2 && j + 1 < nch) drain_stage(bars, sj ^ 1, phase);
+            empty_partial(a, slot);
+            return -1;
         }
         const int ctok = min(ntok - j * CH, CH);
         const int wtok = ctok - warp * W < 0 ? 0 : (ctok - warp * W > W ? W : ctok - warp * W);   // multiple of 16
@@ -1060,7 +1509,7 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
     // ---- warp partial: undo the power-of-two scales, reduce l over the lanes of a head,
     // add the value offset term, combine the 4 warps in shared memory
     float* cw = comb + warp * gqa * D;
-    const bool wlive = live && mrun[0] > -INFINITY;
+    const bool wlive = mrun[0] > -INFINITY;
     const float zfac = exp2i(-Ev), lfac = exp2i(-Ev);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -1090,53 +1539,71 @@ __device__ void packed_item(const DecodeArgs& a, uint8_t* smem, const SmemOffset
         }
     }
     __syncthreads();
-    grid_launch_dependents();   // the merge may start launching; it waits for this grid
-    combine_warps<D>(a, comb, cml, red, b, h, item);
+    combine_warps<D>(a, comb, cml, red, slot);
+    return static_cast<int>(phase);
 }
 
-// One block per (item, kv head, sequence), in the order of block_work.  BITS == 0: no
-// packed path (INT8 rows).
+// One wave of blocks; block j takes its share of the layer's chunks (for_each_segment).
+// BITS == 0: no packed part (INT8 rows).
 template <int D, int BITS, int NT>
-__global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2) k_decode(DecodeArgs a) {
+__global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
+    k_decode(const __grid_constant__ DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     grid_dependency_wait();
-    const BlockWork bw = block_work(a.lo, a.plan);
-    const int item = bw.item, h = bw.h, b = bw.b;
-    const int32_t* st = state_ptr(a.lo, a.cache, a.layer, b);
-    const int64_t n = st[0], qn = st[1];
-    const ItemRange r = item_range(a.lo, a.plan, item, n, qn);
-    if (r.t0 >= r.t1) {
-        empty_partial(a, b, h, item);
-        return;
-    }
     const SmemOffsets so = decode_smem(a.lo, a.plan);
-    if constexpr (BITS != 0) {
-        if (item >= a.plan.NRC)
-            packed_item<D, BITS, NT>(a, smem, so, b, h, item, r.t0, r.t1);
-        else
-            window_item<D, NT>(a, smem, so, b, h, item, r.t0, r.t1);
-        return;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + so.bar);
+    if (threadIdx.x == 0) {
+        mbar_init(bars, 1);
+        mbar_init(bars + 1, 1);
+        mbar_init(bars + kSelfTestBar, 1);
     }
-    rows_item<D>(a, smem, so, b, h, item, r.t0, r.t1);
+    __syncthreads();
+    uint32_t phase = selftest_bits(a);
+    for_each_segment(
+        a, reinterpret_cast<int64_t*>(smem + so.red), reinterpret_cast<int2*>(smem + so.sst),
+        [&](int part, int b, int h, int64_t slot, int64_t t0, int64_t t1) -> bool {
+            int r;
+            if constexpr (BITS != 0) {
+                if (part == 0)
+                    r = packed_item<D, BITS, NT>(a, smem, b, h, slot, t0, t1, phase);
+                else
+                    r = window_item<D, NT>(a, smem, b, h, slot, t0, t1, phase);
+            } else {
+                r = rows_item<D>(a, smem, b, h, slot, t0, t1, phase);
+            }
+            if (r < 0) return false;
+            phase = static_cast<uint32_t>(r);
+            return true;
+        },
+        [&](int64_t slot) { empty_partial(a, slot); });
 }
 
-template <int D, int BITS, int NT>
-int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
-    auto fn = k_decode<D, BITS, NT>;
-    if (a.plan.smem > 48 * 1024 &&
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(a.plan.smem)) !=
-            cudaSuccess)
-        return KVQ_ERR_CUDA;
-    return launch_dependent(fn, decode_grid(a), kDecodeThreads, static_cast<size_t>(a.plan.smem), stream, a) == cudaSuccess
+// Launch of a decode kernel over one wave of resident blocks; records the block count in
+// a.plan.NB for the merge.
+template <typename K>
+int launch_wave(K fn, DecodeArgs& a, cudaStream_t stream) {
+    int nb = 0;
+    const int rc = decode_blocks(reinterpret_cast<const void*>(fn), kDecodeThreads, a.plan.smem, &nb);
+    if (rc != KVQ_OK) return rc;
+    a.plan.NB = nb;
+    a.plan.inv_nb = 1.0f / nb;
+    a.plan.unit_aligned = 2 * (int64_t)a.lo.B * a.lo.H <= nb ? 1 : 0;
+    return launch_dependent(fn, dim3(static_cast<unsigned>(nb)), kDecodeThreads, static_cast<size_t>(a.plan.smem),
+                            stream, a) == cudaSuccess
                ? KVQ_OK
                : KVQ_ERR_CUDA;
 }
 
+template <int D, int BITS, int NT>
+int launch_decode_t(DecodeArgs& a, cudaStream_t stream) {
+    return launch_wave(k_decode<D, BITS, NT>, a, stream);
+}
+
 // Dispatchers, one per translation unit.
-int launch_decode_kivi2(const DecodeArgs& a, cudaStream_t stream);
-int launch_decode_kivi4(const DecodeArgs& a, cudaStream_t stream);
-int launch_decode_kivi8(const DecodeArgs& a, cudaStream_t stream);
-int launch_decode_rows(const DecodeArgs& a, cudaStream_t stream);
-int launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi2(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi4(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi8(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_rows(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_fp8(DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace kvq

@@ -1,9 +1,9 @@
-// kvq_decode_fp8.cu -- single-query decode attention over FP8 E4M3 caches on the tensor
-// cores.
+// kvq_decode_fp8.cu -- single-query decode attention over FP8 (E4M3 or E5M2) caches on the
+// tensor cores.
 //
 // An E4M3 value is exactly an fp16 value (3 mantissa bits, exponents inside fp16's
-// range), so the codes go straight into mma.sync.m16n8k16 (f16 -> f32) after one
-// conversion per code pair.  The key and value scales are per (layer, kv head)
+// range), and an E5M2 value is the upper byte of its fp16 value, so the codes go straight
+// into mma.sync.m16n8k16 (f16 -> f32) after one conversion per code pair.  The key and value scales are per (layer, kv head)
 // ("How the KV cache is quantized": one scale per tensor or head), so the query operand
 // (query * key scale, split into fp16 major + minor parts) is built once per block and
 // stays in registers, and the value scale is applied once to the block's output.
@@ -18,21 +18,28 @@
 namespace kvq {
 namespace {
 
-// The four E4M3 codes of `w` as two fp16 pairs: lo <- bytes 0, 1 and hi <- bytes 2, 3 (the
+// The four FP8 codes of `w` as two fp16 pairs: lo <- bytes 0, 1 and hi <- bytes 2, 3 (the
 // lower byte of each 16-bit half to the lower fp16).  One conversion per pair, straight
-// from the register halves.
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}"
-        : "=r"(lo), "=r"(hi)
-        : "r"(w));
+// from the register halves; both FP8 formats convert to fp16 exactly.
+template <bool E5M2>
+__device__ __forceinline__ void fp8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    if constexpr (E5M2)
+        asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e5m2x2 %0, l;\n cvt.rn.f16x2.e5m2x2 %1, h;\n}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+    else
+        asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
 }
 
 // One FP8 work item: a run of chunks of CH = 4 * W tokens of one (sequence, kv head).
 // Each warp takes W tokens (whole 16-token tiles but the sequence's last) of a chunk and
 // keeps an online softmax across the item's chunks.
-template <int D, int NT>
-__device__ void fp8_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& so, int b, int h, int item,
-                         int64_t t0, int64_t t1) {
+template <int D, int NT, bool E5M2>
+__device__ __forceinline__ int fp8_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64_t slot, int64_t t0,
+                                     int64_t t1, uint32_t phase) {
+    const SmemOffsets so = decode_smem(a.lo, a.plan);
     constexpr int NPAIR = D / 8;            // B words per lane and head block
     constexpr int KSTEPS = D / 16;
     constexpr int MTV = D / 16;             // 16-channel tiles of the value contraction
@@ -67,10 +74,6 @@ __device__ void fp8_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& 
         bulk_copy_pieces(st, kbase + (int64_t)j * CH * D, kb, bar);
         bulk_copy_pieces(st + CH * D, vbase + (int64_t)j * CH * D, vb, bar);
     };
-    if (tid == 0) {
-        for (int s2 = 0; s2 < nstage; ++s2) mbar_init(bars + s2, 1);
-    }
-    __syncthreads();
     if (tid == 0) {
         for (int j = 0; j < nstage && j < nch; ++j) issue(j);
     }
@@ -156,18 +159,14 @@ __device__ void fp8_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& 
 #pragma unroll
         for (int mt = 0; mt < MTV; ++mt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.0f;
     }
-    bool live = true;
     const int wt0 = warp * W;               // the warp's first token of every chunk
     for (int j = 0; j < nch; ++j) {
         const int sj = nstage == 2 ? (j & 1) : 0;
-        const uint32_t par = nstage == 2 ? ((j >> 1) & 1) : (j & 1);
-        bool ok = mbar_wait_bounded(bars + sj, par, kWaitLimit);
-        ok = __syncthreads_and(ok);
-        if (!ok) {
-            if (tid == 0) atomicOr(reinterpret_cast<uint32_t*>(a.ws), KVQ_STATUS_TIMEOUT);
-            mbar_wait_bounded(bars + sj, par, kWaitLimit);
-            live = false;
-            break;
+        if (!wait_stage(bars, sj, phase, a.ws)) {
+            // the next chunk's copy may already be armed on the other stage
+            if (nstage == 2 && j + 1 < nch) drain_stage(bars, sj ^ 1, phase);
+            empty_partial(a, slot);
+            return -1;
         }
         const int cnt = min(CH, ntok - j * CH);
         const int wtok = cnt - wt0 < 0 ? 0 : (cnt - wt0 > W ? W : cnt - wt0);
@@ -194,8 +193,8 @@ __device__ void fp8_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& 
 #pragma unroll
                 for (int ks = 0; ks < KSTEPS; ++ks) {
                     uint32_t af[4];
-                    e4m3x4_to_f16x2x2(wa[ks], af[0], af[2]);
-                    e4m3x4_to_f16x2x2(wb[ks], af[1], af[3]);
+                    fp8x4_to_f16x2x2<E5M2>(wa[ks], af[0], af[2]);
+                    fp8x4_to_f16x2x2<E5M2>(wb[ks], af[1], af[3]);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma_16816(acc[ks & 1][nt], af, bq[nt][2 * ks], bq[nt][2 * ks + 1]);
                 }
@@ -266,8 +265,8 @@ __device__ void fp8_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& 
                     const uint32_t w0 = lds32(vt + 256 * q) & vmask;          // channel 16q + g
                     const uint32_t w1 = lds32(vt + 256 * q + 128) & vmask;    // channel 16q + g + 8
                     uint32_t af[4];
-                    e4m3x4_to_f16x2x2(w0, af[0], af[2]);
-                    e4m3x4_to_f16x2x2(w1, af[1], af[3]);
+                    fp8x4_to_f16x2x2<E5M2>(w0, af[0], af[2]);
+                    fp8x4_to_f16x2x2<E5M2>(w1, af[1], af[3]);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma_16816(oacc[q][nt], af, b0[nt], b1[nt]);
                 }
@@ -279,7 +278,7 @@ __device__ void fp8_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& 
     // ---- warp partial (o carries the value scale; o and l share the factor 2^15), then
     // the 4 warps combined in shared memory
     float* cw = comb + warp * gqa * D;
-    const bool wlive = live && mrun[0] > -INFINITY;
+    const bool wlive = mrun[0] > -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int head = 4 * nt + tig;
@@ -301,43 +300,45 @@ __device__ void fp8_item(const DecodeArgs& a, uint8_t* smem, const SmemOffsets& 
         }
     }
     __syncthreads();
-    grid_launch_dependents();   // the merge may start launching; it waits for this grid
-    combine_warps<D>(a, comb, cml, red, b, h, item);
+    combine_warps<D>(a, comb, cml, red, slot);
+    return static_cast<int>(phase);
 }
 
-// One block per (item, kv head, sequence), in the order of block_work.
-template <int D, int NT>
-__global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2) k_decode_fp8(DecodeArgs a) {
+// One wave of blocks; block j takes its share of the layer's chunks (for_each_segment).
+template <int D, int NT, bool E5M2>
+__global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
+    k_decode_fp8(const __grid_constant__ DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     grid_dependency_wait();
-    const BlockWork bw = block_work(a.lo, a.plan);
-    const int item = bw.item, h = bw.h, b = bw.b;
-    const int32_t* st = state_ptr(a.lo, a.cache, a.layer, b);
-    const int64_t n = st[0], qn = st[1];
-    const ItemRange r = item_range(a.lo, a.plan, item, n, qn);
-    if (r.t0 >= r.t1) {
-        empty_partial(a, b, h, item);
-        return;
-    }
     const SmemOffsets so = decode_smem(a.lo, a.plan);
-    fp8_item<D, NT>(a, smem, so, b, h, item, r.t0, r.t1);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + so.bar);
+    if (threadIdx.x == 0) {
+        mbar_init(bars, 1);
+        mbar_init(bars + 1, 1);
+        mbar_init(bars + kSelfTestBar, 1);
+    }
+    __syncthreads();
+    uint32_t phase = selftest_bits(a);
+    for_each_segment(
+        a, reinterpret_cast<int64_t*>(smem + so.red), reinterpret_cast<int2*>(smem + so.sst),
+        [&](int, int b, int h, int64_t slot, int64_t t0, int64_t t1) -> bool {
+            const int r = fp8_item<D, NT, E5M2>(a, smem, b, h, slot, t0, t1, phase);
+            if (r < 0) return false;
+            phase = static_cast<uint32_t>(r);
+            return true;
+        },
+        [&](int64_t slot) { empty_partial(a, slot); });
 }
 
 template <int D, int NT>
-int launch_fp8_t(const DecodeArgs& a, cudaStream_t stream) {
-    auto fn = k_decode_fp8<D, NT>;
-    if (a.plan.smem > 48 * 1024 &&
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(a.plan.smem)) !=
-            cudaSuccess)
-        return KVQ_ERR_CUDA;
-    return launch_dependent(fn, decode_grid(a), kDecodeThreads, static_cast<size_t>(a.plan.smem), stream, a) == cudaSuccess
-               ? KVQ_OK
-               : KVQ_ERR_CUDA;
+int launch_fp8_t(DecodeArgs& a, cudaStream_t stream) {
+    if (a.lo.scheme == KVQ_SCHEME_FP8_E5M2) return launch_wave(k_decode_fp8<D, NT, true>, a, stream);
+    return launch_wave(k_decode_fp8<D, NT, false>, a, stream);
 }
 
 }  // namespace
 
-int launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream) {
+int launch_decode_fp8(DecodeArgs& a, cudaStream_t stream) {
     const bool wide = a.lo.gqa > 4;
     switch (a.lo.D) {
         case 32: return wide ? launch_fp8_t<32, 2>(a, stream) : launch_fp8_t<32, 1>(a, stream);

@@ -4,7 +4,7 @@
 
 namespace kvq {
 
-int launch_decode_kivi4(const DecodeArgs& a, cudaStream_t stream) {
+int launch_decode_kivi4(DecodeArgs& a, cudaStream_t stream) {
     const bool wide = a.lo.gqa > 4;
     switch (a.lo.D) {
         case 64: return wide ? launch_decode_t<64, 4, 2>(a, stream) : launch_decode_t<64, 4, 1>(a, stream);

@@ -24,7 +24,9 @@
 //            of [K row bf16[D], V row bf16[D]]; token t (qn <= t < n) lives in slot t % C.
 //   INT8     per (layer, sequence, kv head), T16 = max_tokens rounded up to 16:
 //            K codes int8[T16][D], V codes int8[T16][D], K scale f32[T16], V scale f32[T16]
-//   FP8      scale table f32[layers][kv heads][2] (K, V), then per (layer, sequence, kv
+//   INT4     the same with K and V codes of D / 2 bytes per row: channel c in byte c / 2,
+//            low four bits for even c, high four for odd c (two's complement)
+//   FP8      (E4M3 or E5M2) scale table f32[layers][kv heads][2] (K, V), then per (layer, sequence, kv
 //            head): K codes e4m3[T16][D], each row's channels in fragment order (channel
 //            r of 16-channel block kb in quarter (r mod 8)/2 at byte 4 kb + 2 (r/8) +
 //            r mod 2); V codes e4m3 in 16-token tiles [channel][16], token tt at byte
@@ -52,32 +54,49 @@ struct Layout {
 
 inline int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 
-// Streaming multiprocessors of the GB300 the decode work is sized for.
-constexpr int kNumSMs = 152;
+// FP8 caches (E4M3 or E5M2 codes, per-(layer, kv head) scales) and per-token row caches
+// (INT8 or INT4 codes, per-(head, token) scales).
+__host__ __device__ inline bool is_fp8(int scheme) {
+    return scheme == KVQ_SCHEME_FP8_E4M3 || scheme == KVQ_SCHEME_FP8_E5M2;
+}
+__host__ __device__ inline bool is_rows(int scheme) {
+    return scheme == KVQ_SCHEME_INT8 || scheme == KVQ_SCHEME_INT4;
+}
 
-// How one decode step is split: every (sequence, kv head) "unit" gets NRC row chunks of
-// CHR tokens (the bf16 window for KIVI, all tokens for INT8/FP8) and NQ packed chunks of
-// CH tokens (KIVI groups), S = NRC + NQ work items in all.  A packed chunk is split among
-// the block's 4 warps, W = CH / 4 tokens (whole groups) each; a packed item covers CPI
-// consecutive chunks, staged through NSTAGE shared-memory buffers.  Each item leaves a
-// partial softmax result (m, l, o[D]) per query head in the workspace.
+// How one decode step is split.  Every (sequence, kv head) "unit" has two parts: part 0,
+// the packed tokens (KIVI groups, FP8 tiles), cut into chunks of CH tokens; part 1, the row
+// tokens (the KIVI bf16 window, INT8 rows), cut into chunks of CHR tokens.  A chunk costs
+// its tokens times cpt0 or cpt1 (16-byte units of the bytes a token reads), so the layer's
+// total cost C follows the real token counts in the cache state.  The decode runs NB
+// blocks, one wave of resident blocks; block j takes the chunks whose cost position starts
+// in [ceil(C j / NB), ceil(C (j + 1) / NB)) and leaves, for every part of a unit it
+// touches, one partial softmax result (m, l, o[D]) per query head in workspace slot
+// j + 2 unit + part.  A packed chunk is split among the block's 4 warps, W = CH / 4 tokens
+// (whole groups) each, staged through NSTAGE shared-memory buffers.
 struct DecodePlan {
-    int CH, W, CPI, NSTAGE, NQ, CHR, NRC, S, NT;
-    int64_t ws_o_off, ws_ml_off, ws_total;
+    int CH, W, NSTAGE, CHR, NT;
+    int NB;                          // decode blocks of the launch (set by the launcher)
+    int unit_aligned;                // 1: every unit gets whole blocks (set by the launcher)
+    int64_t cpt0, cpt1;              // scheduling cost of a packed token and of a row token
+    float inv_nb, inv_cc0, inv_cc1;  // 1 / NB and 1 / (chunk cost) of each part
+    int64_t nslot;                   // partial-result slots the workspace holds
+    int64_t ws_o_off, ws_ml_off, ws_total;   // partial o, partial (m, l)
     int64_t smem;
 };
 
 // Shared-memory carve of the decode block, identical on host and device.
 struct SmemOffsets {
-    int64_t bar, red, hstat, qs, qpa, qpb, pw, sc, data, total;
+    int64_t bar, red, hstat, sst, qs, qpa, qpb, pw, sc, data, total;
 };
 __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const DecodePlan& p) {
     SmemOffsets o;
     int64_t off = 0;
     o.bar = off;   off += 64;                         // mbarriers, one per stage
     o.red = off;   off += 4 * 32 * 4;                 // [warp][32] floats
-    o.hstat = off; off += 2 * 32 * 4;                 // per-head max and sum
-    o.qs = off;    off += (int64_t)lo.gqa * lo.D * 4; // scaled query, fp32
+    o.hstat = off; off += 4 * 32 * 4;                 // per-head running max, sum, rescale
+    o.sst = off;   off += 128 * 8;                    // sequence states (n, qn), batch <= 128
+    o.qs = off;                                       // scaled query fp32 [gqa][D], or the
+    off += (lo.gqa > 4 ? lo.gqa : 4) * (int64_t)lo.D * 4;   // window's bf16 query words [8][D / 2]
     o.qpa = off;   off += (int64_t)32 * p.NT * (lo.D / 8 + 4) * 4;   // query tables: [32 NT][D/8 + 4]
     o.qpb = off;   off += (int64_t)32 * p.NT * (lo.D / 8 + 4) * 4;
     o.pw = off;    off += 4 * 16 * 8 * 4;                // window path: [warp][token][head] p
@@ -96,7 +115,7 @@ __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const Decod
     if (lo.scheme == KVQ_SCHEME_KIVI) {
         rows = (int64_t)p.CHR * 4 * lo.D;
         packed = (int64_t)p.NSTAGE * (p.CH / lo.G) * lo.rec;
-    } else if (lo.scheme == KVQ_SCHEME_INT8) {
+    } else if (is_rows(lo.scheme)) {
         rows = (int64_t)p.CHR * (2 * lo.D + 8);
     } else {
         rows = (int64_t)p.NSTAGE * p.CH * 2 * lo.D;      // FP8: key rows + value tiles per stage
@@ -159,14 +178,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait: gives up after `limit` polls (each poll may suspend the thread for a
-// while), so a copy that never lands cannot hang the GPU.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
-constexpr uint32_t kWaitLimit = 1u << 22;
+// Bounded wait: gives up once `limit_ns` nanoseconds of the GPU's global timer have passed,
+// so a copy that never lands cannot hang the GPU.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+// A staged copy of at most a few tens of KiB lands in microseconds; one second means it
+// never will.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// Barrier slot (in the decode block's barrier area) that nothing ever completes: the
+// workspace self-test of the bounded waits waits on it.
+constexpr int kSelfTestBar = 2;
+constexpr uint32_t kSelfTestBit = 1u << 30;   // phase bits stay non-negative as an int
 
 // D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col)
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,

@@ -11,6 +11,8 @@ namespace kvq {
 constexpr int kSmallAppend = 16;  // appends of at most this many tokens run as one kernel
 
 int make_plan(const Layout& lo, DecodePlan* plan);
+int device_sm_count(int device);
+int decode_blocks(const void* fn, int threads, int64_t smem, int* nb);
 
 int launch_append(const Layout& lo, uint8_t* cache, int layer, int seq_begin, int seq_count,
                   const void* k_new, const void* v_new, int n_new, const int32_t* n_valid,

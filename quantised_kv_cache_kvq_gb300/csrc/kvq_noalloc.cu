@@ -10,6 +10,8 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "kvq_decode.cuh"
 #include "kvq_internal.cuh"
 #include "kvq_launch.h"
@@ -22,19 +24,60 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_B
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch on the current device, looked up once per device (with
-// that device current) and remembered.  Returns nullptr when the lookup fails.
+// The scratch's device address is a property of the module loaded into one CUDA context.
+// After cudaDeviceReset (or any release of the primary context) the module is loaded
+// again and the array may sit elsewhere, so a remembered address is only reused while the
+// device's current context is the one it was looked up in.  Contexts are told apart by
+// the driver's context ID (cuCtxGetId, unique for the life of the process), reached
+// through the runtime's driver entry points so that the library needs no link to the
+// driver library.  Without those entry points the address is looked up on every call.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void* ptr;
+};
+
+std::mutex g_mutex;
+ScratchEntry g_scratch[kMaxDevices] = {};
+bool g_entry_points_tried = false;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// ID of the calling thread's current context; false when it cannot be had.
+bool current_context_id(unsigned long long* id) {
+    if (!g_entry_points_tried) {
+        g_entry_points_tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+    }
+    if (!g_ctx_get_current || !g_ctx_get_id) return false;
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch in the current context of `device`, remembered per
+// (device, context).  Returns nullptr when the lookup fails.
 void* scratch_address(int device) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch_ptr[device] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        g_scratch_ptr[device] = p;
-    }
-    return g_scratch_ptr[device];
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    if (have_id && g_scratch[device].ptr != nullptr && g_scratch[device].ctx_id == id) return g_scratch[device].ptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_scratch[device].ctx_id = have_id ? id : 0ull;
+    g_scratch[device].ptr = have_id ? p : nullptr;
+    return p;
 }
 
 }  // namespace

@@ -67,6 +67,8 @@ def test_formula_mode_reproduces_the_pages_numbers():
     dict(bits=8, group_k=48, group_v=64, residual=20, head_dim=64, max_tokens=777),
     dict(scheme=1, head_dim=32, q_heads=4, kv_heads=4, max_tokens=256, in_dtype=1),
     dict(scheme=2, layers=32, batch=64, q_heads=32, kv_heads=8, max_tokens=8192),
+    dict(scheme=3, layers=2, batch=3, q_heads=32, kv_heads=8, max_tokens=1000),
+    dict(scheme=4, head_dim=64, q_heads=8, kv_heads=2, max_tokens=333, in_dtype=1),
     dict(residual=0, max_tokens=10),
 ])
 def test_layout_size_matches_the_specification(kw):
@@ -76,7 +78,7 @@ def test_layout_size_matches_the_specification(kw):
 
 
 BAD = [
-    (dict(scheme=3), N.KVQ_ERR_ARG),
+    (dict(scheme=5), N.KVQ_ERR_ARG),
     (dict(q_heads=6, kv_heads=4), N.KVQ_ERR_ARG),
     (dict(q_heads=48, kv_heads=2), N.KVQ_ERR_UNSUPPORTED),
     (dict(head_dim=96), N.KVQ_ERR_UNSUPPORTED),

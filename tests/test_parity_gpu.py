@@ -187,14 +187,15 @@ def test_int8_tiny_workload():
 
 @pytest.mark.parametrize("D,gqa,dtype", [(128, 4, "bf16"), (64, 8, "f32"), (256, 1, "bf16"), (32, 2, "f32")])
 def test_int8_and_fp8_ragged(D, gqa, dtype):
-    for scheme in ("int8", "fp8"):
+    for scheme in ("int8", "fp8", "fp8e5m2", "int4"):
         p = Pair(scheme, layers=2, batch=3, q_heads=2 * gqa, kv_heads=2, head_dim=D, max_tokens=333,
                  in_dtype=dtype)
         g = gen(D + gqa)
         k, v = p.rand_kv(3, 250, g)
         sc = None
-        if scheme == "fp8":
-            sc = torch.stack([k.float().abs().amax(dim=(0, 1, 3)), v.float().abs().amax(dim=(0, 1, 3))], 1) / 448
+        if scheme.startswith("fp8"):
+            fmax = 448.0 if scheme == "fp8" else 57344.0
+            sc = torch.stack([k.float().abs().amax(dim=(0, 1, 3)), v.float().abs().amax(dim=(0, 1, 3))], 1) / fmax
         p.append(1, k, v, n_valid=[250, 17, 0], fp8_scales=sc)
         for _ in range(5):
             k2, v2 = p.rand_kv(3, 1, g)
@@ -216,6 +217,20 @@ def test_fp8_saturation_and_subnormals():
     sc = torch.tensor([[1.0, 0.5]])
     p.append(0, k, v, fp8_scales=sc)
     p.assert_same_image()
+
+
+def test_fp8_e5m2_saturation_nonfinite_and_subnormals():
+    # E5M2 saturates at +-57344 (infinities included), keeps NaN as 0x7f and reaches
+    # subnormals down to 2^-16 of the scale; the codes must match the oracle byte for byte
+    p = Pair("fp8e5m2", batch=1, q_heads=4, kv_heads=1, head_dim=128, max_tokens=32)
+    g = gen(14)
+    k, v = p.rand_kv(1, 20, g)
+    k[0, 0, 0, :10] = torch.tensor([1e6, -1e6, 6e4, 57344.0, 3e-5, -2e-5, 0.0, -0.0, float("inf"), float("-inf")])
+    v[0, 1, 0, :2] = torch.tensor([float("nan"), 1.5e-5])
+    sc = torch.tensor([[1.0, 0.5]])
+    p.append(0, k, v, fp8_scales=sc)
+    p.assert_same_image()
+    assert p.status() == 4      # the non-finite inputs are flagged (and stored)
 
 
 def test_fp8_long_context_separate_merge():
@@ -243,3 +258,102 @@ def test_int8_merge_paths_at_the_boundary(max_tokens):
     p.assert_same_image()
     out, ref = p.decode(0, p.rand_q(g))
     assert_close(out, ref, what="int8 merge boundary %d" % max_tokens)
+
+
+# ------------------------------------------------------------------------- decode scheduling
+# The decode grid is one wave of resident blocks that split the layer's bytes evenly, so a
+# block may take the end of one unit and the start of the next, or nothing at all.  These
+# cases mix empty, one-token, window-only and long sequences in one batch.
+RAGGED_LENS = [0, 1, 5, 31, 32, 33, 160, 161, 700, 0, 2047, 3000, 17, 129, 64, 1000]
+
+
+@pytest.mark.parametrize("scheme,bits,G,R", [("kivi", 2, 32, 128), ("kivi", 4, 16, 8), ("fp8", 8, 32, 0),
+                                             ("int8", 8, 32, 0), ("fp8e5m2", 8, 32, 0), ("int4", 4, 32, 0)])
+def test_decode_schedule_ragged_batch(scheme, bits, G, R):
+    B = len(RAGGED_LENS)
+    p = Pair(scheme, batch=B, q_heads=16, kv_heads=4, head_dim=128, max_tokens=max(RAGGED_LENS) + 8,
+             bits=bits, group_k=G, group_v=32, residual=R)
+    g = gen(21 + bits + G)
+    k, v = p.rand_kv(B, max(RAGGED_LENS), g)
+    sc = None
+    if scheme.startswith("fp8"):
+        sc = torch.stack([k.float().abs().amax(dim=(0, 1, 3)), v.float().abs().amax(dim=(0, 1, 3))], 1) / 448
+    p.append(0, k, v, n_valid=RAGGED_LENS, fp8_scales=sc)
+    p.assert_same_image()
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="ragged %s" % scheme)
+    assert not out[0].any() and not out[9].any()       # empty sequences give 0
+    # a step later (every sequence one token longer)
+    k, v = p.rand_kv(B, 1, g)
+    p.append(0, k, v, fp8_scales=sc)
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="ragged %s after a step" % scheme)
+    assert p.status() == 0
+
+
+def test_decode_schedule_many_units_cost_ranges():
+    # 160 ragged sequences x 4 kv heads: more units than half the grid, so the decode splits
+    # the layer's bytes into equal cost ranges that cross unit boundaries (the other tests
+    # with few units give every unit whole blocks)
+    lens = [(37 * i * i + 11 * i) % 1900 for i in range(160)]
+    lens[5] = 0
+    p = Pair("kivi", batch=160, q_heads=16, kv_heads=4, head_dim=128, max_tokens=1920, bits=2, group_k=32,
+             group_v=32, residual=64)
+    g = gen(26)
+    for s0 in range(0, 160, 40):
+        k, v = p.rand_kv(40, max(lens[s0:s0 + 40]), g)
+        p.append(0, k, v, seq_begin=s0, n_valid=lens[s0:s0 + 40])
+    p.assert_same_image()
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="many units")
+    assert not out[5].any()
+    k, v = p.rand_kv(160, 1, g)
+    p.append(0, k, v)
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="many units after a step")
+
+
+def test_decode_schedule_total_smaller_than_the_grid():
+    # a few tokens in all: most blocks of the wave get no chunk, some units get one block
+    p = Pair("kivi", batch=3, q_heads=8, kv_heads=2, head_dim=64, max_tokens=64, bits=2, group_k=16,
+             group_v=16, residual=4)
+    g = gen(23)
+    k, v = p.rand_kv(3, 30, g)
+    p.append(0, k, v, n_valid=[30, 0, 3])
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="tiny total")
+    assert not out[1].any()
+
+
+def test_decode_all_sequences_empty():
+    p = Pair("kivi", batch=2, q_heads=8, kv_heads=2, head_dim=128, max_tokens=256, bits=2)
+    out, ref = p.decode(0, p.rand_q(gen(24)))
+    assert not out.any() and not ref.any()
+    assert p.status() == 0
+
+
+# ------------------------------------------------------------------------- bounded waits
+def test_bounded_wait_gives_up_and_reports_timeout():
+    # the workspace self-test word makes every decode block wait once on a barrier that
+    # nothing completes: the wait must give up (about a second), report
+    # KVQ_STATUS_TIMEOUT, leave empty partials (outputs 0) and keep the GPU usable
+    import quantised_kv_cache_kvq_gb300 as K
+    from quantised_kv_cache_kvq_gb300 import _native as N
+    p = Pair("kivi", batch=2, q_heads=8, kv_heads=2, head_dim=128, max_tokens=3000, bits=2, group_k=32,
+             group_v=32, residual=128)
+    g = gen(25)
+    k, v = p.rand_kv(2, 2900, g)
+    p.append(0, k, v)
+    q = p.rand_q(g)
+    p.ws.zero_()
+    p.ws[8:16].copy_(torch.tensor([N.KVQ_SELFTEST_WAIT_MAGIC], dtype=torch.int64).view(torch.uint8))
+    out = torch.full((2, 8, 128), float("nan"), device="cuda")
+    K.kvq_decode_attention(p.lib_cfg, p.gpu, 0, q.cuda(), 1.0 / math.sqrt(128), out, p.ws)
+    torch.cuda.synchronize()
+    assert K.kvq_read_status(None, p.ws) == N.KVQ_STATUS_TIMEOUT
+    assert not out.cpu().numpy().any()
+    # the context stays usable: with the header cleared the same decode is correct
+    p.ws[:16].zero_()
+    got, ref = p.decode(0, q)
+    assert_close(got, ref, what="after the self-test")
+    assert p.status() == 0

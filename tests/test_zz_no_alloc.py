@@ -63,11 +63,12 @@ def test_noalloc_matches_workspace_decode_two_calls(scheme):
 
 
 def test_noalloc_rejects_configurations_beyond_its_scratch():
-    # 64 sequences x 8 kv heads of 8192 INT8 tokens (64 row chunks each) need far more
-    # split-context scratch than the fixed 16 MiB: rejected on the host, before any device work
+    # 1024 sequences x 8 kv heads need room for two partial results per (sequence, kv head),
+    # far more split-context scratch than the fixed 16 MiB: rejected on the host, before any
+    # device work
     import quantised_kv_cache_kvq_gb300 as K
     from quantised_kv_cache_kvq_gb300 import _native as N
-    cfg = K.make_config("int8", 1, 64, 32, 8, 128, 8192)
+    cfg = K.make_config("int8", 1, 1024, 32, 8, 128, 8192)
     assert K.kvq_workspace_bytes(cfg) > N.KVQ_NOALLOC_SCRATCH_BYTES
     fake = C.c_void_p(1 << 20)
     rc = K.load().kvq_decode_attention_noalloc(C.byref(cfg), fake, 0, fake, C.c_float(1.0), fake, None)
