@@ -202,7 +202,8 @@ int kvq_flush_group(const kvq_config* cfg, void* cache, int32_t layer, kvq_strea
 /*
  * kvq_workspace_bytes -- device scratch needed by kvq_decode_attention for this
  * configuration: the per-chunk partial softmax results of the split context, plus a
- * 256-byte header holding the decode status word.  The pages define no split of the
+ * 256-byte header holding the decode status word and a 4096-byte table of chunk counters
+ * (bytes 256..4351) that the decode uses and leaves at zero.  The pages define no split of the
  * context: splitting a sequence's tokens into chunks that run in parallel and merging
  * their partial softmax results by log-sum-exp is this library's design for long
  * contexts (the merge is exact: the chunks' partials give the unsplit softmax).  Host
@@ -221,13 +222,16 @@ int kvq_workspace_bytes(const kvq_config* cfg, uint64_t* out_bytes);
  *   cache       device, the cache (read only)
  *   q           device, [batch][q_heads][head_dim] in cfg->in_dtype
  *   out         device fp32, [batch][q_heads][head_dim]; a sequence with no tokens gets 0
- *   workspace   device, at least kvq_workspace_bytes bytes; its first 4 bytes are the
- *               decode status word (sticky; clear it with a memset to restart)
+ *   workspace   device, at least kvq_workspace_bytes bytes, whose first 4352 bytes are
+ *               zero before its first decode (every decode leaves bytes 4..4351 as it
+ *               found them); its first 4 bytes are the decode status word (sticky; clear
+ *               it with a memset to restart)
  * Every cache byte is read once per step for all the query heads that share it.  The
  * context is split into chunks processed in parallel; their partial results are merged
  * by log-sum-exp.  The split follows the token counts held in the cache: one wave of
- * blocks, each taking an equal share of the bytes the step reads.  Calls that overlap on
- * the GPU must not share a workspace.
+ * blocks, each taking an equal share of the bytes the step reads (or, for few long
+ * sequences, taking chunks of its sequence on demand until none is left).  Calls that
+ * overlap on the GPU must not share a workspace.
  * Self-test of the bounded waits: when bytes 8..15 of the workspace hold
  * KVQ_SELFTEST_WAIT_MAGIC (little-endian uint64), every decode block makes its first
  * staging wait on a barrier that nothing completes.  The wait gives up after its limit

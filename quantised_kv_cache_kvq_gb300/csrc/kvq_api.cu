@@ -130,7 +130,8 @@ int make_plan(const Layout& lo, DecodePlan* p) {
     const int64_t units = (int64_t)lo.B * lo.H;
     p->nslot = KVQ_MAX_DECODE_BLOCKS + (2 * units > KVQ_MAX_DECODE_BLOCKS ? 2 * units : KVQ_MAX_DECODE_BLOCKS);
     const int64_t slots = p->nslot * lo.gqa;
-    p->ws_o_off = 256;
+    p->ws_ctr_off = 256;                                    // KVQ_MAX_DECODE_BLOCKS / 2 int32
+    p->ws_o_off = p->ws_ctr_off + 2 * KVQ_MAX_DECODE_BLOCKS;
     p->ws_ml_off = align256(p->ws_o_off + slots * lo.D * 4);
     p->ws_total = align256(p->ws_ml_off + slots * 8);
     p->smem = decode_smem(lo, *p).total;

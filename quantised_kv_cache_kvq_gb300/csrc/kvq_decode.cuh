@@ -341,19 +341,70 @@ __device__ inline UnitPlan unit_plan(const DecodeArgs& a, int64_t* scratch, int2
     return up;
 }
 
-// Calls fn(part, b, h, slot, t0, t1) for every run of chunks of one part of one unit that
-// this block takes, in cost order (whole block, uniform).  The run's partial result goes
-// to slot j + part * B H + unit: unique, because block ranges are contiguous in cost order.
-// fn returns false once the block cannot go on (a bounded wait gave up); the remaining runs
-// then get empty partials via dead(slot).
-template <typename F, typename E>
+// Chunks taken on demand (the unit-aligned split of the KIVI kernels, plan.steal, for a
+// unit with at least 4 packed chunks per block): the k blocks of the unit share its packed
+// chunks through a counter in the workspace instead of a fixed split, so blocks that run
+// faster (or hold no window rows) take more chunks and the unit's blocks finish together.
+// The window's row chunks go, by count, to the last kw = min(nc1, max(k - 1, 1)) blocks,
+// which take them first; each of the other nw = k - kw blocks r starts with the fixed
+// chunks r + s nw (s < NSTAGE), so no block waits on the counter before its first copy;
+// every further chunk is NSTAGE nw + an atomic increment of the unit's counter (the merge
+// sets it back to zero).  on == 0: the chunks of [t0, t1) in order.
+struct StealCtx {
+    int on, r, nw;
+    int* ctr;
+};
+__device__ __forceinline__ bool unit_steals(const DecodePlan& p, int64_t n0, int k) {
+    return p.steal && n0 > (4 * (int64_t)k - 1) * p.CH;   // ceil(n0 / CH) >= 4 k
+}
+__device__ __forceinline__ int window_blocks(const DecodePlan& p, int64_t n1, int k) {
+    const int nc1 = (static_cast<int>(n1) + p.CHR - 1) / p.CHR;
+    return nc1 == 0 ? 0 : min(nc1, max(k - 1, 1));
+}
+
+// Calls fn(part, b, h, slot, t0, t1, steal) for every run of chunks of one part of one
+// unit that this block takes, in cost order (whole block, uniform).  The run's partial
+// result goes to slot j + part * B H + unit: unique, because block ranges are contiguous in
+// cost order (slot 2 j + part in the unit-aligned split).  fn returns false once the block
+// cannot go on (a bounded wait gave up); the remaining runs then get empty partials via
+// dead(slot).  STEAL: the kernel variant that may share a unit's chunks on demand.
+template <bool STEAL, typename F, typename E>
 __device__ void for_each_segment(const DecodeArgs& a, int64_t* scratch, int2* sst, F&& fn, E&& dead) {
     const Layout& lo = a.lo;
     const int64_t units = (int64_t)lo.B * lo.H;
+    StealCtx none;
+    none.on = 0;
+    none.r = none.nw = 0;
+    none.ctr = nullptr;
     if (a.plan.unit_aligned) {
         const UnitPlan up = unit_plan(a, scratch, sst, blockIdx.x);
         grid_launch_dependents();   // the merge may start its own planning; it waits for this grid
         if (up.b >= lo.B) return;
+        if (STEAL && unit_steals(a.plan, up.n0, up.k)) {
+            // slot 2 j + 1 only on the kw window blocks, slot 2 j on every block
+            const int nc1 = (static_cast<int>(up.n1) + a.plan.CHR - 1) / a.plan.CHR;
+            const int kw = window_blocks(a.plan, up.n1, up.k);
+            const int w = up.r - (up.k - kw);
+            const int64_t slot0 = 2 * (int64_t)blockIdx.x, slot1 = slot0 + 1;
+            bool go = true;
+            if (w >= 0) {
+                const int64_t t0 = (int64_t)a.plan.CHR * (nc1 * w / kw);
+                const int64_t t1e = (int64_t)a.plan.CHR * (nc1 * (w + 1) / kw);
+                __syncthreads();
+                go = fn(1, up.b, up.h, slot1, t0, t1e < up.n1 ? t1e : up.n1, none);
+            }
+            StealCtx sc;
+            sc.on = 1;
+            sc.r = up.r;
+            sc.nw = up.k - kw;
+            sc.ctr = reinterpret_cast<int*>(a.ws + a.plan.ws_ctr_off) + (up.b * lo.H + up.h);
+            __syncthreads();   // the window run is done with shared memory
+            if (go && up.n0 > 0)
+                fn(0, up.b, up.h, slot0, 0, up.n0, sc);
+            else
+                dead(slot0);
+            return;
+        }
         const int64_t nc0 = (up.n0 + a.plan.CH - 1) / a.plan.CH, nc1 = (up.n1 + a.plan.CHR - 1) / a.plan.CHR;
         const int64_t N = nc0 + nc1;
         const int64_t clo = N * up.r / up.k, chi = N * (up.r + 1) / up.k;
@@ -371,7 +422,7 @@ __device__ void for_each_segment(const DecodeArgs& a, int64_t* scratch, int2* ss
                     const int64_t t1 = k_hi * gs < nt ? k_hi * gs : nt;
                     __syncthreads();   // the previous run is done with shared memory
                     if (go)
-                        go = fn(part, up.b, up.h, slot, k_lo * gs, t1);
+                        go = fn(part, up.b, up.h, slot, k_lo * gs, t1, none);
                     else
                         dead(slot);
                 }
@@ -411,7 +462,7 @@ __device__ void for_each_segment(const DecodeArgs& a, int64_t* scratch, int2* ss
                     const int64_t t1 = k_hi * gs < nt ? k_hi * gs : nt;
                     __syncthreads();   // the previous run is done with shared memory
                     if (live)
-                        live = fn(part, b, h, slot, k_lo * gs, t1);
+                        live = fn(part, b, h, slot, k_lo * gs, t1, none);
                     else
                         dead(slot);
                 }
@@ -450,6 +501,12 @@ __device__ inline int unit_candidates(const DecodeArgs& a, int u, int2 st, const
         const int64_t U = n0 * a.plan.cpt0 + n1 * a.plan.cpt1;
         const int k = x.C > 0 ? unit_blocks(U, x.C, NB - x.live) : 0;
         const int64_t K = x.K + (int64_t)h * k;
+        if (unit_steals(a.plan, n0, k)) {   // slot 2 j of every block, 2 j + 1 of the window blocks
+            const int kw = window_blocks(a.plan, n1, k);
+            for (int i = tid; i < k + kw; i += nthreads)
+                cand[i] = i < k ? static_cast<int>(2 * (K + i)) : static_cast<int>(2 * (K + k - kw + (i - k)) + 1);
+            return k + kw;
+        }
         const int64_t nc0 = (n0 + a.plan.CH - 1) / a.plan.CH, nc1 = (n1 + a.plan.CHR - 1) / a.plan.CHR;
         const int64_t N = nc0 + nc1;
         for (int i = tid; i < 2 * k; i += nthreads) {
@@ -1042,9 +1099,9 @@ __device__ __forceinline__ uint32_t split_mul(__half2 s, uint32_t x, uint32_t y)
 // largest value scale seen so far times 2^Ev is below 2^15 (lowered, and what was
 // accumulated rescaled by the exact power of two, when a larger scale arrives); the code
 // position p is fixed per accumulator element, so 2^(24 - p) is applied at the end.
-template <int D, int BITS, int NT>
+template <int D, int BITS, int NT, bool STEAL>
 __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64_t slot,
-                                        int64_t t0, int64_t t1, uint32_t phase) {
+                                        int64_t t0, int64_t t1, uint32_t phase, const StealCtx& sc) {
     const SmemOffsets so = decode_smem(a.lo, a.plan);
     constexpr int CPW = 32 / BITS;          // key channels per 32-bit word
     constexpr int HPW = CPW / 2;            // code pairs per word (keys and values)
@@ -1075,20 +1132,43 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
     const int64_t u = unit_index(lo, a.layer, b, h);
     const uint8_t* src_unit = a.cache + lo.data_off + u * lo.unit;
 
-    // the item's groups (t0 and t1 are group boundaries): chunk j holds gpc of them
+    // the item's groups (t0 and t1 are group boundaries): chunk c holds gpc of them
     const int gpc = CH / G;
     const uint8_t* src_groups = src_unit + (t0 / G) * (int64_t)rec;
     const int ngroups = ntok / G;
-    auto issue = [&](int j) {       // stage chunk j (thread 0 only)
-        const int gj = min(gpc, ngroups - j * gpc);
+    auto issue = [&](int c, int sj) {       // stage chunk c into stage sj (thread 0 only)
+        const int gj = min(gpc, ngroups - c * gpc);
         const uint32_t bytes = static_cast<uint32_t>(gj) * rec;
-        const int sj = nstage == 2 ? (j & 1) : 0;   // stage of chunk j
         uint64_t* bar = bars + sj;
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_copy_pieces(smem + so.data + sj * stage_bytes, src_groups + (int64_t)j * gpc * rec, bytes, bar);
+        bulk_copy_pieces(smem + so.data + sj * stage_bytes, src_groups + (int64_t)c * gpc * rec, bytes, bar);
     };
-    if (tid == 0) {
-        for (int j = 0; j < nstage && j < nch; ++j) issue(j);
+    // the chunk each stage holds (-1: none; the chunks come in increasing order, so the
+    // first stage without one ends the item): chunks 0, 1, ... of the run, or (sc.on) the
+    // block's fixed chunks and then counter grabs.  Thread 0 writes an entry before a
+    // block barrier that precedes every read of it.
+    int* chunk_of = reinterpret_cast<int*>(smem + so.hstat);
+    const int dyn0 = nstage * sc.nw;    // chunk of counter value 0
+    int pending = 0;                    // thread 0: the counter value fetched for the next chunk
+    if constexpr (STEAL) {
+        if (tid == 0) {
+            for (int s2 = 0; s2 < nstage; ++s2) {
+                int c;
+                if (!sc.on) {
+                    c = s2;
+                } else if (sc.r < sc.nw) {
+                    c = sc.r + s2 * sc.nw;
+                } else {
+                    c = dyn0 + atomicAdd(sc.ctr, 1);
+                }
+                c = c < nch ? c : -1;
+                chunk_of[s2] = c;
+                if (c >= 0) issue(c, s2);
+            }
+            if (sc.on) pending = atomicAdd(sc.ctr, 1);   // lands while the first chunks run
+        }
+    } else if (tid == 0) {
+        for (int j = 0; j < nstage && j < nch; ++j) issue(j, j);   // chunk j into stage j
     }
     // query prep (whole block) while the copies are in flight: fp32 scaled query, a
     // power-of-two prescale bringing max|q| into [0.5, 1) so fp16 products cannot
@@ -1202,15 +1282,20 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
     // the warp's tokens start W * warp tokens into every chunk: group g0 of the chunk's
     // records, offset ti0 in it (a group may be shared by two warps)
     const int g0 = (warp * W) / G, ti0 = (warp * W) % G;
-    for (int j = 0; j < nch; ++j) {
-        const int sj = nstage == 2 ? (j & 1) : 0;                       // stage of chunk j
+    for (int j = 0; STEAL || j < nch; ++j) {
+        const int sj = nstage == 2 ? (j & 1) : 0;                       // stage of step j
+        int c = j;
+        if constexpr (STEAL) {
+            c = chunk_of[sj];
+            if (c < 0) break;
+        }
         if (!wait_stage(bars, sj, phase, a.ws)) {
             // the next chunk's copy may already be armed on the other stage
-            if (nstage == 2 && j + 1 < nch) drain_stage(bars, sj ^ 1, phase);
+            if (nstage == 2 && (STEAL ? chunk_of[sj ^ 1] >= 0 : j + 1 < nch)) drain_stage(bars, sj ^ 1, phase);
             empty_partial(a, slot);
             return -1;
         }
-        const int ctok = min(ntok - j * CH, CH);
+        const int ctok = min(ntok - c * CH, CH);
         const int wtok = ctok - warp * W < 0 ? 0 : (ctok - warp * W > W ? W : ctok - warp * W);   // multiple of 16
         const uint32_t st0 = sbase + static_cast<uint32_t>(so.data) + sj * stage_bytes + g0 * rec;
         int ngrp = 0;                                  // groups the warp's tokens touch (<= 8)
@@ -1503,8 +1588,20 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
                 default: if constexpr (MTV > 8) pass2(std::integral_constant<int, 4>{}); break;
             }
         }
-        __syncthreads();            // every warp is done with this stage
-        if (tid == 0 && j + nstage < nch) issue(j + nstage);
+        if constexpr (STEAL) {
+            if (tid == 0) {         // this stage's next chunk
+                const int nx = sc.on ? dyn0 + pending : j + nstage;
+                chunk_of[sj] = nx < nch ? nx : -1;
+            }
+            __syncthreads();        // every warp is done with this stage
+            if (tid == 0 && chunk_of[sj] >= 0) {
+                issue(chunk_of[sj], sj);
+                if (sc.on) pending = atomicAdd(sc.ctr, 1);
+            }
+        } else {
+            __syncthreads();        // every warp is done with this stage
+            if (tid == 0 && j + nstage < nch) issue(j + nstage, sj);
+        }
     }
     // ---- warp partial: undo the power-of-two scales, reduce l over the lanes of a head,
     // add the value offset term, combine the 4 warps in shared memory
@@ -1544,8 +1641,9 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
 }
 
 // One wave of blocks; block j takes its share of the layer's chunks (for_each_segment).
-// BITS == 0: no packed part (INT8 rows).
-template <int D, int BITS, int NT>
+// BITS == 0: no packed part (INT8 rows).  STEAL: units may share their packed chunks on
+// demand (a separate instantiation: the extra code slows the kernels that never use it).
+template <int D, int BITS, int NT, bool STEAL>
 __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
     k_decode(const __grid_constant__ DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1559,13 +1657,13 @@ __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
     }
     __syncthreads();
     uint32_t phase = selftest_bits(a);
-    for_each_segment(
+    for_each_segment<STEAL>(
         a, reinterpret_cast<int64_t*>(smem + so.red), reinterpret_cast<int2*>(smem + so.sst),
-        [&](int part, int b, int h, int64_t slot, int64_t t0, int64_t t1) -> bool {
+        [&](int part, int b, int h, int64_t slot, int64_t t0, int64_t t1, const StealCtx& sc) -> bool {
             int r;
             if constexpr (BITS != 0) {
                 if (part == 0)
-                    r = packed_item<D, BITS, NT>(a, smem, b, h, slot, t0, t1, phase);
+                    r = packed_item<D, BITS, NT, STEAL>(a, smem, b, h, slot, t0, t1, phase, sc);
                 else
                     r = window_item<D, NT>(a, smem, b, h, slot, t0, t1, phase);
             } else {
@@ -1579,24 +1677,45 @@ __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
 }
 
 // Launch of a decode kernel over one wave of resident blocks; records the block count in
-// a.plan.NB for the merge.
+// a.plan.NB for the merge.  fn_steal (when not null) is the on-demand variant of fn, used
+// when some unit could get 4 packed chunks per block: when the layer's packed capacity
+// holds 4 NB chunks (a unit of cost U gets about U NB / C blocks and holds U / (CH cpt0)
+// packed chunks, so the ratio is C / (NB CH cpt0) for every unit).
 template <typename K>
-int launch_wave(K fn, DecodeArgs& a, cudaStream_t stream) {
+int launch_wave(K fn, K fn_steal, DecodeArgs& a, cudaStream_t stream) {
     int nb = 0;
     const int rc = decode_blocks(reinterpret_cast<const void*>(fn), kDecodeThreads, a.plan.smem, &nb);
     if (rc != KVQ_OK) return rc;
     a.plan.NB = nb;
     a.plan.inv_nb = 1.0f / nb;
     a.plan.unit_aligned = 2 * (int64_t)a.lo.B * a.lo.H <= nb ? 1 : 0;
-    return launch_dependent(fn, dim3(static_cast<unsigned>(nb)), kDecodeThreads, static_cast<size_t>(a.plan.smem),
+    const int64_t packed_chunks = (int64_t)a.lo.B * a.lo.H * (((int64_t)a.lo.NG * a.lo.G) / a.plan.CH);
+    a.plan.steal = fn_steal && a.plan.unit_aligned && a.lo.scheme == KVQ_SCHEME_KIVI && packed_chunks >= 4 * (int64_t)nb;
+    K run = a.plan.steal ? fn_steal : fn;
+    if (run != fn) {
+        int nb2 = 0;   // same shared memory and register bound: the same wave (checked)
+        if (decode_blocks(reinterpret_cast<const void*>(run), kDecodeThreads, a.plan.smem, &nb2) != KVQ_OK || nb2 != nb) {
+            a.plan.steal = 0;
+            run = fn;
+        }
+    }
+    return launch_dependent(run, dim3(static_cast<unsigned>(nb)), kDecodeThreads, static_cast<size_t>(a.plan.smem),
                             stream, a) == cudaSuccess
                ? KVQ_OK
                : KVQ_ERR_CUDA;
 }
 
+template <typename K>
+int launch_wave(K fn, DecodeArgs& a, cudaStream_t stream) {
+    return launch_wave(fn, static_cast<K>(nullptr), a, stream);
+}
+
 template <int D, int BITS, int NT>
 int launch_decode_t(DecodeArgs& a, cudaStream_t stream) {
-    return launch_wave(k_decode<D, BITS, NT>, a, stream);
+    if constexpr (BITS != 0)
+        return launch_wave(k_decode<D, BITS, NT, false>, k_decode<D, BITS, NT, true>, a, stream);
+    else
+        return launch_wave(k_decode<D, BITS, NT, false>, a, stream);
 }
 
 // Dispatchers, one per translation unit.

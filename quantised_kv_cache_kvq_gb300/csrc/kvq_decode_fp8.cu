@@ -319,9 +319,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
     }
     __syncthreads();
     uint32_t phase = selftest_bits(a);
-    for_each_segment(
+    for_each_segment<false>(
         a, reinterpret_cast<int64_t*>(smem + so.red), reinterpret_cast<int2*>(smem + so.sst),
-        [&](int, int b, int h, int64_t slot, int64_t t0, int64_t t1) -> bool {
+        [&](int, int b, int h, int64_t slot, int64_t t0, int64_t t1, const StealCtx&) -> bool {
             const int r = fp8_item<D, NT, E5M2>(a, smem, b, h, slot, t0, t1, phase);
             if (r < 0) return false;
             phase = static_cast<uint32_t>(r);

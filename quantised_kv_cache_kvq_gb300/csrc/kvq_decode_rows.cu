@@ -78,6 +78,9 @@ __global__ void __launch_bounds__(32 * W) k_merge(const __grid_constant__ Decode
     const int total = unit_candidates(a, u, st, x, cand, NT);
     if (tid == 0) ncand = total;
     grid_dependency_wait();
+    // the decode is complete: its chunk counter of this unit goes back to zero
+    if (a.plan.steal && z == 0 && hh == 0 && tid == 0)
+        reinterpret_cast<int*>(a.ws + a.plan.ws_ctr_off)[u] = 0;
     __syncthreads();
     const int n = ncand;
     const int c0 = 32 * z + lane * CPL;  // this lane's first channel

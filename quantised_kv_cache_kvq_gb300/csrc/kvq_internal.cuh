@@ -71,15 +71,18 @@ __host__ __device__ inline bool is_rows(int scheme) {
 // blocks, one wave of resident blocks; block j takes the chunks whose cost position starts
 // in [ceil(C j / NB), ceil(C (j + 1) / NB)) and leaves, for every part of a unit it
 // touches, one partial softmax result (m, l, o[D]) per query head in workspace slot
-// j + 2 unit + part.  A packed chunk is split among the block's 4 warps, W = CH / 4 tokens
-// (whole groups) each, staged through NSTAGE shared-memory buffers.
+// j + part B H + unit.  With at most half as many units as blocks, units instead get whole
+// blocks (unit_aligned).  A packed chunk is split among the block's 4 warps,
+// W = CH / 4 tokens (whole groups) each, staged through NSTAGE shared-memory buffers.
 struct DecodePlan {
     int CH, W, NSTAGE, CHR, NT;
     int NB;                          // decode blocks of the launch (set by the launcher)
     int unit_aligned;                // 1: every unit gets whole blocks (set by the launcher)
+    int steal;                       // 1: those blocks share the unit's packed chunks on demand
     int64_t cpt0, cpt1;              // scheduling cost of a packed token and of a row token
     float inv_nb, inv_cc0, inv_cc1;  // 1 / NB and 1 / (chunk cost) of each part
     int64_t nslot;                   // partial-result slots the workspace holds
+    int64_t ws_ctr_off;              // per-unit chunk counters (zero between decodes)
     int64_t ws_o_off, ws_ml_off, ws_total;   // partial o, partial (m, l)
     int64_t smem;
 };
