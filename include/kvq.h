@@ -96,7 +96,9 @@ enum kvq_status_bits {
     KVQ_STATUS_CAPACITY = 1u,  /* an append would exceed max_tokens: that sequence was skipped */
     KVQ_STATUS_RING_FULL = 2u, /* KIVI no-autoflush append would overflow the window: skipped */
     KVQ_STATUS_NONFINITE = 4u, /* a NaN or infinity reached a quantiser (values still stored) */
-    KVQ_STATUS_TIMEOUT = 8u    /* a bounded wait for an asynchronous copy gave up: output invalid */
+    KVQ_STATUS_TIMEOUT = 8u,   /* a bounded wait for an asynchronous copy gave up: output invalid */
+    KVQ_STATUS_BAD_PAGE = 16u  /* a block-table entry outside the page pool: appends and flushes
+                                  left that sequence unchanged, a decode's output is invalid */
 };
 
 /*
@@ -117,6 +119,24 @@ enum kvq_status_bits {
  *   residual    KIVI R: newest tokens kept in the bf16 window (>= 0)
  *   max_tokens  per-sequence capacity in tokens (>= 1)
  *   in_dtype    kvq_dtype of keys, values and queries (KIVI: bf16 only)
+ *   page_groups KIVI paged layout: group records per page; 0 for the contiguous layout
+ *               (the other schemes: 0 only)
+ *   num_pages   paged layout: pages in the cache's pool (>= 1)
+ *   block_table paged layout, device int32 [batch][max_pages], max_pages = ceil(NG /
+ *               page_groups) with NG = floor((max_tokens - residual) / group_k) group slots
+ *               per sequence: the pool page holding each run of page_groups group slots of
+ *               each sequence.  Read by every call that reads or writes group records
+ *               (appends, flushes, decodes), so the caller may hand a sequence new pages
+ *               between calls; unused for the contiguous layout.
+ * Paged layout ("KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache", "Key
+ * Takeaways for Interviews": KIVI pairs with PagedAttention, whose fixed-size pages are
+ * found through a per-sequence block table): the packed group records live in a pool of
+ * num_pages pages instead of one fixed region per (layer, sequence, KV head).  A page holds
+ * page_groups consecutive group slots of one sequence for every layer and KV head; group
+ * slot g of sequence b is in page block_table[b][g / page_groups].  The bf16 window, the
+ * token counts and the header stay where they are.  A table entry outside [0, num_pages)
+ * sets KVQ_STATUS_BAD_PAGE: an append or flush that would write through it leaves that
+ * sequence unchanged; a decode reads page 0 instead (its output is then invalid).
  */
 typedef struct kvq_config {
     int32_t scheme;
@@ -131,6 +151,9 @@ typedef struct kvq_config {
     int32_t residual;
     int32_t max_tokens;
     int32_t in_dtype;
+    int32_t page_groups;
+    int32_t num_pages;
+    const int32_t* block_table;
 } kvq_config;
 
 /*

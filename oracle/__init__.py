@@ -19,14 +19,15 @@ _lib = None
 
 SCHEME_KIVI, SCHEME_INT8, SCHEME_FP8, SCHEME_FP8_E5M2, SCHEME_INT4 = 0, 1, 2, 3, 4
 DT_BF16, DT_F32 = 0, 1
-ST_CAPACITY, ST_RING_FULL, ST_NONFINITE = 1, 2, 4
+ST_CAPACITY, ST_RING_FULL, ST_NONFINITE, ST_BAD_PAGE = 1, 2, 4, 16
 FLAG_NO_AUTOFLUSH = 1
 
 
 class OracleConfig(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "scheme", "layers", "batch", "q_heads", "kv_heads", "head_dim", "bits",
-        "group_k", "group_v", "residual", "max_tokens", "in_dtype")]
+        "group_k", "group_v", "residual", "max_tokens", "in_dtype", "page_groups", "num_pages")] + [
+        ("block_table", C.c_void_p)]
 
 
 def lib():
@@ -51,6 +52,7 @@ def lib():
             "kvqo_int8_token": (None, [P, C.c_int, P, P]),
             "kvqo_image_bytes": (i64, [P]),
             "kvqo_image_regions": (None, [P, P]),
+            "kvqo_record_offset": (i64, [P, C.c_int, C.c_int, C.c_int, i64]),
             "kvqo_image_init": (None, [P, P]),
             "kvqo_append": (u32, [P, P, C.c_int, C.c_int, C.c_int, P, P, C.c_int, P, P, u32]),
             "kvqo_flush": (None, [P, P, C.c_int]),
@@ -139,14 +141,28 @@ def int8_token(x):
 
 
 # ----------------------------------------------------------------------------- the cache image
-def make_config(**kw):
+def make_config(block_table=None, **kw):
+    """block_table (paged KIVI layout): int32 [batch][max_pages], kept alive on the config."""
     c = OracleConfig()
     defaults = dict(scheme=0, layers=1, batch=1, q_heads=1, kv_heads=1, head_dim=64, bits=2,
-                    group_k=32, group_v=32, residual=0, max_tokens=64, in_dtype=DT_BF16)
+                    group_k=32, group_v=32, residual=0, max_tokens=64, in_dtype=DT_BF16, page_groups=0,
+                    num_pages=0)
     defaults.update(kw)
     for k, v in defaults.items():
         setattr(c, k, int(v))
+    set_block_table(c, block_table)
     return c
+
+
+def set_block_table(cfg, table):
+    """Point the config at a (new) block table: int32 [batch][max_pages] or None."""
+    cfg._table = None if table is None else np.ascontiguousarray(table, dtype=np.int32)
+    cfg.block_table = None if cfg._table is None else cfg._table.ctypes.data
+
+
+def record_offset(cfg, layer, seq, kv_head, group):
+    """Byte offset of a KIVI group record in the image (either layout)."""
+    return int(lib().kvqo_record_offset(C.byref(cfg), layer, seq, kv_head, group))
 
 
 class Image:

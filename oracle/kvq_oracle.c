@@ -49,11 +49,14 @@ typedef struct {
     int32_t residual;   /* KIVI: R, newest tokens kept in full precision */
     int32_t max_tokens; /* per-sequence capacity T */
     int32_t in_dtype;   /* 0 = bf16, 1 = fp32 (inputs K, V and q) */
+    int32_t page_groups;          /* KIVI paged layout: group records per page (0: none) */
+    int32_t num_pages;            /* pages in the pool */
+    const int32_t* block_table;   /* [batch][max_pages]: pool page of each page of a sequence */
 } kvqo_config;
 
 enum { SCHEME_KIVI = 0, SCHEME_INT8 = 1, SCHEME_FP8 = 2, SCHEME_FP8_E5M2 = 3, SCHEME_INT4 = 4 };
 enum { DT_BF16 = 0, DT_F32 = 1 };
-enum { ST_CAPACITY = 1u, ST_RING_FULL = 2u, ST_NONFINITE = 4u };
+enum { ST_CAPACITY = 1u, ST_RING_FULL = 2u, ST_NONFINITE = 4u, ST_BAD_PAGE = 16u };
 enum { FLAG_NO_AUTOFLUSH = 1u };
 
 /* ------------------------------------------------------------------------------------
@@ -337,7 +340,9 @@ void kvqo_int4_token(const float* x, int n, float* scale_out, int8_t* codes)
  *   state: for (layer l, sequence b): int32 n (tokens cached), int32 qn (tokens held in
  *          packed groups; n for INT8/FP8), then two reserved int32 that are zero whenever
  *          no call is running, at byte 16 * (l * batch + b).
- *   KIVI:  group records, one per (l, b, kv head h, group slot g), NG = (T - R) / G slots:
+ *   KIVI:  group records, one per (l, b, kv head h, group slot g), NG = (T - R) / G slots
+ *          (contiguous layout: record (l, b, h, g) at ((l * batch + b) * kv_heads + h) * NG
+ *          + g; paged layout, below: through the sequence's block table):
  *            K codes  G*D*b/8 bytes, token-major: (token t, channel c) at bit (t*D + c)*b
  *            V codes  D*G*b/8 bytes of 32-bit words, 2*D*b bytes per 16-token tile, in
  *                     the order of vcode_bit (a word's halves hold tokens tt and tt + 8
@@ -356,11 +361,23 @@ void kvqo_int4_token(const float* x, int n, float* scale_out, int8_t* codes)
  *            K codes e4m3 [T16][D], each row in the channel order of fp8_kbyte
  *            V codes e4m3 [T16 / 16 tiles][D][16 tokens], tokens in the order of fp8_vbyte
  * Bits are numbered LSB-first within a byte: bit i is bit (i mod 8) of byte i / 8.
+ *
+ * Paged KIVI layout ("KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache",
+ * "Key Takeaways for Interviews": it pairs with PagedAttention, whose pages hold the cache
+ * of a run of tokens of one sequence and are found through a per-sequence block table).
+ * The group-record region is a pool of num_pages pages; a page holds page_groups (PG)
+ * consecutive group slots of one sequence for every layer and kv head, ordered (l, h,
+ * slot): record (l, b, h, g) sits in pool page P = block_table[b * MP + g / PG] (MP =
+ * ceil(NG / PG) entries per sequence) at record index (l * kv_heads + h) * PG + g mod PG.
+ * Only the group records move; the header, the counts and the bf16 ring are as above.
+ * A block-table entry outside [0, num_pages) is an error: an append or flush that would
+ * write through it leaves the sequence unchanged and sets status bit 16.
  * ---------------------------------------------------------------------------------- */
 typedef struct {
     int64_t header, state, scales, data, ring, total;  /* byte offsets of the regions */
     int64_t unit;           /* bytes of one (l, b, h) block in the data region */
     int64_t rec, kc, vc, kp, vp, ng, cap, ngv, t16;
+    int64_t pg, mp, page;   /* paged: group slots per page, table entries per sequence, page bytes */
 } layout_t;
 
 static int64_t up256(int64_t x) { return (x + 255) / 256 * 256; }
@@ -437,7 +454,14 @@ static layout_t make_layout(const kvqo_config* c)
         L.rec = L.kc + L.vc + L.kp + L.vp;
         L.unit = L.ng * L.rec;
         L.data = pos;
-        pos += up256(units * L.unit);
+        if (c->page_groups > 0) {
+            L.pg = c->page_groups;
+            L.mp = (L.ng + L.pg - 1) / L.pg;
+            L.page = (int64_t)c->layers * c->kv_heads * L.pg * L.rec;
+            pos += up256((int64_t)c->num_pages * L.page);
+        } else {
+            pos += up256(units * L.unit);
+        }
         L.ring = pos;
         pos += up256(units * L.cap * 4 * D);
     } else if (c->scheme == SCHEME_INT8) {
@@ -483,6 +507,50 @@ static uint8_t* unit_base(const kvqo_config* c, const layout_t* L, uint8_t* img,
 {
     int64_t u = ((int64_t)l * c->batch + b) * c->kv_heads + h;
     return img + L->data + u * L->unit;
+}
+
+/* Pool page of group slot g of sequence b (paged layout), -1 when the block table names no
+ * page of the pool. */
+static int64_t page_of(const kvqo_config* c, const layout_t* L, int b, int64_t g)
+{
+    int64_t p = c->block_table[(int64_t)b * L->mp + g / L->pg];
+    return (p >= 0 && p < c->num_pages) ? p : -1;
+}
+
+/* Byte offset of the record of KIVI group slot g of (l, b, h), in either layout.  A paged
+ * slot whose table entry is out of range reads page 0 (decoding then reports nothing: the
+ * append and flush rules keep such slots from being written). */
+static int64_t record_offset(const kvqo_config* c, const layout_t* L, int l, int b, int h, int64_t g)
+{
+    if (c->page_groups <= 0) {
+        int64_t u = ((int64_t)l * c->batch + b) * c->kv_heads + h;
+        return L->data + u * L->unit + g * L->rec;
+    }
+    int64_t p = page_of(c, L, b, g);
+    if (p < 0) p = 0;
+    return L->data + p * L->page + (((int64_t)l * c->kv_heads + h) * L->pg + g % L->pg) * L->rec;
+}
+
+static uint8_t* group_record(const kvqo_config* c, const layout_t* L, uint8_t* img, int l, int b, int h,
+                             int64_t g)
+{
+    return img + record_offset(c, L, l, b, h, g);
+}
+
+/* 1 when every group slot in [g0, g1) of sequence b has a page (always, unpaged). */
+static int pages_ok(const kvqo_config* c, const layout_t* L, int b, int64_t g0, int64_t g1)
+{
+    if (c->page_groups <= 0) return 1;
+    for (int64_t g = g0; g < g1; g++)
+        if (page_of(c, L, b, g) < 0) return 0;
+    return 1;
+}
+
+/* byte offset of the record of (l, b, h, g), for tests that look inside the image */
+int64_t kvqo_record_offset(const kvqo_config* c, int l, int b, int h, int64_t g)
+{
+    layout_t L = make_layout(c);
+    return record_offset(c, &L, l, b, h, g);
 }
 
 static void put_bits(uint8_t* base, int64_t bit, int bits, int code)
@@ -556,7 +624,7 @@ static void kivi_quantise_group(const kvqo_config* c, const layout_t* L, uint8_t
         }
     }
     int64_t g = t0 / G;
-    uint8_t* rec = unit_base(c, L, img, l, b, h) + g * L->rec;
+    uint8_t* rec = group_record(c, L, img, l, b, h, g);
     uint8_t* kcodes = rec;
     uint8_t* vcodes = rec + L->kc;
     uint8_t* kpar = rec + L->kc + L->vc;
@@ -629,6 +697,12 @@ uint32_t kvqo_append(const kvqo_config* c, uint8_t* img, int l, int seq_begin, i
         if (c->scheme == SCHEME_KIVI && (flags & FLAG_NO_AUTOFLUSH) && n + m - qn > L.cap) {
             st |= ST_RING_FULL;
             continue;
+        }
+        if (c->scheme == SCHEME_KIVI && !(flags & FLAG_NO_AUTOFLUSH)) {
+            /* the groups this append packs must all have pages */
+            int64_t G = c->group_k, over = n + m - qn - c->residual;
+            int64_t qn2 = over >= G ? qn + G * (over / G) : qn;
+            if (!pages_ok(c, &L, b, qn / G, qn2 / G)) { st |= ST_BAD_PAGE; continue; }
         }
         /* non-finite inputs are flagged; the values are still stored */
         for (int h = 0; h < H; h++)
@@ -735,6 +809,11 @@ void kvqo_flush(const kvqo_config* c, uint8_t* img, int l)
     for (int b = 0; b < c->batch; b++) {
         int32_t* s = state_of(c, img, l, b);
         int64_t n = s[0], qn = s[1];
+        int64_t ready = n - qn - c->residual >= c->group_k ? (n - qn - c->residual) / c->group_k : 0;
+        if (!pages_ok(c, &L, b, qn / c->group_k, qn / c->group_k + ready)) {
+            *(uint32_t*)img |= ST_BAD_PAGE;   /* the sequence's window stays as it is */
+            continue;
+        }
         while (n - qn >= (int64_t)c->residual + c->group_k) {
             for (int h = 0; h < c->kv_heads; h++)
                 kivi_quantise_group(c, &L, img, l, b, h, qn, n, NULL, NULL, 0, 0);
@@ -757,7 +836,7 @@ void kvqo_dequant_token(const kvqo_config* c, const uint8_t* img, int l, int b, 
     if (c->scheme == SCHEME_KIVI) {
         int G = c->group_k, Gv = c->group_v, bits = c->bits;
         if (t < qn) {
-            const uint8_t* rec = base + (t / G) * L.rec;
+            const uint8_t* rec = group_record(c, &L, (uint8_t*)img, l, b, h, t / G);
             const uint8_t* kpar = rec + L.kc + L.vc;
             const uint8_t* vpar = kpar + L.kp;
             int i = (int)(t % G);

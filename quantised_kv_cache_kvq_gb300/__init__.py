@@ -11,7 +11,7 @@ from ._native import (  # noqa: F401
     EXPORTS, KVQ_BYTES_FORMULA, KVQ_BYTES_LAYOUT, KVQ_DTYPE_BF16, KVQ_DTYPE_F32,
     KVQ_NO_AUTOFLUSH, KVQ_SCHEME_FP8_E4M3, KVQ_SCHEME_FP8_E5M2, KVQ_SCHEME_INT4, KVQ_SCHEME_INT8,
     KVQ_SCHEME_KIVI,
-    KVQ_STATUS_CAPACITY, KVQ_STATUS_NONFINITE, KVQ_STATUS_RING_FULL, KVQ_STATUS_TIMEOUT,
+    KVQ_STATUS_BAD_PAGE, KVQ_STATUS_CAPACITY, KVQ_STATUS_NONFINITE, KVQ_STATUS_RING_FULL, KVQ_STATUS_TIMEOUT,
     KvqConfig, KvqError, kvq_cache_bytes, kvq_cache_init, kvq_decode_attention,
     kvq_decode_attention_noalloc,
     kvq_flush_group, kvq_quantize_append, kvq_read_status, kvq_sequence_lengths,
@@ -23,7 +23,9 @@ _SCHEMES = {"kivi": KVQ_SCHEME_KIVI, "int8": KVQ_SCHEME_INT8, "fp8": KVQ_SCHEME_
 
 
 def make_config(scheme, layers, batch, q_heads, kv_heads, head_dim, max_tokens, bits=None,
-                group_k=32, group_v=32, residual=0, in_dtype="bf16") -> KvqConfig:
+                group_k=32, group_v=32, residual=0, in_dtype="bf16", page_groups=0, num_pages=0,
+                block_table=None) -> KvqConfig:
+    """block_table: paged KIVI layout, a device int32 tensor [batch][max_pages]."""
     s = _SCHEMES[scheme] if isinstance(scheme, str) else int(scheme)
     if bits is None:
         bits = {KVQ_SCHEME_KIVI: 2, KVQ_SCHEME_INT4: 4}.get(s, 8)
@@ -32,7 +34,15 @@ def make_config(scheme, layers, batch, q_heads, kv_heads, head_dim, max_tokens, 
     c.head_dim, c.bits, c.group_k, c.group_v, c.residual = head_dim, bits, group_k, group_v, residual
     c.max_tokens = max_tokens
     c.in_dtype = KVQ_DTYPE_BF16 if in_dtype in ("bf16", KVQ_DTYPE_BF16) else KVQ_DTYPE_F32
+    c.page_groups, c.num_pages = page_groups, num_pages
+    c.set_block_table(block_table)
     return c
+
+
+def max_pages(cfg) -> int:
+    """Block-table entries per sequence of a paged configuration."""
+    ng = (cfg.max_tokens - cfg.residual) // cfg.group_k if cfg.max_tokens > cfg.residual else 0
+    return (ng + cfg.page_groups - 1) // cfg.page_groups if cfg.page_groups > 0 else 0
 
 
 class QuantizedKVCache:

@@ -13,6 +13,7 @@ KVQ_NO_AUTOFLUSH = 1
 KVQ_OK, KVQ_ERR_ARG, KVQ_ERR_ALIGN, KVQ_ERR_CAPACITY = 0, -1, -2, -3
 KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA, KVQ_ERR_UNSUPPORTED = -4, -5, -6
 KVQ_STATUS_CAPACITY, KVQ_STATUS_RING_FULL, KVQ_STATUS_NONFINITE, KVQ_STATUS_TIMEOUT = 1, 2, 4, 8
+KVQ_STATUS_BAD_PAGE = 16
 
 # every symbol include/kvq.h declares
 EXPORTS = (
@@ -29,10 +30,17 @@ class KvqConfig(C.Structure):
     """struct kvq_config"""
     _fields_ = [(n, C.c_int32) for n in (
         "scheme", "layers", "batch", "q_heads", "kv_heads", "head_dim", "bits", "group_k",
-        "group_v", "residual", "max_tokens", "in_dtype")]
+        "group_v", "residual", "max_tokens", "in_dtype", "page_groups", "num_pages")] + [
+        ("block_table", C.c_void_p)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
+
+    def set_block_table(self, table):
+        """Paged layout: point the configuration at a device int32 [batch][max_pages] tensor
+        (kept alive here) or None."""
+        self._table = table
+        self.block_table = None if table is None else int(table.data_ptr())
 
 
 class KvqError(RuntimeError):

@@ -26,6 +26,15 @@ UNITS = {
     "kvq_decode_kivi2.cu": [],
     "kvq_decode_kivi4.cu": [],
     "kvq_decode_kivi8.cu": [],
+    "kvq_decode_kivi2_steal.cu": [],
+    "kvq_decode_kivi4_steal.cu": [],
+    "kvq_decode_kivi8_steal.cu": [],
+    "kvq_decode_kivi2_paged.cu": [],
+    "kvq_decode_kivi4_paged.cu": [],
+    "kvq_decode_kivi8_paged.cu": [],
+    "kvq_decode_kivi2_paged_steal.cu": [],
+    "kvq_decode_kivi4_paged_steal.cu": [],
+    "kvq_decode_kivi8_paged_steal.cu": [],
     "kvq_decode_rows.cu": [],
     "kvq_decode_fp8.cu": [],
     "kvq_noalloc.cu": [],

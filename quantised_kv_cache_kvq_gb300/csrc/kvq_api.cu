@@ -21,6 +21,7 @@ int make_layout(const kvq_config* c, int64_t max_tokens, Layout* out) {
     if (c->q_heads % c->kv_heads != 0) return KVQ_ERR_ARG;
     if (max_tokens < 1 || max_tokens > (int64_t)1 << 30) return KVQ_ERR_ARG;
     if (c->in_dtype != KVQ_DTYPE_BF16 && c->in_dtype != KVQ_DTYPE_F32) return KVQ_ERR_ARG;
+    if (c->page_groups < 0 || c->num_pages < 0) return KVQ_ERR_ARG;
     const int gqa = c->q_heads / c->kv_heads;
     if (gqa != 1 && gqa != 2 && gqa != 4 && gqa != 8) return KVQ_ERR_UNSUPPORTED;
     const int D = c->head_dim;
@@ -58,10 +59,21 @@ int make_layout(const kvq_config* c, int64_t max_tokens, Layout* out) {
         lo.rec = lo.kc + lo.vc + lo.kp + lo.vp;
         lo.unit = (int64_t)lo.NG * lo.rec;
         lo.data_off = pos;
-        pos += align256(units * lo.unit);
+        if (c->page_groups > 0) {
+            if (c->num_pages < 1) return KVQ_ERR_ARG;
+            lo.PG = c->page_groups;
+            lo.NP = c->num_pages;
+            lo.MP = (lo.NG + lo.PG - 1) / lo.PG;
+            lo.page = (int64_t)lo.L * lo.H * lo.PG * lo.rec;
+            lo.table = c->block_table;
+            pos += align256((int64_t)lo.NP * lo.page);
+        } else {
+            pos += align256(units * lo.unit);
+        }
         lo.ring_off = pos;
         pos += align256(units * lo.C * 4 * (int64_t)D);
     } else {
+        if (c->page_groups > 0) return KVQ_ERR_UNSUPPORTED;   // pages hold KIVI group records
         if (!pow2_in(D, 32, 256)) return KVQ_ERR_UNSUPPORTED;
         if (is_rows(c->scheme)) {
             lo.unit = (int64_t)lo.T16 * ((c->scheme == KVQ_SCHEME_INT8 ? 2 * D : D) + 8);
@@ -273,8 +285,10 @@ int kvq_quantize_append(const kvq_config* cfg, void* cache, int32_t layer, int32
     if (seq_count == 0 || n_new == 0) return KVQ_OK;
     if (!k_new || !v_new) return KVQ_ERR_ARG;
     if (kvq::is_fp8(lo.scheme) && !fp8_scales) return KVQ_ERR_ARG;
+    if (lo.PG > 0 && !lo.table) return KVQ_ERR_ARG;
     if (!aligned(cache, 256) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
-        (n_valid && !aligned(n_valid, 4)) || (fp8_scales && !aligned(fp8_scales, 4)))
+        (n_valid && !aligned(n_valid, 4)) || (fp8_scales && !aligned(fp8_scales, 4)) ||
+        (lo.table && !aligned(lo.table, 4)))
         return KVQ_ERR_ALIGN;
     return kvq::launch_append(lo, static_cast<uint8_t*>(cache), layer, seq_begin, seq_count, k_new, v_new,
                               n_new, n_valid, fp8_scales, flags, reinterpret_cast<cudaStream_t>(stream));
@@ -286,7 +300,8 @@ int kvq_flush_group(const kvq_config* cfg, void* cache, int32_t layer, kvq_strea
     int rc = kvq::make_layout(cfg, cfg->max_tokens, &lo);
     if (rc != KVQ_OK) return rc;
     if (layer < 0 || layer >= lo.L) return KVQ_ERR_ARG;
-    if (!aligned(cache, 256)) return KVQ_ERR_ALIGN;
+    if (lo.PG > 0 && !lo.table) return KVQ_ERR_ARG;
+    if (!aligned(cache, 256) || (lo.table && !aligned(lo.table, 4))) return KVQ_ERR_ALIGN;
     return kvq::launch_flush(lo, static_cast<uint8_t*>(cache), layer, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -314,7 +329,9 @@ int kvq_decode_attention(const kvq_config* cfg, const void* cache, int32_t layer
     rc = kvq::make_plan(lo, &plan);
     if (rc != KVQ_OK) return rc;
     if (workspace_bytes < static_cast<uint64_t>(plan.ws_total)) return KVQ_ERR_WORKSPACE;
-    if (!aligned(cache, 256) || !aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 256))
+    if (lo.PG > 0 && !lo.table) return KVQ_ERR_ARG;
+    if (!aligned(cache, 256) || !aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 256) ||
+        (lo.table && !aligned(lo.table, 4)))
         return KVQ_ERR_ALIGN;
     return kvq::launch_decode(lo, plan, static_cast<const uint8_t*>(cache), layer, q, softmax_scale, out,
                               static_cast<uint8_t*>(workspace), reinterpret_cast<cudaStream_t>(stream));

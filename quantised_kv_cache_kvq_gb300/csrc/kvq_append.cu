@@ -40,7 +40,15 @@ __device__ __forceinline__ int64_t input_row(const Layout& lo, int n_new, int bi
 
 // Tokens a sequence takes in this append, or -1 when it is skipped (capacity or a full
 // window); sets the matching status bit in *st.
-__device__ __forceinline__ int tokens_taken(const Layout& lo, int n, int qn, int m, uint32_t flags,
+// qn after taking m tokens (the window is flushed while it would hold >= R + G tokens).
+__device__ __forceinline__ int qn_after(const Layout& lo, int n, int qn, int m, uint32_t flags) {
+    if (lo.scheme != KVQ_SCHEME_KIVI) return n + m;
+    if (flags & KVQ_NO_AUTOFLUSH) return qn;
+    int over = n + m - qn - lo.R;
+    return over >= lo.G ? qn + lo.G * (over / lo.G) : qn;
+}
+
+__device__ __forceinline__ int tokens_taken(const Layout& lo, int b, int n, int qn, int m, uint32_t flags,
                                             uint32_t* st) {
     if ((int64_t)n + m > lo.T) {
         *st |= KVQ_STATUS_CAPACITY;
@@ -50,15 +58,12 @@ __device__ __forceinline__ int tokens_taken(const Layout& lo, int n, int qn, int
         *st |= KVQ_STATUS_RING_FULL;
         return -1;
     }
+    // paged layout: every group this append packs needs a page of the pool
+    if (lo.PG > 0 && !pages_ok(lo, b, qn / lo.G, qn_after(lo, n, qn, m, flags) / lo.G)) {
+        *st |= KVQ_STATUS_BAD_PAGE;
+        return -1;
+    }
     return m;
-}
-
-// qn after taking m tokens (the window is flushed while it would hold >= R + G tokens).
-__device__ __forceinline__ int qn_after(const Layout& lo, int n, int qn, int m, uint32_t flags) {
-    if (lo.scheme != KVQ_SCHEME_KIVI) return n + m;
-    if (flags & KVQ_NO_AUTOFLUSH) return qn;
-    int over = n + m - qn - lo.R;
-    return over >= lo.G ? qn + lo.G * (over / lo.G) : qn;
 }
 
 // Q_b parameters of one group: offset = min rounded down to binary16, scale = (max -
@@ -104,8 +109,8 @@ __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int 
     const int D = lo.D, G = lo.G, Gv = lo.Gv, bits = lo.bits;
     const int levels = (1 << bits) - 1;
     const float flevels = static_cast<float>(levels);
-    const int64_t u = unit_index(lo, l, b, h);
-    uint8_t* rec = cache + lo.data_off + u * lo.unit + (t0 / G) * (int64_t)lo.rec;
+    // (a paged record's page was checked by the caller's admission rule)
+    uint8_t* rec = cache + group_offset(lo, l, b, h, t0 / G);
     __half* kpar = reinterpret_cast<__half*>(rec + lo.kc + lo.vc);
     __half* vpar = reinterpret_cast<__half*>(rec + lo.kc + lo.vc + lo.kp);
     uint16_t* ks = reinterpret_cast<uint16_t*>(smem);
@@ -400,7 +405,7 @@ __global__ void __launch_bounds__(kThreads) k_append_small(AppendArgs a) {
     uint32_t status = 0;
     int m = new_tokens(a, bi);
     m = m < 0 ? 0 : (m > a.n_new ? a.n_new : m);
-    if (tokens_taken(lo, n, qn, m, a.flags, &status) < 0) {
+    if (tokens_taken(lo, b, n, qn, m, a.flags, &status) < 0) {
         if (threadIdx.x == 0 && h == 0) atomicOr(reinterpret_cast<uint32_t*>(a.cache), status);
         return;
     }
@@ -454,7 +459,7 @@ __global__ void __launch_bounds__(kThreads) k_append_groups(AppendArgs a) {
     uint32_t dummy = 0;
     int m = new_tokens(a, bi);
     m = m < 0 ? 0 : (m > a.n_new ? a.n_new : m);
-    if (tokens_taken(lo, n, qn, m, a.flags, &dummy) < 0) return;
+    if (tokens_taken(lo, b, n, qn, m, a.flags, &dummy) < 0) return;
     const int qn2 = qn_after(lo, n, qn, m, a.flags);
     const int64_t t0 = qn + (int64_t)blockIdx.x * lo.G;
     if (t0 >= qn2) return;
@@ -480,7 +485,7 @@ __global__ void __launch_bounds__(kThreads) k_append_rows(AppendArgs a) {
     uint32_t dummy = 0;
     int m = new_tokens(a, bi);
     m = m < 0 ? 0 : (m > a.n_new ? a.n_new : m);
-    if (tokens_taken(lo, n, qn, m, a.flags, &dummy) < 0) return;
+    if (tokens_taken(lo, b, n, qn, m, a.flags, &dummy) < 0) return;
     const int lane = threadIdx.x & 31;
     const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     uint32_t bad = 0;
@@ -517,7 +522,7 @@ __global__ void k_append_commit(AppendArgs a) {
         const int n = st[0], qn = st[1];
         int m = new_tokens(a, bi);
         m = m < 0 ? 0 : (m > a.n_new ? a.n_new : m);
-        if (tokens_taken(lo, n, qn, m, a.flags, &status) >= 0) {
+        if (tokens_taken(lo, b, n, qn, m, a.flags, &status) >= 0) {
             st[1] = qn_after(lo, n, qn, m, a.flags);
             st[0] = n + m;
         }
@@ -534,6 +539,7 @@ __global__ void __launch_bounds__(kThreads) k_flush_groups(Layout lo, uint8_t* c
     const int n = st[0], qn = st[1];
     const int ready = (n - qn - lo.R) >= lo.G ? (n - qn - lo.R) / lo.G : 0;
     if (static_cast<int>(blockIdx.x) >= ready) return;
+    if (!pages_ok(lo, b, qn / lo.G, qn / lo.G + ready)) return;   // k_flush_commit reports it
     TokenSource s;
     s.ring_unit = cache + lo.ring_off + unit_index(lo, layer, b, h) * lo.C * (int64_t)(4 * lo.D);
     s.k_new = nullptr;
@@ -552,6 +558,10 @@ __global__ void k_flush_commit(Layout lo, uint8_t* cache, int layer) {
     int32_t* st = state_ptr(lo, cache, layer, b);
     const int n = st[0], qn = st[1];
     const int ready = (n - qn - lo.R) >= lo.G ? (n - qn - lo.R) / lo.G : 0;
+    if (!pages_ok(lo, b, qn / lo.G, qn / lo.G + ready)) {   // the window stays as it is
+        atomicOr(reinterpret_cast<uint32_t*>(cache), KVQ_STATUS_BAD_PAGE);
+        return;
+    }
     st[1] = qn + ready * lo.G;
 }
 

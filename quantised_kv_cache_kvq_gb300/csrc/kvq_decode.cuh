@@ -1099,7 +1099,7 @@ __device__ __forceinline__ uint32_t split_mul(__half2 s, uint32_t x, uint32_t y)
 // largest value scale seen so far times 2^Ev is below 2^15 (lowered, and what was
 // accumulated rescaled by the exact power of two, when a larger scale arrives); the code
 // position p is fixed per accumulator element, so 2^(24 - p) is applied at the end.
-template <int D, int BITS, int NT, bool STEAL>
+template <int D, int BITS, int NT, bool STEAL, bool PAGED>
 __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64_t slot,
                                         int64_t t0, int64_t t1, uint32_t phase, const StealCtx& sc) {
     const SmemOffsets so = decode_smem(a.lo, a.plan);
@@ -1140,8 +1140,25 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
         const int gj = min(gpc, ngroups - c * gpc);
         const uint32_t bytes = static_cast<uint32_t>(gj) * rec;
         uint64_t* bar = bars + sj;
+        uint8_t* dst = smem + so.data + sj * stage_bytes;
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_copy_pieces(smem + so.data + sj * stage_bytes, src_groups + (int64_t)c * gpc * rec, bytes, bar);
+        if constexpr (!PAGED) {
+            bulk_copy_pieces(dst, src_groups + (int64_t)c * gpc * rec, bytes, bar);
+        } else {
+            // paged layout: one copy per run of the chunk's groups that shares a page
+            int g = static_cast<int>(t0 / G) + c * gpc;
+            for (int x = 0; x < gj;) {
+                const int run = min(lo.PG - g % lo.PG, gj - x);
+                int64_t off = group_offset(lo, a.layer, b, h, g);
+                if (off < 0) {   // a table entry outside the pool: read page 0, report it
+                    atomicOr(reinterpret_cast<uint32_t*>(a.ws), KVQ_STATUS_BAD_PAGE);
+                    off = lo.data_off + (((int64_t)a.layer * lo.H + h) * lo.PG + g % lo.PG) * rec;
+                }
+                bulk_copy_pieces(dst + (int64_t)x * rec, a.cache + off, static_cast<uint32_t>(run) * rec, bar);
+                x += run;
+                g += run;
+            }
+        }
     };
     // the chunk each stage holds (-1: none; the chunks come in increasing order, so the
     // first stage without one ends the item): chunks 0, 1, ... of the run, or (sc.on) the
@@ -1643,7 +1660,8 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
 // One wave of blocks; block j takes its share of the layer's chunks (for_each_segment).
 // BITS == 0: no packed part (INT8 rows).  STEAL: units may share their packed chunks on
 // demand (a separate instantiation: the extra code slows the kernels that never use it).
-template <int D, int BITS, int NT, bool STEAL>
+// PAGED: the group records are found through the block table (paged layout).
+template <int D, int BITS, int NT, bool STEAL, bool PAGED>
 __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
     k_decode(const __grid_constant__ DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1663,7 +1681,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
             int r;
             if constexpr (BITS != 0) {
                 if (part == 0)
-                    r = packed_item<D, BITS, NT, STEAL>(a, smem, b, h, slot, t0, t1, phase, sc);
+                    r = packed_item<D, BITS, NT, STEAL, PAGED>(a, smem, b, h, slot, t0, t1, phase, sc);
                 else
                     r = window_item<D, NT>(a, smem, b, h, slot, t0, t1, phase);
             } else {
@@ -1676,13 +1694,14 @@ __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
         [&](int64_t slot) { empty_partial(a, slot); });
 }
 
-// Launch of a decode kernel over one wave of resident blocks; records the block count in
-// a.plan.NB for the merge.  fn_steal (when not null) is the on-demand variant of fn, used
-// when some unit could get 4 packed chunks per block: when the layer's packed capacity
-// holds 4 NB chunks (a unit of cost U gets about U NB / C blocks and holds U / (CH cpt0)
-// packed chunks, so the ratio is C / (NB CH cpt0) for every unit).
+// The decode's wave: NB = one wave of resident blocks of kernel fn (SM count times the
+// occupancy calculator's blocks per SM), the split (unit_aligned) and whether the blocks of
+// a unit should take its chunks on demand: when some unit could get 4 packed chunks per
+// block, i.e. when the layer's packed capacity holds 4 NB chunks (a unit of cost U gets
+// about U NB / C blocks and holds U / (CH cpt0) packed chunks, so the ratio is
+// C / (NB CH cpt0) for every unit).
 template <typename K>
-int launch_wave(K fn, K fn_steal, DecodeArgs& a, cudaStream_t stream) {
+int plan_wave(K fn, DecodeArgs& a) {
     int nb = 0;
     const int rc = decode_blocks(reinterpret_cast<const void*>(fn), kDecodeThreads, a.plan.smem, &nb);
     if (rc != KVQ_OK) return rc;
@@ -1690,32 +1709,91 @@ int launch_wave(K fn, K fn_steal, DecodeArgs& a, cudaStream_t stream) {
     a.plan.inv_nb = 1.0f / nb;
     a.plan.unit_aligned = 2 * (int64_t)a.lo.B * a.lo.H <= nb ? 1 : 0;
     const int64_t packed_chunks = (int64_t)a.lo.B * a.lo.H * (((int64_t)a.lo.NG * a.lo.G) / a.plan.CH);
-    a.plan.steal = fn_steal && a.plan.unit_aligned && a.lo.scheme == KVQ_SCHEME_KIVI && packed_chunks >= 4 * (int64_t)nb;
-    K run = a.plan.steal ? fn_steal : fn;
-    if (run != fn) {
-        int nb2 = 0;   // same shared memory and register bound: the same wave (checked)
-        if (decode_blocks(reinterpret_cast<const void*>(run), kDecodeThreads, a.plan.smem, &nb2) != KVQ_OK || nb2 != nb) {
-            a.plan.steal = 0;
-            run = fn;
-        }
-    }
-    return launch_dependent(run, dim3(static_cast<unsigned>(nb)), kDecodeThreads, static_cast<size_t>(a.plan.smem),
+    a.plan.steal = a.plan.unit_aligned && a.lo.scheme == KVQ_SCHEME_KIVI && packed_chunks >= 4 * (int64_t)nb;
+    return KVQ_OK;
+}
+
+// Launches fn over the wave plan_wave sized (a.plan.NB blocks); KVQ_ERR_UNSUPPORTED, with
+// nothing launched, when fn has another number of resident blocks.
+template <typename K>
+int launch_on_wave(K fn, DecodeArgs& a, cudaStream_t stream) {
+    int nb = 0;
+    const int rc = decode_blocks(reinterpret_cast<const void*>(fn), kDecodeThreads, a.plan.smem, &nb);
+    if (rc != KVQ_OK) return rc;
+    if (nb != a.plan.NB) return KVQ_ERR_UNSUPPORTED;
+    return launch_dependent(fn, dim3(static_cast<unsigned>(nb)), kDecodeThreads, static_cast<size_t>(a.plan.smem),
                             stream, a) == cudaSuccess
                ? KVQ_OK
                : KVQ_ERR_CUDA;
 }
 
+// One kernel on its own wave, the fixed split (FP8, rows).
 template <typename K>
 int launch_wave(K fn, DecodeArgs& a, cudaStream_t stream) {
-    return launch_wave(fn, static_cast<K>(nullptr), a, stream);
+    const int rc = plan_wave(fn, a);
+    if (rc != KVQ_OK) return rc;
+    a.plan.steal = 0;
+    return launch_on_wave(fn, a, stream);
 }
 
+// KIVI variants beyond the base kernel, each family in translation units of its own (so
+// the builds run in parallel): on demand (STEAL), paged layout (PAGED) and both.  The
+// paged fixed-split kernel plans its own wave (it is the paged fallback).
+template <int D, int BITS, int NT, bool STEAL, bool PAGED>
+int launch_kivi_variant(DecodeArgs& a, cudaStream_t stream) {
+    if constexpr (PAGED && !STEAL) {   // the fixed split, on the paged kernel's own wave
+        const int rc = plan_wave(k_decode<D, BITS, NT, false, true>, a);
+        if (rc != KVQ_OK) return rc;
+        a.plan.steal = 0;
+    }
+    return launch_on_wave(k_decode<D, BITS, NT, STEAL, PAGED>, a, stream);
+}
+template <int BITS, bool STEAL, bool PAGED>
+int launch_kivi_family(DecodeArgs& a, cudaStream_t stream) {
+    const bool wide = a.lo.gqa > 4;
+    switch (a.lo.D) {
+        case 64:
+            return wide ? launch_kivi_variant<64, BITS, 2, STEAL, PAGED>(a, stream)
+                        : launch_kivi_variant<64, BITS, 1, STEAL, PAGED>(a, stream);
+        case 128:
+            return wide ? launch_kivi_variant<128, BITS, 2, STEAL, PAGED>(a, stream)
+                        : launch_kivi_variant<128, BITS, 1, STEAL, PAGED>(a, stream);
+        case 256:
+            return wide ? launch_kivi_variant<256, BITS, 2, STEAL, PAGED>(a, stream)
+                        : launch_kivi_variant<256, BITS, 1, STEAL, PAGED>(a, stream);
+        default: return KVQ_ERR_UNSUPPORTED;
+    }
+}
+int launch_decode_kivi2_steal(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi4_steal(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi8_steal(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi2_paged(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi4_paged(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi8_paged(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi2_paged_steal(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi4_paged_steal(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi8_paged_steal(DecodeArgs& a, cudaStream_t stream);
+
+// The base kernel sizes the wave; paged caches and on-demand splits go to their variants.
 template <int D, int BITS, int NT>
 int launch_decode_t(DecodeArgs& a, cudaStream_t stream) {
-    if constexpr (BITS != 0)
-        return launch_wave(k_decode<D, BITS, NT, false>, k_decode<D, BITS, NT, true>, a, stream);
-    else
-        return launch_wave(k_decode<D, BITS, NT, false>, a, stream);
+    int rc = plan_wave(k_decode<D, BITS, NT, false, false>, a);
+    if (rc != KVQ_OK) return rc;
+    if constexpr (BITS != 0) {
+        if (a.lo.PG > 0) {
+            if constexpr (BITS == 2) return launch_decode_kivi2_paged(a, stream);
+            else if constexpr (BITS == 4) return launch_decode_kivi4_paged(a, stream);
+            else return launch_decode_kivi8_paged(a, stream);
+        }
+        if (a.plan.steal) {
+            if constexpr (BITS == 2) rc = launch_decode_kivi2_steal(a, stream);
+            else if constexpr (BITS == 4) rc = launch_decode_kivi4_steal(a, stream);
+            else rc = launch_decode_kivi8_steal(a, stream);
+            if (rc != KVQ_ERR_UNSUPPORTED) return rc;
+        }
+    }
+    a.plan.steal = 0;   // the fixed split
+    return launch_on_wave(k_decode<D, BITS, NT, false, false>, a, stream);
 }
 
 // Dispatchers, one per translation unit.

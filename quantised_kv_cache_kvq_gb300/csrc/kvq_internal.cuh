@@ -20,6 +20,9 @@
 //              K params 4*D B: fp16 scale[D] then fp16 zero[D] (per channel, "min")
 //              V params 4*G*(D/Gv) B: fp16 scale[D/Gv][G] then fp16 zero[D/Gv][G], tile
 //                       token tt of a group's row at position 2 (tt mod 8) + tt / 8
+//            Paged layout (page_groups PG > 0): the records live in a pool of NP pages of
+//            L * H * PG records; record (l, b, h, g) is record (l * H + h) * PG + g mod PG
+//            of page block_table[b * MP + g / PG], MP = ceil(NG / PG).
 //            then the bf16 window ("ring"): per (layer, sequence, kv head) C = R + G slots
 //            of [K row bf16[D], V row bf16[D]]; token t (qn <= t < n) lives in slot t % C.
 //   INT8     per (layer, sequence, kv head), T16 = max_tokens rounded up to 16:
@@ -50,6 +53,9 @@ struct Layout {
     int64_t state_off, scales_off, data_off, ring_off, total;
     int64_t unit;                    // bytes of one (layer, sequence, kv head) data block
     int32_t rec, kc, vc, kp, vp;     // KIVI record: total, K codes, V codes, K params, V params
+    int32_t PG, NP, MP;              // paged layout: records per page and sequence, pages, table row
+    int64_t page;                    // paged layout: bytes of a page
+    const int32_t* table;            // paged layout: the block table (device)
 };
 
 inline int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
@@ -142,6 +148,25 @@ __device__ __forceinline__ const int32_t* state_ptr(const Layout& lo, const uint
 }
 __device__ __forceinline__ int64_t unit_index(const Layout& lo, int l, int b, int h) {
     return ((int64_t)l * lo.B + b) * lo.H + h;
+}
+
+// Byte offset, from the cache base, of KIVI group record g of unit (l, b, h).  Paged
+// layout: through the sequence's block table; -1 when its entry is outside the pool.
+__device__ __forceinline__ int64_t group_offset(const Layout& lo, int l, int b, int h, int64_t g) {
+    if (lo.PG == 0) return lo.data_off + unit_index(lo, l, b, h) * lo.unit + g * lo.rec;
+    const int pg = static_cast<int>(g) / lo.PG;
+    const int32_t p = lo.table[(int64_t)b * lo.MP + pg];
+    if (p < 0 || p >= lo.NP) return -1;
+    return lo.data_off + (int64_t)p * lo.page + (((int64_t)l * lo.H + h) * lo.PG + (g - (int64_t)pg * lo.PG)) * lo.rec;
+}
+// True when every group slot in [g0, g1) of sequence b has a page in the pool.
+__device__ __forceinline__ bool pages_ok(const Layout& lo, int b, int64_t g0, int64_t g1) {
+    if (lo.PG == 0 || g0 >= g1) return true;
+    for (int64_t pg = g0 / lo.PG; pg <= (g1 - 1) / lo.PG; ++pg) {
+        const int32_t p = lo.table[(int64_t)b * lo.MP + pg];
+        if (p < 0 || p >= lo.NP) return false;
+    }
+    return true;
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t v) {

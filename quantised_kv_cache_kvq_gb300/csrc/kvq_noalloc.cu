@@ -94,8 +94,9 @@ extern "C" int kvq_decode_attention_noalloc(const kvq_config* cfg, const void* c
     rc = kvq::make_plan(lo, &plan);
     if (rc != KVQ_OK) return rc;
     if (plan.ws_total > static_cast<int64_t>(KVQ_NOALLOC_SCRATCH_BYTES)) return KVQ_ERR_WORKSPACE;
+    if (lo.PG > 0 && !lo.table) return KVQ_ERR_ARG;
     if (reinterpret_cast<uintptr_t>(cache) % 256 || reinterpret_cast<uintptr_t>(q) % 16 ||
-        reinterpret_cast<uintptr_t>(out) % 16)
+        reinterpret_cast<uintptr_t>(out) % 16 || reinterpret_cast<uintptr_t>(lo.table) % 4)
         return KVQ_ERR_ALIGN;
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) return KVQ_ERR_CUDA;

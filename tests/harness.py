@@ -29,14 +29,18 @@ def q_as_float(q: torch.Tensor) -> np.ndarray:
 
 class Pair:
     def __init__(self, scheme="kivi", layers=1, batch=2, q_heads=8, kv_heads=2, head_dim=128,
-                 max_tokens=256, bits=2, group_k=32, group_v=32, residual=32, in_dtype="bf16"):
+                 max_tokens=256, bits=2, group_k=32, group_v=32, residual=32, in_dtype="bf16",
+                 page_groups=0, num_pages=0, block_table=None):
         sch = {"kivi": 0, "int8": 1, "fp8": 2, "fp8e5m2": 3, "int4": 4}[scheme]
         dt = 0 if in_dtype == "bf16" else 1
         self.kw = dict(scheme=sch, layers=layers, batch=batch, q_heads=q_heads, kv_heads=kv_heads,
                        head_dim=head_dim, bits=bits if sch == 0 else (4 if sch == 4 else 8), group_k=group_k,
-                       group_v=group_v, residual=residual, max_tokens=max_tokens, in_dtype=dt)
+                       group_v=group_v, residual=residual, max_tokens=max_tokens, in_dtype=dt,
+                       page_groups=page_groups, num_pages=num_pages)
         self.lib_cfg = K.KvqConfig(**self.kw)
         self.orc_cfg = O.make_config(**self.kw)
+        if block_table is not None:
+            self.set_block_table(block_table)
         self.torch_dtype = torch.bfloat16 if dt == 0 else torch.float32
         self.nbytes = K.kvq_cache_bytes(self.lib_cfg, max_tokens)
         self.img = O.Image(self.orc_cfg)
@@ -44,6 +48,12 @@ class Pair:
         self.gpu = torch.zeros(self.nbytes, dtype=torch.uint8, device="cuda")
         K.kvq_cache_init(self.lib_cfg, self.gpu)
         self.ws = torch.zeros(K.kvq_workspace_bytes(self.lib_cfg), dtype=torch.uint8, device="cuda")
+
+    def set_block_table(self, table):
+        """Paged layout: the same block table (int32 [batch][max_pages]) on both sides."""
+        table = np.ascontiguousarray(table, dtype=np.int32)
+        self.lib_cfg.set_block_table(torch.from_numpy(table).cuda())
+        O.set_block_table(self.orc_cfg, table)
 
     # ------------------------------------------------------------------ inputs
     def rand_kv(self, seq_count, n_new, gen, scale=1.0, outliers=True):

@@ -70,6 +70,9 @@ def test_formula_mode_reproduces_the_pages_numbers():
     dict(scheme=3, layers=2, batch=3, q_heads=32, kv_heads=8, max_tokens=1000),
     dict(scheme=4, head_dim=64, q_heads=8, kv_heads=2, max_tokens=333, in_dtype=1),
     dict(residual=0, max_tokens=10),
+    dict(page_groups=4, num_pages=10),                                       # paged KIVI layouts
+    dict(bits=4, group_k=128, group_v=128, max_tokens=20000, page_groups=1, num_pages=300, layers=3),
+    dict(residual=0, max_tokens=10, page_groups=3, num_pages=1),
 ])
 def test_layout_size_matches_the_specification(kw):
     c = _cfg(**kw)
@@ -90,6 +93,10 @@ BAD = [
     (dict(in_dtype=1), N.KVQ_ERR_ARG),                    # KIVI window keeps bf16 inputs
     (dict(max_tokens=0), N.KVQ_ERR_ARG),
     (dict(batch=0), N.KVQ_ERR_ARG),
+    (dict(page_groups=-1), N.KVQ_ERR_ARG),
+    (dict(page_groups=2, num_pages=0), N.KVQ_ERR_ARG),        # a paged cache needs a pool
+    (dict(scheme=1, head_dim=32, q_heads=4, kv_heads=4, in_dtype=1, page_groups=2, num_pages=4),
+     N.KVQ_ERR_UNSUPPORTED),                                   # pages hold KIVI group records
 ]
 
 
@@ -128,6 +135,17 @@ def test_host_side_argument_checks_before_any_launch():
     assert lib.kvq_read_status(None, None, None, None) == N.KVQ_ERR_ARG
     # zero-size appends are accepted and do nothing
     assert lib.kvq_quantize_append(C.byref(c), q, 0, 0, 0, None, None, 1, None, None, 0, None) == N.KVQ_OK
+    # a paged cache without its block table, or with a misaligned one
+    pg = _cfg(page_groups=4, num_pages=64)
+    lib.kvq_workspace_bytes(C.byref(pg), C.byref(ws))
+    assert lib.kvq_quantize_append(C.byref(pg), q, 0, 0, 1, q, q, 1, None, None, 0, None) == N.KVQ_ERR_ARG
+    assert lib.kvq_flush_group(C.byref(pg), q, 0, None) == N.KVQ_ERR_ARG
+    assert lib.kvq_decode_attention(C.byref(pg), q, 0, q, C.c_float(1.0), q, q, ws.value, None) == N.KVQ_ERR_ARG
+    assert lib.kvq_decode_attention_noalloc(C.byref(pg), q, 0, q, C.c_float(1.0), q, None) == N.KVQ_ERR_ARG
+    pg.block_table = fake + 2
+    assert lib.kvq_quantize_append(C.byref(pg), q, 0, 0, 1, q, q, 1, None, None, 0, None) == N.KVQ_ERR_ALIGN
+    assert lib.kvq_flush_group(C.byref(pg), q, 0, None) == N.KVQ_ERR_ALIGN
+    assert lib.kvq_decode_attention(C.byref(pg), q, 0, q, C.c_float(1.0), q, q, ws.value, None) == N.KVQ_ERR_ALIGN
 
 
 def test_status_strings():

@@ -753,3 +753,120 @@ def test_int4_attention_brute_force():
         den = sum(e)
         ref = [sum(e[t] / den * V[t][i] for t in range(n)) for i in range(32)]
         np.testing.assert_allclose(out[0, hq], ref, rtol=1e-11, atol=1e-13)
+
+
+# ------------------------------------------------------------------------- paged layout
+def _paged_cfg(**kw):
+    base = dict(scheme=0, layers=2, batch=2, kv_heads=2, q_heads=2, head_dim=64, bits=2, group_k=16,
+                group_v=16, residual=0, max_tokens=64)
+    base.update(kw)
+    return base
+
+
+def _golden_lines(name):
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.split("#")[0].strip()
+        if line:
+            rows.append(line.split())
+    return rows
+
+
+def test_paged_layout_golden_offsets():
+    table = np.array([[3, 0], [4, 1]], np.int32)
+    cfg = O.make_config(page_groups=2, num_pages=5, block_table=table, **_paged_cfg())
+    rows = [r for r in _golden_lines("layout_paged.txt")]
+    recs = [r for r in rows if len(r) == 5]
+    assert len(recs) == 10
+    for l, b, h, g, off in recs:
+        assert O.record_offset(cfg, int(l), int(b), int(h), int(g)) == int(off), (l, b, h, g)
+    reg = O.Image(cfg).regions()
+    named = {r[0]: int(r[1]) for r in rows if len(r) == 2}
+    assert reg["ring"] == named["ring"] and reg["total"] == named["total"]
+
+
+def _kv(seed, seqs, n, H, D):
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randn(seqs, n, H, D, generator=g)
+    v = torch.randn(seqs, n, H, D, generator=g)
+    k[..., 5] *= 10.0
+    return _bf16_bits(k.to(torch.bfloat16)), _bf16_bits(v.to(torch.bfloat16))
+
+
+def test_paged_layout_one_page_per_sequence_is_the_contiguous_layout():
+    # one sequence whose single page holds all its group slots, page 0: record (l, 0, h, g)
+    # lands at ((l * H + h) * NG + g) records, the contiguous layout's place, so the two
+    # images must agree byte for byte after the same calls
+    kw = dict(scheme=0, layers=2, batch=1, kv_heads=3, q_heads=6, head_dim=64, bits=4, group_k=32,
+              group_v=32, residual=40, max_tokens=300)
+    ng = (300 - 40) // 32
+    flat = O.Image(O.make_config(**kw))
+    paged = O.Image(O.make_config(page_groups=ng, num_pages=1, block_table=np.zeros((1, 1), np.int32), **kw))
+    assert flat.nbytes == paged.nbytes
+    for layer in range(2):
+        k, v = _kv(40 + layer, 1, 150, 3, 64)
+        for img in (flat, paged):
+            img.append(layer, 0, k, v)
+        for step in range(45):
+            k, v = _kv(100 + step, 1, 1, 3, 64)
+            for img in (flat, paged):
+                img.append(layer, 0, k, v)
+    assert np.array_equal(flat.buf, paged.buf)
+
+
+def test_paged_layout_decodes_as_the_contiguous_layout():
+    # a shuffled block table over a larger pool: placement only, so every dequantised token
+    # and the attention outputs are the contiguous cache's, exactly
+    kw = dict(scheme=0, layers=1, batch=3, kv_heads=2, q_heads=4, head_dim=64, bits=2, group_k=16,
+              group_v=32, residual=20, max_tokens=200)
+    ng = (200 - 20) // 16
+    pg = 3
+    mp = (ng + pg - 1) // pg
+    rng = np.random.default_rng(5)
+    table = rng.permutation(3 * mp + 4)[:3 * mp].reshape(3, mp).astype(np.int32)
+    flat = O.Image(O.make_config(**kw))
+    paged = O.Image(O.make_config(page_groups=pg, num_pages=3 * mp + 4, block_table=table, **kw))
+    k, v = _kv(7, 3, 190, 2, 64)
+    nv = np.array([190, 37, 111], np.int32)
+    for img in (flat, paged):
+        assert img.append(0, 0, k, v, n_valid=nv) == 0
+    assert not np.array_equal(flat.buf, paged.buf)
+    for b in range(3):
+        for h in range(2):
+            for t in (0, 15, 16, 36, 100, 150, 189):
+                if t < nv[b]:
+                    fk, fv = flat.dequant_token(0, b, h, t)
+                    pk, pv = paged.dequant_token(0, b, h, t)
+                    assert np.array_equal(fk, pk) and np.array_equal(fv, pv)
+    q = np.random.default_rng(6).standard_normal((3, 4, 64)).astype(np.float32)
+    assert np.array_equal(flat.decode(0, q, 0.125), paged.decode(0, q, 0.125))
+    # the rings, counts and header are where the contiguous layout has them
+    rf, rp = flat.regions(), paged.regions()
+    assert np.array_equal(flat.buf[:rf["data"]], paged.buf[:rp["data"]])
+    assert np.array_equal(flat.buf[rf["ring"]:], paged.buf[rp["ring"]:])
+
+
+def test_paged_layout_page_outside_the_pool_leaves_the_sequence_unchanged():
+    kw = _paged_cfg(layers=1, residual=8)
+    ng = (64 - 8) // 16
+    mp = (ng + 1) // 2
+    table = np.array([[0, 1], [2, 7]], np.int32)       # page 7 is outside a pool of 4
+    img = O.Image(O.make_config(page_groups=2, num_pages=4, block_table=table, **kw))
+    k, v = _kv(9, 2, 30, 2, 64)
+    # 30 tokens with R = 8: groups 0 (tokens 0..15) leave the window -- page 0 (seq 0), 2 (seq 1)
+    assert img.append(0, 0, k, v) == 0
+    assert img.state(0, 0) == (30, 16) and img.state(0, 1) == (30, 16)
+    before = img.buf.copy()
+    # 34 more: groups 1 and 2 of each sequence leave the window; group 2 of sequence 1 is in
+    # its table page 1 -> 7, so that sequence must stay as it was
+    k, v = _kv(10, 2, 34, 2, 64)
+    st = img.append(0, 0, k, v)
+    assert st == O.ST_BAD_PAGE and img.status & O.ST_BAD_PAGE
+    assert img.state(0, 0) == (64, 48) and img.state(0, 1) == (30, 16)
+    s1 = 256 + 16 * 1
+    assert np.array_equal(img.buf[s1:s1 + 16], before[s1:s1 + 16])
+    ring = img.regions()["ring"]
+    cap = 8 + 16
+    u1 = slice(ring + 2 * cap * 256, ring + 4 * cap * 256)   # the two ring blocks of sequence 1
+    assert np.array_equal(img.buf[u1], before[u1])
+    assert mp == 2

@@ -9,6 +9,8 @@ import numpy as np
 import pytest
 import torch
 
+import oracle as O
+import quantised_kv_cache_kvq_gb300 as K
 from harness import Pair, assert_close
 
 pytestmark = pytest.mark.gpu
@@ -332,6 +334,90 @@ def test_decode_schedule_chunks_on_demand():
         k, v = p.rand_kv(2, 1, g)
         p.append(0, k, v)
     assert p.status() == 0
+
+
+# ------------------------------------------------------------------------- paged layout
+def _table(rng, batch, mp, spare):
+    """A block table over a shuffled pool with `spare` pages nobody uses."""
+    return rng.permutation(batch * mp + spare)[:batch * mp].reshape(batch, mp).astype(np.int32)
+
+
+@pytest.mark.parametrize("bits,G,PG", [(2, 32, 4), (4, 16, 1), (8, 64, 3)])
+def test_paged_kivi_append_flush_and_decode(bits, G, PG):
+    # the group records live in a pool of pages found through a per-sequence block table;
+    # the image (pool included) must match the oracle's byte for byte, and the decode must
+    # give exactly what the same cache in the contiguous layout gives
+    lens = [333, 0, 517]
+    kw = dict(batch=3, q_heads=8, kv_heads=2, head_dim=128, max_tokens=600, bits=bits, group_k=G, group_v=32,
+              residual=24)
+    ng = (600 - 24) // G
+    mp = (ng + PG - 1) // PG
+    rng = np.random.default_rng(bits * 100 + G)
+    p = Pair("kivi", page_groups=PG, num_pages=3 * mp + 5, block_table=_table(rng, 3, mp, 5), **kw)
+    f = Pair("kivi", **kw)
+    g = gen(40 + bits)
+    k, v = p.rand_kv(3, max(lens), g)
+    for x in (p, f):
+        x.append(0, k, v, n_valid=lens)
+    p.assert_same_image()
+    for step in range(40):
+        k, v = p.rand_kv(3, 1, g)
+        for x in (p, f):
+            x.append(0, k, v, flags=K.KVQ_NO_AUTOFLUSH if step % 7 == 3 else 0)
+        if step % 13 == 5:
+            for x in (p, f):
+                x.flush(0)
+    p.assert_same_image()
+    q = p.rand_q(g)
+    out, ref = p.decode(0, q)
+    out_f, _ = f.decode(0, q)
+    assert_close(out, ref, what="paged %d-bit" % bits)
+    assert np.array_equal(out, out_f)
+    assert p.status() == 0
+
+
+def test_paged_decode_chunks_on_demand():
+    # long sequences in a paged cache: the blocks take their chunks on demand and every
+    # chunk's groups may straddle pages
+    lens = [400000, 300007]
+    kw = dict(batch=2, q_heads=4, kv_heads=2, head_dim=64, max_tokens=max(lens) + 64, bits=2, group_k=32,
+              group_v=32, residual=100)
+    ng = (kw["max_tokens"] - 100) // 32
+    PG = 5
+    mp = (ng + PG - 1) // PG
+    p = Pair("kivi", page_groups=PG, num_pages=2 * mp + 3, block_table=_table(np.random.default_rng(3), 2, mp, 3),
+             **kw)
+    g = gen(28)
+    k, v = p.rand_kv(2, max(lens), g)
+    p.append(0, k, v, n_valid=lens)
+    del k, v
+    p.assert_same_image()
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="paged, chunks on demand")
+    assert p.status() == 0
+
+
+def test_paged_page_outside_the_pool_is_reported():
+    kw = dict(batch=2, q_heads=8, kv_heads=2, head_dim=128, max_tokens=256, bits=2, group_k=32, group_v=32,
+              residual=16)
+    ng = (256 - 16) // 32
+    mp = (ng + 1) // 2
+    table = _table(np.random.default_rng(9), 2, mp, 0)
+    table[1, 1] = 2 * mp + 7                  # sequence 1's second page is outside the pool
+    p = Pair("kivi", page_groups=2, num_pages=2 * mp, block_table=table, **kw)
+    g = gen(29)
+    k, v = p.rand_kv(2, 140, g)
+    p.append(0, k, v)              # groups 0..2 of each: sequence 1's group 2 needs the bad page
+    assert p.img.status & O.ST_BAD_PAGE
+    p.assert_same_image()          # sequence 1 unchanged on both sides, status word included
+    assert p.status() & K.KVQ_STATUS_BAD_PAGE
+    # a decode that reads through a bad entry reports it (its output is invalid)
+    table2 = table.copy()
+    table2[1, 1] = table[1, 0]
+    table2[0, 0] = -3
+    p.set_block_table(table2)
+    p.decode(0, p.rand_q(g))
+    assert K.kvq_read_status(None, p.ws) & K.KVQ_STATUS_BAD_PAGE
 
 
 def test_decode_schedule_total_smaller_than_the_grid():
