@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = ("quantised-cache decode attention tokens/s and achieved HBM GB/s (% of peak), 1 GB300")
 L2_BYTES = 129 * 2 ** 20
 # the timed workloads (the tiny INT8 one is a correctness case, checked by the tests)
-SUITE = ("kivi2_llama3_8b", "kivi4_128k", "fp8_32layer", "serve_mix")
+SUITE = ("kivi2_llama3_8b", "kivi4_128k", "fp8_32layer", "serve_mix", "serve_mix_paged")
 
 
 def peaks():
@@ -196,9 +196,13 @@ def run_gpu(args, w, world, all_layers, nsteps, sampler_on):
     total_steps = args.warmup + nsteps * replays + e2e_steps * e2e_runs
     appends_per_rep = math.ceil(total_steps / reps) + 1
     max_tokens = max(lens0) + appends_per_rep + 16
+    paging = {}
+    if w.page_groups:   # one block table for every replica (each has its own pool)
+        pool, table = W.block_table(w, max_tokens, device=dev)
+        paging = dict(page_groups=w.page_groups, num_pages=pool, block_table=table)
     cfg = K.make_config(w.scheme, layers, w.batch, w.q_heads, w.kv_heads, w.head_dim, max_tokens,
                         bits=w.bits, group_k=w.group_k, group_v=w.group_v, residual=w.residual,
-                        in_dtype=w.in_dtype)
+                        in_dtype=w.in_dtype, **paging)
     caches = []
     fp8 = None
     if w.scheme == 2:   # static per-(kv head) scales from the first replica's fill
@@ -429,6 +433,9 @@ def oracle_setup(w, nseq):
     kw = dict(scheme=w.scheme, layers=1, batch=nseq, q_heads=w.q_heads, kv_heads=w.kv_heads,
               head_dim=w.head_dim, bits=w.bits if w.scheme == 0 else 8, group_k=w.group_k, group_v=w.group_v,
               residual=w.residual, max_tokens=n0 + 4096, in_dtype=0 if w.in_dtype == "bf16" else 1)
+    if w.page_groups:
+        pool, table = W.block_table(w, kw["max_tokens"])
+        kw.update(page_groups=w.page_groups, num_pages=pool, block_table=table[:nseq].numpy())
     img = O.Image(O.make_config(**kw))
     k, v = W.kv_tokens(w, 0, 0, nseq, 0, n0, device="cpu", tag="cpu")
     to = (lambda t: t.view(torch.int16).numpy().view(np.uint16)) if w.in_dtype == "bf16" else (lambda t: t.numpy())
@@ -479,10 +486,14 @@ def cpu_record(w, res, layers):
 # ---------------------------------------------------------------------------- records
 def workload_config(w, layers):
     ragged = w.context[0] != w.context[1]
-    return {"workload": w.name, "scheme": ["kivi", "int8", "fp8"][w.scheme], "bits": w.bits,
-            "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads, "head_dim": w.head_dim,
-            "context": list(w.context) if ragged else w.context[0], "group_k": w.group_k,
-            "group_v": w.group_v, "residual": w.residual, "layers": layers}
+    cfg = {"workload": w.name, "scheme": ["kivi", "int8", "fp8", "fp8e5m2", "int4"][w.scheme], "bits": w.bits,
+           "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads, "head_dim": w.head_dim,
+           "context": list(w.context) if ragged else w.context[0], "group_k": w.group_k,
+           "group_v": w.group_v, "residual": w.residual, "layers": layers}
+    if w.page_groups:
+        cfg["layout"] = "paged: %d group records (%d tokens) a page, shuffled block table" % (
+            w.page_groups, w.page_groups * w.group_k)
+    return cfg
 
 
 def gpu_record(w, r, world, peak, peak_kind):

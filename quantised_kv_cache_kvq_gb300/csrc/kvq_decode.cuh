@@ -1145,21 +1145,36 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
         if constexpr (!PAGED) {
             bulk_copy_pieces(dst, src_groups + (int64_t)c * gpc * rec, bytes, bar);
         } else {
-            // paged layout: one copy per run of the chunk's groups that shares a page
-            int g = static_cast<int>(t0 / G) + c * gpc;
+            // paged layout: one copy per run of the chunk's groups that shares a page.  The
+            // item's sequence, kv head and first group come back from shared memory (kept
+            // there so that they hold no registers through the chunk loop).
+            const int* pi = reinterpret_cast<const int*>(smem + so.hstat) + 16;
+            const int pb = pi[0], ph = pi[1];
+            int g = pi[2] + c * gpc;
             for (int x = 0; x < gj;) {
-                const int run = min(lo.PG - g % lo.PG, gj - x);
-                int64_t off = group_offset(lo, a.layer, b, h, g);
-                if (off < 0) {   // a table entry outside the pool: read page 0, report it
+                const int pg = g / lo.PG, slot = g - pg * lo.PG;
+                const int run = min(lo.PG - slot, gj - x);
+                int p = lo.table[(int64_t)pb * lo.MP + pg];
+                if (p < 0 || p >= lo.NP) {   // a table entry outside the pool: read page 0, report it
                     atomicOr(reinterpret_cast<uint32_t*>(a.ws), KVQ_STATUS_BAD_PAGE);
-                    off = lo.data_off + (((int64_t)a.layer * lo.H + h) * lo.PG + g % lo.PG) * rec;
+                    p = 0;
                 }
+                const int64_t off = lo.data_off + (int64_t)p * lo.page + (((int64_t)a.layer * lo.H + ph) * lo.PG + slot) * rec;
                 bulk_copy_pieces(dst + (int64_t)x * rec, a.cache + off, static_cast<uint32_t>(run) * rec, bar);
                 x += run;
                 g += run;
             }
         }
     };
+    if constexpr (PAGED) {
+        if (tid == 0) {
+            int* pi = reinterpret_cast<int*>(smem + so.hstat) + 16;
+            pi[0] = b;
+            pi[1] = h;
+            pi[2] = static_cast<int>(t0 / G);
+        }
+    }
+
     // the chunk each stage holds (-1: none; the chunks come in increasing order, so the
     // first stage without one ends the item): chunks 0, 1, ... of the run, or (sc.on) the
     // block's fixed chunks and then counter grabs.  Thread 0 writes an entry before a

@@ -51,6 +51,7 @@ class Workload:
     softmax_scale: Optional[float] = None   # None: 1/sqrt(head_dim)
     seed: int = 0
     steps: int = 1              # decode steps in the workload
+    page_groups: int = 0        # KIVI paged layout: group records per page (0: contiguous)
 
     @property
     def scale(self) -> float:
@@ -80,7 +81,25 @@ WORKLOADS = {
     "serve_mix": Workload(
         "serve_mix", scheme=0, layers=1, batch=256, q_heads=32, kv_heads=8, head_dim=128,
         context=(1024, 32768), bits=2, group_k=32, group_v=32, residual=128, seed=4, steps=64),
+    # the serving mix with its group records in a page pool (16 groups = 512 tokens a page),
+    # pages handed out in a shuffled order
+    "serve_mix_paged": Workload(
+        "serve_mix_paged", scheme=0, layers=1, batch=256, q_heads=32, kv_heads=8, head_dim=128,
+        context=(1024, 32768), bits=2, group_k=32, group_v=32, residual=128, seed=4, steps=64,
+        page_groups=16),
 }
+
+
+def block_table(w: Workload, max_tokens: int, device="cpu"):
+    """Paged workloads: (num_pages, int32 [batch][max_pages] block table) for caches of
+    `max_tokens` tokens per sequence -- every page of every sequence, in a shuffled order
+    over a pool with 1% spare pages."""
+    ng = (max_tokens - w.residual) // w.group_k if max_tokens > w.residual else 0
+    mp = (ng + w.page_groups - 1) // w.page_groups
+    pool = w.batch * mp + max(1, w.batch * mp // 100)
+    g = _gen((w.seed, "pages"), "cpu")
+    perm = torch.randperm(pool, generator=g)[: w.batch * mp].to(torch.int32)
+    return pool, perm.view(w.batch, mp).to(device)
 
 
 def _gen(seed_parts, device) -> torch.Generator:
