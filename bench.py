@@ -125,8 +125,9 @@ def decode_bytes(w, lengths):
 
 
 DECODE_SOURCES = ("kvq_api.cu", "kvq_decode.cuh", "kvq_decode_rows.cu", "kvq_internal.cuh", "kvq_launch.h")
-SCHEME_SOURCES = {0: ("kvq_decode_kivi2.cu", "kvq_decode_kivi4.cu", "kvq_decode_kivi8.cu"),
-                  1: (), 2: ("kvq_decode_fp8.cu",)}
+SCHEME_SOURCES = {0: tuple("kvq_decode_kivi%d%s.cu" % (b, v) for b in (2, 4, 8)
+                            for v in ("", "_steal", "_paged", "_paged_steal")),
+                  1: (), 2: ("kvq_decode_fp8.cu",), 3: ("kvq_decode_fp8.cu",), 4: ()}
 
 
 def sources_sha256(scheme):

@@ -27,7 +27,7 @@ class OracleConfig(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "scheme", "layers", "batch", "q_heads", "kv_heads", "head_dim", "bits",
         "group_k", "group_v", "residual", "max_tokens", "in_dtype", "page_groups", "num_pages")] + [
-        ("block_table", C.c_void_p)]
+        ("block_table", C.c_void_p), ("rope_base", C.c_float)]
 
 
 def lib():
@@ -53,6 +53,7 @@ def lib():
             "kvqo_image_bytes": (i64, [P]),
             "kvqo_image_regions": (None, [P, P]),
             "kvqo_record_offset": (i64, [P, C.c_int, C.c_int, C.c_int, i64]),
+            "kvqo_rope_key": (None, [C.c_int, f64, i64, P, P]),
             "kvqo_image_init": (None, [P, P]),
             "kvqo_append": (u32, [P, P, C.c_int, C.c_int, C.c_int, P, P, C.c_int, P, P, u32]),
             "kvqo_flush": (None, [P, P, C.c_int]),
@@ -148,10 +149,20 @@ def make_config(block_table=None, **kw):
                     group_k=32, group_v=32, residual=0, max_tokens=64, in_dtype=DT_BF16, page_groups=0,
                     num_pages=0)
     defaults.update(kw)
+    rope = float(defaults.pop("rope_base", 0.0))
     for k, v in defaults.items():
         setattr(c, k, int(v))
+    c.rope_base = rope
     set_block_table(c, block_table)
     return c
+
+
+def rope_key(k, pos, base):
+    """The oracle's rotary embedding of one key row (float32 [D]) at position pos."""
+    k = np.ascontiguousarray(k, np.float32)
+    out = np.zeros(k.shape[0])
+    lib().kvqo_rope_key(k.shape[0], float(base), int(pos), _p(k), _p(out))
+    return out
 
 
 def set_block_table(cfg, table):

@@ -52,6 +52,8 @@ typedef struct {
     int32_t page_groups;          /* KIVI paged layout: group records per page (0: none) */
     int32_t num_pages;            /* pages in the pool */
     const int32_t* block_table;   /* [batch][max_pages]: pool page of each page of a sequence */
+    float rope_base;              /* KIVI keys cached before the rotary embedding: its base
+                                     (0: keys are cached as given) */
 } kvqo_config;
 
 enum { SCHEME_KIVI = 0, SCHEME_INT8 = 1, SCHEME_FP8 = 2, SCHEME_FP8_E5M2 = 3, SCHEME_INT4 = 4 };
@@ -892,6 +894,27 @@ void kvqo_dequant_token(const kvqo_config* c, const uint8_t* img, int l, int b, 
     }
 }
 
+/* The rotary position embedding of a key row at position pos ([KVQ] "Key points": keys
+ * are quantised before RoPE, which rotates channel pairs; the decode applies it to the
+ * dequantised keys).  The pages give no formula: this is the rotary embedding of the
+ * Llama models whose shapes the workloads use, channel i paired with i + D/2 ("rotate
+ * half"): for i < D/2, with w_i = base^(-2i/D) rounded to binary32 and the angle
+ * a = pos * w_i evaluated as one binary32 product (the angles of the usual binary32
+ * rotary tables),
+ *   out[i]       = k[i] cos a - k[i + D/2] sin a
+ *   out[i + D/2] = k[i + D/2] cos a + k[i] sin a,
+ * in binary64 (cos and sin of the binary32 angle). */
+void kvqo_rope_key(int D, double base, int64_t pos, const float* k, double* out)
+{
+    for (int i = 0; i < D / 2; i++) {
+        float w = (float)pow(base, -2.0 * i / D);
+        float a = (float)pos * w;
+        double cs = cos((double)a), sn = sin((double)a);
+        out[i] = (double)k[i] * cs - (double)k[i + D / 2] * sn;
+        out[i + D / 2] = (double)k[i + D / 2] * cs + (double)k[i] * sn;
+    }
+}
+
 /* Single-query decode attention over the cache ([QKV] "Why values per token"):
  *   score_t = softmax_scale * q . Khat_t,  p = softmax(score),  o = sum_t p_t Vhat_t,
  * in binary64 over every cached token of the sequence.  Query head hq reads kv head
@@ -908,14 +931,18 @@ void kvqo_decode_head(const kvqo_config* c, const uint8_t* img, int l, int b, in
     const int32_t* s = state_of(c, (uint8_t*)img, l, b);
     int64_t n = s[0];
     float* kr = (float*)malloc(sizeof(float) * D);
+    double* kd = (double*)malloc(sizeof(double) * D);
     float* vr = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n * D : 1));
     double* sc = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * gqa : 1));
     for (int64_t t = 0; t < n; t++) {
         kvqo_dequant_token(c, img, l, b, h, t, kr, vr + t * D);
+        /* keys cached before the rotary embedding get it now, at their position t */
+        if (c->rope_base > 0.0f) kvqo_rope_key(D, (double)c->rope_base, t, kr, kd);
+        else for (int ch = 0; ch < D; ch++) kd[ch] = (double)kr[ch];
         for (int g = 0; g < gqa; g++) {
             const float* qq = q + ((int64_t)b * Hq + h * gqa + g) * D;
             double acc = 0.0;
-            for (int ch = 0; ch < D; ch++) acc += (double)qq[ch] * (double)kr[ch];
+            for (int ch = 0; ch < D; ch++) acc += (double)qq[ch] * kd[ch];
             sc[t * gqa + g] = softmax_scale * acc;
         }
     }
@@ -934,6 +961,7 @@ void kvqo_decode_head(const kvqo_config* c, const uint8_t* img, int l, int b, in
     }
     free(sc);
     free(vr);
+    free(kd);
     free(kr);
 }
 

@@ -870,3 +870,62 @@ def test_paged_layout_page_outside_the_pool_leaves_the_sequence_unchanged():
     u1 = slice(ring + 2 * cap * 256, ring + 4 * cap * 256)   # the two ring blocks of sequence 1
     assert np.array_equal(img.buf[u1], before[u1])
     assert mp == 2
+
+
+# ------------------------------------------------------------------------- keys before RoPE
+def test_rope_golden_rotations():
+    # hand-derived: D = 4 pairs channel 0 with 2 and 1 with 3; base 10000 gives w = (1, 0.01)
+    # and binary32 100 * 0.01 = 1.0 exactly (0.01 is 0.0099999998 in binary32, the product
+    # 0.99999998 rounds to 1.0), so these rotate by exactly one radian
+    c1, s1 = math.cos(1.0), math.sin(1.0)
+    cases = [([1, 0, 0, 0], 1, [c1, 0, s1, 0]), ([0, 0, 1, 0], 1, [-s1, 0, c1, 0]),
+             ([0, 1, 0, 0], 100, [0, c1, 0, s1]), ([0, 0, 0, 1], 100, [0, -s1, 0, c1]),
+             ([3, -2, 5, 7], 0, [3, -2, 5, 7])]
+    for k, pos, want in cases:
+        got = O.rope_key(np.array(k, np.float32), pos, 10000.0)
+        assert np.allclose(got, want, rtol=0, atol=1e-15), (k, pos, got)
+
+
+def _complex_rotate(k, angles):
+    """Rotation of the channel pairs (i, i + D/2) as complex multiplication."""
+    h = k.shape[-1] // 2
+    z = (k[..., :h].astype(np.float64) + 1j * k[..., h:].astype(np.float64)) * np.exp(1j * angles)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def test_rope_is_a_rotation_by_the_position():
+    # base 1: every pair turns by exactly `pos` radians, as a complex multiplication says;
+    # norms are kept
+    rng = np.random.default_rng(11)
+    for D in (8, 64, 128):
+        for pos in (0, 1, 7, 1000, 131071):
+            k = rng.standard_normal(D).astype(np.float32)
+            got = O.rope_key(k, pos, 1.0)
+            assert np.allclose(got, _complex_rotate(k, np.full(D // 2, float(pos))), rtol=0, atol=1e-12)
+            assert abs(np.linalg.norm(got) - np.linalg.norm(k.astype(np.float64))) < 1e-12
+
+
+def test_rope_decode_is_attention_over_rotated_keys():
+    # unquantised (the whole context in the bf16 window) and quantised KIVI caches whose keys
+    # were cached before the rotary embedding: the oracle's decode equals binary64 attention
+    # over the dequantised keys turned by their positions (base 1: `t` radians)
+    rng = np.random.default_rng(12)
+    for residual, n in ((200, 150), (16, 300)):
+        kw = dict(scheme=0, layers=1, batch=1, kv_heads=1, q_heads=2, head_dim=64, bits=4, group_k=32,
+                  group_v=32, residual=residual, max_tokens=320, rope_base=1.0)
+        img = O.Image(O.make_config(**kw))
+        k = torch.tensor(rng.standard_normal((1, n, 1, 64)), dtype=torch.float32).to(torch.bfloat16)
+        v = torch.tensor(rng.standard_normal((1, n, 1, 64)), dtype=torch.float32).to(torch.bfloat16)
+        assert img.append(0, 0, _bf16_bits(k), _bf16_bits(v)) == 0
+        q = rng.standard_normal((1, 2, 64)).astype(np.float32)
+        out = img.decode(0, q, 0.125)[0]
+        keys = np.zeros((n, 64))
+        vals = np.zeros((n, 64))
+        for t in range(n):
+            kt, vt = img.dequant_token(0, 0, 0, t)
+            keys[t] = _complex_rotate(kt, np.full(32, float(t)))
+            vals[t] = vt
+        s = 0.125 * (q[0].astype(np.float64) @ keys.T)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        want = (p / p.sum(axis=1, keepdims=True)) @ vals
+        assert np.allclose(out, want, rtol=1e-12, atol=1e-12), residual
