@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = ("quantised-cache decode attention tokens/s and achieved HBM GB/s (% of peak), 1 GB300")
 L2_BYTES = 129 * 2 ** 20
 # the timed workloads (the tiny INT8 one is a correctness case, checked by the tests)
-SUITE = ("kivi2_llama3_8b", "kivi4_128k", "fp8_32layer", "serve_mix", "serve_mix_paged")
+SUITE = ("kivi2_llama3_8b", "kivi4_128k", "fp8_32layer", "serve_mix", "serve_mix_paged", "kivi2_llama3_8b_rope")
 
 
 def peaks():
@@ -126,7 +126,7 @@ def decode_bytes(w, lengths):
 
 DECODE_SOURCES = ("kvq_api.cu", "kvq_decode.cuh", "kvq_decode_rows.cu", "kvq_internal.cuh", "kvq_launch.h")
 SCHEME_SOURCES = {0: tuple("kvq_decode_kivi%d%s.cu" % (b, v) for b in (2, 4, 8)
-                            for v in ("", "_steal", "_paged", "_paged_steal")),
+                            for v in ("", "_steal", "_paged", "_paged_steal")) + ("kvq_decode_rope.cu",),
                   1: (), 2: ("kvq_decode_fp8.cu",), 3: ("kvq_decode_fp8.cu",), 4: ()}
 
 
@@ -203,7 +203,7 @@ def run_gpu(args, w, world, all_layers, nsteps, sampler_on):
         paging = dict(page_groups=w.page_groups, num_pages=pool, block_table=table)
     cfg = K.make_config(w.scheme, layers, w.batch, w.q_heads, w.kv_heads, w.head_dim, max_tokens,
                         bits=w.bits, group_k=w.group_k, group_v=w.group_v, residual=w.residual,
-                        in_dtype=w.in_dtype, **paging)
+                        in_dtype=w.in_dtype, rope_base=w.rope_base, **paging)
     caches = []
     fp8 = None
     if w.scheme == 2:   # static per-(kv head) scales from the first replica's fill
@@ -433,7 +433,8 @@ def oracle_setup(w, nseq):
     n0 = max(lens)
     kw = dict(scheme=w.scheme, layers=1, batch=nseq, q_heads=w.q_heads, kv_heads=w.kv_heads,
               head_dim=w.head_dim, bits=w.bits if w.scheme == 0 else 8, group_k=w.group_k, group_v=w.group_v,
-              residual=w.residual, max_tokens=n0 + 4096, in_dtype=0 if w.in_dtype == "bf16" else 1)
+              residual=w.residual, max_tokens=n0 + 4096, in_dtype=0 if w.in_dtype == "bf16" else 1,
+              rope_base=w.rope_base)
     if w.page_groups:
         pool, table = W.block_table(w, kw["max_tokens"])
         kw.update(page_groups=w.page_groups, num_pages=pool, block_table=table[:nseq].numpy())
@@ -494,6 +495,8 @@ def workload_config(w, layers):
     if w.page_groups:
         cfg["layout"] = "paged: %d group records (%d tokens) a page, shuffled block table" % (
             w.page_groups, w.page_groups * w.group_k)
+    if w.rope_base:
+        cfg["keys"] = "cached before the rotary embedding (base %g), rotated in the decode" % w.rope_base
     return cfg
 
 

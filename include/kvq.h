@@ -122,6 +122,14 @@ enum kvq_status_bits {
  *   page_groups KIVI paged layout: group records per page; 0 for the contiguous layout
  *               (the other schemes: 0 only)
  *   num_pages   paged layout: pages in the cache's pool (>= 1)
+ *   rope_base   KIVI: keys are cached before the rotary position embedding and the decode
+ *               rotates every dequantised key at its position ("KVQuant: Towards 10 Million
+ *               Context Length ...", "Key points": keys quantised before RoPE, which mixes
+ *               channel pairs); the embedding's base (e.g. 10000), or 0 for keys cached as
+ *               given.  Channel i is paired with i + head_dim/2; the angle of pair i at
+ *               position t is the binary32 product t * w_i, w_i = base^(-2i/head_dim)
+ *               rounded to binary32; the query is passed already rotated.  The other
+ *               schemes: 0 only.
  *   block_table paged layout, device int32 [batch][max_pages], max_pages = ceil(NG /
  *               page_groups) with NG = floor((max_tokens - residual) / group_k) group slots
  *               per sequence: the pool page holding each run of page_groups group slots of
@@ -154,6 +162,7 @@ typedef struct kvq_config {
     int32_t page_groups;
     int32_t num_pages;
     const int32_t* block_table;
+    float rope_base;
 } kvq_config;
 
 /*

@@ -37,6 +37,7 @@ UNITS = {
     "kvq_decode_kivi8_paged_steal.cu": [],
     "kvq_decode_rows.cu": [],
     "kvq_decode_fp8.cu": [],
+    "kvq_decode_rope.cu": [],
     "kvq_noalloc.cu": [],
 }
 

@@ -22,6 +22,7 @@ int make_layout(const kvq_config* c, int64_t max_tokens, Layout* out) {
     if (max_tokens < 1 || max_tokens > (int64_t)1 << 30) return KVQ_ERR_ARG;
     if (c->in_dtype != KVQ_DTYPE_BF16 && c->in_dtype != KVQ_DTYPE_F32) return KVQ_ERR_ARG;
     if (c->page_groups < 0 || c->num_pages < 0) return KVQ_ERR_ARG;
+    if (!(c->rope_base >= 0.0f) || c->rope_base > 3.0e38f) return KVQ_ERR_ARG;   // NaN, negative, inf
     const int gqa = c->q_heads / c->kv_heads;
     if (gqa != 1 && gqa != 2 && gqa != 4 && gqa != 8) return KVQ_ERR_UNSUPPORTED;
     const int D = c->head_dim;
@@ -72,8 +73,10 @@ int make_layout(const kvq_config* c, int64_t max_tokens, Layout* out) {
         }
         lo.ring_off = pos;
         pos += align256(units * lo.C * 4 * (int64_t)D);
+        lo.rope_base = c->rope_base;
     } else {
         if (c->page_groups > 0) return KVQ_ERR_UNSUPPORTED;   // pages hold KIVI group records
+        if (c->rope_base > 0.0f) return KVQ_ERR_UNSUPPORTED;  // pre-RoPE keys: KIVI caches
         if (!pow2_in(D, 32, 256)) return KVQ_ERR_UNSUPPORTED;
         if (is_rows(c->scheme)) {
             lo.unit = (int64_t)lo.T16 * ((c->scheme == KVQ_SCHEME_INT8 ? 2 * D : D) + 8);

@@ -50,6 +50,7 @@ struct DecodeArgs {
     float qscale;  // softmax_scale * log2(e): scores live in the base-2 domain
     float* out;
     uint8_t* ws;
+    float rope_w[128];   // keys cached before RoPE: w_i = base^(-2i/D) in binary32, i < D/2
 };
 
 // ------------------------------------------------------------------------ scheduling
@@ -1817,5 +1818,6 @@ int launch_decode_kivi4(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi8(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_rows(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_fp8(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_rope(DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace kvq

@@ -1,5 +1,7 @@
 // kvq_decode_rows.cu -- the INT8 / INT4 decode dispatch, the log-sum-exp merge of the partial
 // results, and the decode dispatcher.
+#include <cmath>
+
 #include "kvq_decode.cuh"
 
 namespace kvq {
@@ -221,7 +223,12 @@ int launch_decode(const Layout& lo, const DecodePlan& plan, const uint8_t* cache
     a.out = out;
     a.ws = ws;
     int rc;
-    if (lo.scheme == KVQ_SCHEME_KIVI) {
+    if (lo.scheme == KVQ_SCHEME_KIVI && lo.rope_base > 0.0f) {
+        // keys cached before RoPE: w_i = base^(-2i/D), binary64 power rounded to binary32
+        for (int i = 0; i < lo.D / 2; ++i)
+            a.rope_w[i] = static_cast<float>(std::pow(static_cast<double>(lo.rope_base), -2.0 * i / lo.D));
+        rc = launch_decode_rope(a, stream);
+    } else if (lo.scheme == KVQ_SCHEME_KIVI) {
         rc = lo.bits == 2 ? launch_decode_kivi2(a, stream)
            : lo.bits == 4 ? launch_decode_kivi4(a, stream)
                           : launch_decode_kivi8(a, stream);

@@ -56,6 +56,7 @@ struct Layout {
     int32_t PG, NP, MP;              // paged layout: records per page and sequence, pages, table row
     int64_t page;                    // paged layout: bytes of a page
     const int32_t* table;            // paged layout: the block table (device)
+    float rope_base;                 // > 0: keys cached before the rotary embedding
 };
 
 inline int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }

@@ -52,6 +52,7 @@ class Workload:
     seed: int = 0
     steps: int = 1              # decode steps in the workload
     page_groups: int = 0        # KIVI paged layout: group records per page (0: contiguous)
+    rope_base: float = 0.0      # KIVI keys cached before the rotary embedding (its base)
 
     @property
     def scale(self) -> float:
@@ -87,6 +88,11 @@ WORKLOADS = {
         "serve_mix_paged", scheme=0, layers=1, batch=256, q_heads=32, kv_heads=8, head_dim=128,
         context=(1024, 32768), bits=2, group_k=32, group_v=32, residual=128, seed=4, steps=64,
         page_groups=16),
+    # the KIVI 2-bit Llama-3-8B layer with its keys cached before the rotary embedding
+    # (Llama 3's base 500000), the decode turning every key by its position
+    "kivi2_llama3_8b_rope": Workload(
+        "kivi2_llama3_8b_rope", scheme=0, layers=1, batch=8, q_heads=32, kv_heads=8, head_dim=128,
+        context=(4096, 4096), bits=2, group_k=32, group_v=32, residual=128, seed=1, rope_base=500000.0),
 }
 
 

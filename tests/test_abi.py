@@ -73,6 +73,7 @@ def test_formula_mode_reproduces_the_pages_numbers():
     dict(page_groups=4, num_pages=10),                                       # paged KIVI layouts
     dict(bits=4, group_k=128, group_v=128, max_tokens=20000, page_groups=1, num_pages=300, layers=3),
     dict(residual=0, max_tokens=10, page_groups=3, num_pages=1),
+    dict(rope_base=500000.0),                                # pre-RoPE keys change no byte of the layout
 ])
 def test_layout_size_matches_the_specification(kw):
     c = _cfg(**kw)
@@ -97,6 +98,10 @@ BAD = [
     (dict(page_groups=2, num_pages=0), N.KVQ_ERR_ARG),        # a paged cache needs a pool
     (dict(scheme=1, head_dim=32, q_heads=4, kv_heads=4, in_dtype=1, page_groups=2, num_pages=4),
      N.KVQ_ERR_UNSUPPORTED),                                   # pages hold KIVI group records
+    (dict(rope_base=-1.0), N.KVQ_ERR_ARG),
+    (dict(rope_base=float("nan")), N.KVQ_ERR_ARG),
+    (dict(rope_base=float("inf")), N.KVQ_ERR_ARG),
+    (dict(scheme=2, head_dim=128, rope_base=10000.0), N.KVQ_ERR_UNSUPPORTED),   # pre-RoPE keys: KIVI
 ]
 
 

@@ -420,6 +420,49 @@ def test_paged_page_outside_the_pool_is_reported():
     assert K.kvq_read_status(None, p.ws) & K.KVQ_STATUS_BAD_PAGE
 
 
+# ------------------------------------------------------------------------- keys before RoPE
+@pytest.mark.parametrize("bits,D,gqa,G,Gv,R,base", [(2, 128, 4, 32, 32, 128, 500000.0),
+                                                     (4, 64, 8, 128, 64, 32, 10000.0),
+                                                     (8, 256, 1, 16, 16, 16, 10000.0)])
+def test_rope_keys_cached_before_the_embedding(bits, D, gqa, G, Gv, R, base):
+    # the cache holds keys before the rotary embedding; the decode turns every dequantised
+    # key (packed groups and bf16 window) by its position
+    lens = [0, 5, R + 3, 777, 2 * G + R, 3000]
+    p = Pair("kivi", batch=6, q_heads=2 * gqa, kv_heads=2, head_dim=D, max_tokens=3100, bits=bits, group_k=G,
+             group_v=Gv, residual=R, rope_base=base)
+    g = gen(50 + bits)
+    k, v = p.rand_kv(6, max(lens), g)
+    p.append(0, k, v, n_valid=lens)
+    p.assert_same_image()
+    for step in range(3):
+        out, ref = p.decode(0, p.rand_q(g))
+        assert_close(out, ref, what="rope %d-bit, step %d" % (bits, step))
+        assert not out[0].any() or step > 0
+        k, v = p.rand_kv(6, 1, g)
+        p.append(0, k, v)
+    assert p.status() == 0
+
+
+def test_rope_long_context_large_angles_and_pages():
+    # positions past 100000: the fastest pair turns by more than 10^5 radians (the long
+    # argument reduction of sin and cos); the records in a paged pool
+    lens = [120000, 70001]
+    kw = dict(batch=2, q_heads=4, kv_heads=1, head_dim=64, max_tokens=120064, bits=2, group_k=32, group_v=32,
+              residual=64, rope_base=10000.0)
+    ng = (120064 - 64) // 32
+    mp = (ng + 7) // 8
+    table = np.random.default_rng(13).permutation(2 * mp + 1)[:2 * mp].reshape(2, mp).astype(np.int32)
+    p = Pair("kivi", page_groups=8, num_pages=2 * mp + 1, block_table=table, **kw)
+    g = gen(55)
+    k, v = p.rand_kv(2, max(lens), g)
+    p.append(0, k, v, n_valid=lens)
+    del k, v
+    p.assert_same_image()
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="rope, long context, paged")
+    assert p.status() == 0
+
+
 def test_decode_schedule_total_smaller_than_the_grid():
     # a few tokens in all: most blocks of the wave get no chunk, some units get one block
     p = Pair("kivi", batch=3, q_heads=8, kv_heads=2, head_dim=64, max_tokens=64, bits=2, group_k=16,
