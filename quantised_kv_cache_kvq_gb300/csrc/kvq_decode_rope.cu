@@ -38,6 +38,25 @@ __device__ __forceinline__ int code_at(const uint8_t* p, int bit) {
 __device__ __forceinline__ float half_at(const uint8_t* p, int byte) {
     return __half2float(*reinterpret_cast<const __half*>(p + byte));
 }
+// cos and sin of a binary32 angle a.  For |a| < 2^17, Cody and Waite's reduction by 2 pi
+// in three binary32 parts (the first, 6.28125, has 8 significant bits, so k * C1 is exact
+// for the |k| < 2^15 that occur; C2 and C3 carry the rest of 2 pi), then the hardware sine
+// and cosine on the reduced |r| <= pi (absolute error about 1e-6).  Larger angles take the
+// library's sincosf with its full argument reduction.
+__device__ __forceinline__ void rope_sincos(float a, float* sn, float* cs) {
+    if (fabsf(a) < 131072.0f) {
+        constexpr float kInv2Pi = 0.159154943091895336f;
+        constexpr float C1 = 6.28125f, C2 = 1.9353072e-3f, C3 = 1.0253132e-11f;
+        const float k = rintf(a * kInv2Pi);
+        float r = fmaf(-k, C1, a);
+        r = fmaf(-k, C2, r);
+        r = fmaf(-k, C3, r);
+        __sincosf(r, sn, cs);
+    } else {
+        sincosf(a, sn, cs);
+    }
+}
+
 // Dequantised value of a code: code * scale + zero, a binary32 product, then a sum.
 __device__ __forceinline__ float dequant(int code, float s, float z) {
     return __fadd_rn(__fmul_rn(static_cast<float>(code), s), z);
@@ -133,7 +152,7 @@ __device__ int rope_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64
 #pragma unroll
             for (int j = 0; j < HP; ++j) {
                 float sn, cs;
-                sincosf(__fmul_rn(pos, a.rope_w[lane + 32 * j]), &sn, &cs);
+                rope_sincos(__fmul_rn(pos, a.rope_w[lane + 32 * j]), &sn, &cs);
                 const float x = k[j], y = k[j + HP];
                 k[j] = x * cs - y * sn;
                 k[j + HP] = y * cs + x * sn;
@@ -187,22 +206,42 @@ __device__ int rope_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64
                 for (int hh = 0; hh < 8; ++hh)
                     if (hh < gqa) o[x][hh] *= hstat[64 + hh];
                 const int jv = c / lo.Gv;
-                for (int i = 0; i < cnt; ++i) {
-                    float v;
-                    if (part == 0) {
-                        const uint8_t* rp = data + (int64_t)(i / G) * rec;
-                        const int ig = i % G;
-                        const uint8_t* vpar = rp + lo.kc + lo.vc + lo.kp;
-                        const int pb = value_param_byte(G, jv, ig);
-                        v = dequant(code_at<BITS>(rp + lo.kc, value_code_bit<D, BITS>(ig, c)), half_at(vpar, pb),
-                                    half_at(vpar, 2 * G * lo.NGv + pb));
-                    } else {
-                        v = bf16_bits_to_float(
-                            reinterpret_cast<const uint16_t*>(data + (int64_t)i * 4 * D)[D + c]);
-                    }
+                if (part == 0) {
+                    // a 16-token tile at a time: the channel's codes of tokens tt and tt + 8
+                    // share a word (value_code_bit), the tile's 16 scales (and zeros) are 32
+                    // contiguous bytes in the order 2 (tt mod 8) + tt / 8
+                    for (int i0 = 0; i0 < cnt; i0 += 16) {
+                        const uint8_t* rp = data + (int64_t)(i0 / G) * rec;
+                        const int ig0 = i0 % G;
+                        const uint8_t* vpar = rp + lo.kc + lo.vc + lo.kp + value_param_byte(G, jv, ig0);
+                        const uint4* sp = reinterpret_cast<const uint4*>(vpar);
+                        const uint4* zp = reinterpret_cast<const uint4*>(vpar + 2 * G * lo.NGv);
+                        const uint4 s0 = sp[0], s1 = sp[1], z0 = zp[0], z1 = zp[1];
+                        const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                        const uint32_t zw[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
 #pragma unroll
-                    for (int hh = 0; hh < 8; ++hh)
-                        if (hh < gqa) o[x][hh] = fmaf(sc[hh * CH + i], v, o[x][hh]);
+                        for (int e = 0; e < 8; ++e) {       // tokens tt = e and e + 8
+                            const int bit = value_code_bit<D, BITS>(ig0 + e, c);   // low half: token e
+                            const uint32_t word = *reinterpret_cast<const uint32_t*>(rp + lo.kc + 4 * (bit >> 5));
+                            const int sh = bit & 31;
+                            const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sw[e]));
+                            const float2 zf = __half22float2(*reinterpret_cast<const __half2*>(&zw[e]));
+                            const float v0 = dequant((word >> sh) & ((1u << BITS) - 1u), sf.x, zf.x);
+                            const float v1 = dequant((word >> (sh + 16)) & ((1u << BITS) - 1u), sf.y, zf.y);
+#pragma unroll
+                            for (int hh = 0; hh < 8; ++hh)
+                                if (hh < gqa)
+                                    o[x][hh] = fmaf(sc[hh * CH + i0 + e + 8], v1, fmaf(sc[hh * CH + i0 + e], v0, o[x][hh]));
+                        }
+                    }
+                } else {
+                    for (int i = 0; i < cnt; ++i) {
+                        const float v = bf16_bits_to_float(
+                            reinterpret_cast<const uint16_t*>(data + (int64_t)i * 4 * D)[D + c]);
+#pragma unroll
+                        for (int hh = 0; hh < 8; ++hh)
+                            if (hh < gqa) o[x][hh] = fmaf(sc[hh * CH + i], v, o[x][hh]);
+                    }
                 }
             }
         }
