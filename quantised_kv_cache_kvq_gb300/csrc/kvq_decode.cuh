@@ -96,6 +96,14 @@ __host__ __device__ __forceinline__ void chunks_in(int64_t base, int64_t nch, fl
     if (k_hi > nch) k_hi = nch;
 }
 
+// floor(N r / k) for chunk counts N < 2^31 and 0 <= r <= k <= 2048 in 32-bit integer
+// arithmetic, as (N / k) r + floor((N mod k) r / k) (a 64-bit division is a long
+// instruction sequence on the GPU).
+__host__ __device__ __forceinline__ int64_t share_lo(int N, int r, int k) {
+    const int q = N / k, m = N - q * k;
+    return (int64_t)q * r + (m * r) / k;
+}
+
 // Tokens n, qn of sequence b in this layer's state.
 __device__ __forceinline__ int2 seq_state(const DecodeArgs& a, int b) {
     return *reinterpret_cast<const int2*>(state_ptr(a.lo, a.cache, a.layer, b));
@@ -406,9 +414,10 @@ __device__ void for_each_segment(const DecodeArgs& a, int64_t* scratch, int2* ss
                 dead(slot0);
             return;
         }
-        const int64_t nc0 = (up.n0 + a.plan.CH - 1) / a.plan.CH, nc1 = (up.n1 + a.plan.CHR - 1) / a.plan.CHR;
-        const int64_t N = nc0 + nc1;
-        const int64_t clo = N * up.r / up.k, chi = N * (up.r + 1) / up.k;
+        const int64_t nc0 = (static_cast<int>(up.n0) + a.plan.CH - 1) / a.plan.CH;
+        const int64_t nc1 = (static_cast<int>(up.n1) + a.plan.CHR - 1) / a.plan.CHR;
+        const int N = static_cast<int>(nc0 + nc1);
+        const int64_t clo = share_lo(N, up.r, up.k), chi = share_lo(N, up.r + 1, up.k);
         bool go = true;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
@@ -508,11 +517,12 @@ __device__ inline int unit_candidates(const DecodeArgs& a, int u, int2 st, const
                 cand[i] = i < k ? static_cast<int>(2 * (K + i)) : static_cast<int>(2 * (K + k - kw + (i - k)) + 1);
             return k + kw;
         }
-        const int64_t nc0 = (n0 + a.plan.CH - 1) / a.plan.CH, nc1 = (n1 + a.plan.CHR - 1) / a.plan.CHR;
-        const int64_t N = nc0 + nc1;
+        const int64_t nc0 = (static_cast<int>(n0) + a.plan.CH - 1) / a.plan.CH;
+        const int64_t nc1 = (static_cast<int>(n1) + a.plan.CHR - 1) / a.plan.CHR;
+        const int N = static_cast<int>(nc0 + nc1);
         for (int i = tid; i < 2 * k; i += nthreads) {
             const int part = i / k, r = i - part * k;
-            const int64_t clo = N * r / k, chi = N * (r + 1) / k;
+            const int64_t clo = share_lo(N, r, k), chi = share_lo(N, r + 1, k);
             const int64_t lo_c = part ? nc0 : 0, hi_c = part ? N : nc0;
             const bool any = (clo > lo_c ? clo : lo_c) < (chi < hi_c ? chi : hi_c);
             cand[i] = any ? static_cast<int>(2 * (K + r) + part) : -1;
@@ -1135,7 +1145,7 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
 
     // the item's groups (t0 and t1 are group boundaries): chunk c holds gpc of them
     const int gpc = CH / G;
-    const uint8_t* src_groups = src_unit + (t0 / G) * (int64_t)rec;
+    const uint8_t* src_groups = src_unit + (int64_t)(static_cast<int>(t0) / G) * rec;
     const int ngroups = ntok / G;
     auto issue = [&](int c, int sj) {       // stage chunk c into stage sj (thread 0 only)
         const int gj = min(gpc, ngroups - c * gpc);
