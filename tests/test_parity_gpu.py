@@ -319,19 +319,21 @@ def test_decode_schedule_chunks_on_demand():
     # few units with long contexts: at least 4 packed chunks per block, so the blocks of a
     # unit take its chunks from a counter (the window rows first, on the last blocks); a
     # second decode checks that the merge set the counters back to zero
-    lens = [400000, 300007]
-    p = Pair("kivi", batch=2, q_heads=4, kv_heads=2, head_dim=64, max_tokens=max(lens) + 64, bits=2,
+    # (the third sequence is short: its units get a single block, which takes the window
+    # first and then every packed chunk from the counter)
+    lens = [400000, 300007, 1000]
+    p = Pair("kivi", batch=3, q_heads=4, kv_heads=2, head_dim=64, max_tokens=max(lens) + 64, bits=2,
              group_k=32, group_v=32, residual=100)
     g = gen(27)
-    k, v = p.rand_kv(2, max(lens), g)
+    k, v = p.rand_kv(3, max(lens), g)
     p.append(0, k, v, n_valid=lens)
     del k, v
     p.assert_same_image()
     for step in range(2):
         out, ref = p.decode(0, p.rand_q(g))
         assert_close(out, ref, what="chunks on demand, step %d" % step)
-        assert not p.ws[256:256 + 16].any()      # the four unit counters are back at zero
-        k, v = p.rand_kv(2, 1, g)
+        assert not p.ws[256:256 + 24].any()      # the six unit counters are back at zero
+        k, v = p.rand_kv(3, 1, g)
         p.append(0, k, v)
     assert p.status() == 0
 
