@@ -30,7 +30,13 @@
  * resident decode blocks per SM it sizes its decode grid by.  All device work is enqueued asynchronously on the caller's stream; no
  * call synchronises except kvq_read_status.  Pointers marked "device" must be device
  * (or managed) memory; the cache must be 256-byte aligned, every other device pointer
- * 16-byte aligned.
+ * 16-byte aligned.  Pointers marked "device or mapped host" may also point into
+ * page-locked host memory that is mapped into the device's address space under the same
+ * address (cudaHostAlloc, or cudaHostRegister with mapping, on a system with unified
+ * addressing), with the same alignment: the kernels then read the inputs, or write the
+ * outputs, across the host link themselves, with no copy enqueued by the library.  The
+ * caller keeps such memory unchanged (inputs) or unread (outputs) until the work on
+ * `stream` has completed.
  *
  * Errors: each call returns KVQ_OK (0) or a negative KVQ_ERR_* code for problems found
  * on the host before any work is enqueued (nothing is enqueued then).  Problems that only
@@ -187,7 +193,8 @@ int kvq_cache_init(const kvq_config* cfg, void* cache, kvq_stream_t stream);
 /*
  * kvq_quantize_append -- append new tokens' keys and values of one layer to sequences
  * [seq_begin, seq_begin + seq_count), quantising and packing them.
- *   k_new, v_new  device, [seq_count][n_new][kv_heads][head_dim] in cfg->in_dtype
+ *   k_new, v_new  device or mapped host, [seq_count][n_new][kv_heads][head_dim] in
+ *                 cfg->in_dtype
  *   n_new         tokens per sequence in the input rows (0 <= n_new <= max_tokens)
  *   n_valid       device int32 [seq_count] or NULL: sequence i appends its first
  *                 n_valid[i] rows (0..n_new), the rest of its rows are ignored
@@ -252,8 +259,9 @@ int kvq_workspace_bytes(const kvq_config* cfg, uint64_t* out_bytes);
  * one layer ("Quantizing the KV cache", "Why values per token": o = sum_t p_t V_t with
  * p = softmax over the cached tokens of softmax_scale * q . K_t).
  *   cache       device, the cache (read only)
- *   q           device, [batch][q_heads][head_dim] in cfg->in_dtype
- *   out         device fp32, [batch][q_heads][head_dim]; a sequence with no tokens gets 0
+ *   q           device or mapped host, [batch][q_heads][head_dim] in cfg->in_dtype
+ *   out         device or mapped host, fp32 [batch][q_heads][head_dim]; a sequence with
+ *               no tokens gets 0
  *   workspace   device, at least kvq_workspace_bytes bytes, whose first 4352 bytes are
  *               zero before its first decode (every decode leaves bytes 4..4351 as it
  *               found them); its first 4 bytes are the decode status word (sticky; clear

@@ -11,7 +11,7 @@ import torch
 
 import oracle as O
 import quantised_kv_cache_kvq_gb300 as K
-from harness import Pair, assert_close
+from harness import Pair, assert_close, q_as_float, to_np_input
 
 pytestmark = pytest.mark.gpu
 
@@ -508,4 +508,41 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     p.ws[:16].zero_()
     got, ref = p.decode(0, q)
     assert_close(got, ref, what="after the self-test")
+    assert p.status() == 0
+
+
+@pytest.mark.parametrize("scheme,bits,G,R", [("kivi", 2, 32, 128), ("kivi", 4, 128, 128), ("fp8", 8, 32, 0),
+                                             ("int8", 8, 32, 0)])
+def test_mapped_host_inputs_and_outputs(scheme, bits, G, R):
+    # the new tokens and the queries passed as page-locked host memory, the outputs written
+    # into page-locked host memory: the kernels move them across the host link themselves,
+    # and the cache and the outputs are those of the oracle
+    p = Pair(scheme, batch=4, q_heads=16, kv_heads=4, head_dim=128, max_tokens=3000, bits=bits, group_k=G,
+             group_v=min(G, 128), residual=R)
+    g = gen(31 + bits)
+    k, v = p.rand_kv(4, 2000, g)
+    sc = None
+    if scheme == "fp8":
+        sc = torch.stack([k.float().abs().amax(dim=(0, 1, 3)), v.float().abs().amax(dim=(0, 1, 3))], 1) / 448
+    p.append(0, k, v, n_valid=[2000, 1500, 733, 64], fp8_scales=sc)
+    sc_gpu = None if sc is None else sc.float().contiguous().cuda()
+    for step in range(G + 2):
+        k1, v1 = p.rand_kv(4, 1, g)
+        hk, hv = k1.contiguous().pin_memory(), v1.contiguous().pin_memory()
+        K.kvq_quantize_append(p.lib_cfg, p.gpu, 0, 0, 4, hk, hv, 1, None, sc_gpu, 0)
+        p.img.append(0, 0, to_np_input(k1), to_np_input(v1), None,
+                     None if sc is None else sc.float().numpy(), 0)
+        torch.cuda.synchronize()
+        if step % 11 == 0 or step == G + 1:
+            p.assert_same_image()
+            q = p.rand_q(g)
+            hq = q.contiguous().pin_memory()
+            hout = torch.full((4, 16, 128), float("nan"), dtype=torch.float32).pin_memory()
+            p.ws[:4].zero_()
+            K.kvq_decode_attention(p.lib_cfg, p.gpu, 0, hq, 1.0 / math.sqrt(128), hout, p.ws)
+            torch.cuda.synchronize()
+            ref = p.img.decode(0, q_as_float(q), 1.0 / math.sqrt(128))
+            assert_close(hout.numpy().astype(np.float64), ref, what="%s mapped step %d" % (scheme, step))
+            dev_out, _ = p.decode(0, q)
+            np.testing.assert_allclose(hout.numpy(), dev_out, rtol=1e-5, atol=1e-6)
     assert p.status() == 0
