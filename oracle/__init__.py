@@ -27,7 +27,7 @@ class OracleConfig(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "scheme", "layers", "batch", "q_heads", "kv_heads", "head_dim", "bits",
         "group_k", "group_v", "residual", "max_tokens", "in_dtype", "page_groups", "num_pages")] + [
-        ("block_table", C.c_void_p), ("rope_base", C.c_float)]
+        ("block_table", C.c_void_p), ("rope_base", C.c_float), ("outliers", C.c_int32)]
 
 
 def lib():
@@ -48,6 +48,7 @@ def lib():
             "kvqo_e5m2_from_float": (C.c_uint8, [f32]),
             "kvqo_int4_token": (None, [P, C.c_int, P, P]),
             "kvqo_qb_group": (None, [P, C.c_int, C.c_int, C.c_int, P, P, P]),
+            "kvqo_qb_group_sparse": (None, [P, C.c_int, C.c_int, C.c_int, C.c_int, P, P, P, P]),
             "kvqo_qb_dequant": (f32, [C.c_int, u16, u16]),
             "kvqo_int8_token": (None, [P, C.c_int, P, P]),
             "kvqo_image_bytes": (i64, [P]),
@@ -113,6 +114,19 @@ def qb_group(x, bits):
     return int(s[0]), int(z[0]), codes
 
 
+def qb_group_sparse(x, bits, k):
+    """Dense-and-sparse Q_b over one vector (bf16-exact float32 values): returns (scale
+    bits, zero bits, codes uint8, side entries uint32 [k])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert 0 <= k < x.size
+    s = np.zeros(1, np.uint16)
+    z = np.zeros(1, np.uint16)
+    codes = np.zeros(x.size, np.uint8)
+    ent = np.zeros(max(k, 1), np.uint32)
+    lib().kvqo_qb_group_sparse(_p(x), x.size, 1, bits, k, _p(s), _p(z), _p(codes), _p(ent))
+    return int(s[0]), int(z[0]), codes, ent[:k]
+
+
 def qb_dequant(code, scale_bits, zero_bits):
     return lib().kvqo_qb_dequant(int(code), int(scale_bits), int(zero_bits))
 
@@ -147,8 +161,12 @@ def make_config(block_table=None, **kw):
     c = OracleConfig()
     defaults = dict(scheme=0, layers=1, batch=1, q_heads=1, kv_heads=1, head_dim=64, bits=2,
                     group_k=32, group_v=32, residual=0, max_tokens=64, in_dtype=DT_BF16, page_groups=0,
-                    num_pages=0)
+                    num_pages=0, outliers=0)
     defaults.update(kw)
+    k = int(defaults["outliers"])
+    if k and not (0 < k <= 4 and k < defaults["group_k"] and k < defaults["group_v"]
+                  and defaults["scheme"] == SCHEME_KIVI):
+        raise ValueError("outliers: KIVI only, 1..4 and fewer than group_k and group_v")
     rope = float(defaults.pop("rope_base", 0.0))
     for k, v in defaults.items():
         setattr(c, k, int(v))

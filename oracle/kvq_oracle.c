@@ -17,6 +17,9 @@
  *          equation) and "Why values per token".
  *   [KIVI] "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache" summary,
  *          section "How It Works".
+ *   [KVQ]  "kv cache quantization" (the KVQuant summary), "Summary" and "Key points":
+ *          keys quantised before RoPE, and a small fraction of outliers moved, per
+ *          vector, into a separate sparse representation.
  *
  * Arithmetic contract (so that quantised codes can be compared bit for bit):
  *   - quantisation runs in IEEE binary32 with round-to-nearest-even, no contraction
@@ -54,6 +57,8 @@ typedef struct {
     const int32_t* block_table;   /* [batch][max_pages]: pool page of each page of a sequence */
     float rope_base;              /* KIVI keys cached before the rotary embedding: its base
                                      (0: keys are cached as given) */
+    int32_t outliers;             /* KIVI dense-and-sparse: elements per quantisation vector
+                                     moved to the sparse side list (0: none) */
 } kvqo_config;
 
 enum { SCHEME_KIVI = 0, SCHEME_INT8 = 1, SCHEME_FP8 = 2, SCHEME_FP8_E5M2 = 3, SCHEME_INT4 = 4 };
@@ -254,11 +259,15 @@ uint8_t kvqo_e5m2_from_float(float xf)
  * constant group (s = 0) gets all-zero codes.
  * x[i * stride], i < n; codes written one per byte.
  * ---------------------------------------------------------------------------------- */
-void kvqo_qb_group(const float* x, int n, int stride, int bits, uint16_t* scale_out,
-                   uint16_t* zero_out, uint8_t* codes)
+static void qb_fit(const float* x, int n, int stride, int bits, const unsigned char* skip,
+                   uint16_t* scale_out, uint16_t* zero_out, uint8_t* codes)
 {
-    float mn = x[0], mx = x[0];
-    for (int i = 1; i < n; i++) {
+    /* min and max over the elements not skipped (at least one is not) */
+    int first = 0;
+    while (skip && skip[first]) first++;
+    float mn = x[first * stride], mx = mn;
+    for (int i = first + 1; i < n; i++) {
+        if (skip && skip[i]) continue;
         mn = fminf(mn, x[i * stride]);
         mx = fmaxf(mx, x[i * stride]);
     }
@@ -278,10 +287,54 @@ void kvqo_qb_group(const float* x, int n, int stride, int bits, uint16_t* scale_
             if (r > (float)levels) r = (float)levels;
             code = (int)r;
         }
-        codes[i] = (uint8_t)code;
+        codes[i] = (uint8_t)((skip && skip[i]) ? 0 : code);
     }
     *scale_out = s;
     *zero_out = z;
+}
+
+void kvqo_qb_group(const float* x, int n, int stride, int bits, uint16_t* scale_out,
+                   uint16_t* zero_out, uint8_t* codes)
+{
+    qb_fit(x, n, stride, bits, NULL, scale_out, zero_out, codes);
+}
+
+/* bfloat16 bits of a binary32 value that is a bfloat16 already (KIVI inputs are) */
+static uint16_t bf16_bits_of(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------------------------------------
+ * Dense-and-sparse quantisation of one vector ([KVQ] "Summary": a small fraction of
+ * outliers is moved, per vector, into a separate sparse representation; "Key points":
+ * 1% outliers).  Reading: the vector is a quantisation vector of the Q_b rule above (a
+ * key channel over the G tokens of a group, or a token's values over one group of Gv
+ * channels); its k elements of largest magnitude leave the dense part.  Magnitude is
+ * the bfloat16 pattern with the sign cleared (an integer order: NaN above infinity);
+ * equal magnitudes go to the lower index first.  The Q_b parameters are fitted to the
+ * other n - k elements, the outliers' dense codes are 0, and side entry e (the e-th
+ * largest) is the 32-bit word (bfloat16 bits of the element << 16) | its index.  The
+ * element the cache then holds is its own bfloat16 value.  Requires 0 <= k < n.
+ * ---------------------------------------------------------------------------------- */
+void kvqo_qb_group_sparse(const float* x, int n, int stride, int bits, int k, uint16_t* scale_out,
+                          uint16_t* zero_out, uint8_t* codes, uint32_t* entries)
+{
+    unsigned char* skip = (unsigned char*)calloc((size_t)n, 1);
+    for (int e = 0; e < k; e++) {
+        int best = -1;
+        for (int i = 0; i < n; i++) {
+            if (skip[i]) continue;
+            unsigned m = bf16_bits_of(x[i * stride]) & 0x7fffu;
+            if (best < 0 || m > (bf16_bits_of(x[best * stride]) & 0x7fffu)) best = i;
+        }
+        skip[best] = 1;
+        entries[e] = ((uint32_t)bf16_bits_of(x[best * stride]) << 16) | (uint32_t)best;
+    }
+    qb_fit(x, n, stride, bits, skip, scale_out, zero_out, codes);
+    free(skip);
 }
 
 /* Dequantisation of one element: code * s + z, a binary32 multiply then a binary32 add. */
@@ -352,6 +405,13 @@ void kvqo_int4_token(const float* x, int n, float* scale_out, int8_t* codes)
  *            K params 4*D bytes: fp16 scale[D], then fp16 zero[D]
  *            V params 4*G*NGv bytes: fp16 scale[NGv][G], then fp16 zero[NGv][G], the G
  *                     tokens of a value group in tile order (see vparam_byte)
+ *            with k = outliers > 0 (dense-and-sparse, kvqo_qb_group_sparse), two side lists
+ *            of 32-bit entries follow:
+ *            K outliers 4*k*D bytes: entry [e][c] of key channel c, its index the token
+ *                     within the group
+ *            V outliers 4*k*NGv*G bytes: entry [e][j][position] of the value group j of a
+ *                     token, its index the channel within the group, the G tokens of a
+ *                     group in the tile order of the value parameters (vparam_byte / 2)
  *          then the bf16 ring: (l, b, h, slot s) holds K row[D] then V row[D], C = R + G
  *          slots; token t (qn <= t < n) sits in slot t mod C.
  *   INT8:  per (l, b, h) block over T16 = T rounded up to 16:
@@ -378,7 +438,7 @@ void kvqo_int4_token(const float* x, int n, float* scale_out, int8_t* codes)
 typedef struct {
     int64_t header, state, scales, data, ring, total;  /* byte offsets of the regions */
     int64_t unit;           /* bytes of one (l, b, h) block in the data region */
-    int64_t rec, kc, vc, kp, vp, ng, cap, ngv, t16;
+    int64_t rec, kc, vc, kp, vp, ko, vo, ng, cap, ngv, t16;
     int64_t pg, mp, page;   /* paged: group slots per page, table entries per sequence, page bytes */
 } layout_t;
 
@@ -453,7 +513,9 @@ static layout_t make_layout(const kvqo_config* c)
         L.vc = D * G * b / 8;
         L.kp = 4 * D;
         L.vp = 4 * G * L.ngv;
-        L.rec = L.kc + L.vc + L.kp + L.vp;
+        L.ko = 4 * (int64_t)c->outliers * D;
+        L.vo = 4 * (int64_t)c->outliers * L.ngv * G;
+        L.rec = L.kc + L.vc + L.kp + L.vp + L.ko + L.vo;
         L.unit = L.ng * L.rec;
         L.data = pos;
         if (c->page_groups > 0) {
@@ -577,6 +639,8 @@ static int get_bits(const uint8_t* base, int64_t bit, int bits)
 
 static void put_u16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)v; p[1] = (uint8_t)(v >> 8); }
 static uint16_t get_u16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+static void put_u32(uint8_t* p, uint32_t v) { put_u16(p, (uint16_t)v); put_u16(p + 2, (uint16_t)(v >> 16)); }
+static uint32_t get_u32(const uint8_t* p) { return (uint32_t)get_u16(p) | ((uint32_t)get_u16(p + 2) << 16); }
 
 /* one input row (K or V of sequence b, new token j, kv head h) as binary32 values */
 static void input_row(const kvqo_config* c, const void* src, int n_new, int bi, int j, int h,
@@ -593,12 +657,6 @@ static void input_row(const kvqo_config* c, const void* src, int n_new, int bi, 
     }
 }
 
-static uint16_t float_to_bf16_exact(float f)  /* inputs are bf16 already: keep the top half */
-{
-    uint32_t u;
-    memcpy(&u, &f, 4);
-    return (uint16_t)(u >> 16);
-}
 
 /* The key group starting at token t0 (G tokens) and the matching value rows, taken from
  * the ring for tokens before n and from the new input for the rest. */
@@ -631,10 +689,16 @@ static void kivi_quantise_group(const kvqo_config* c, const layout_t* L, uint8_t
     uint8_t* vcodes = rec + L->kc;
     uint8_t* kpar = rec + L->kc + L->vc;
     uint8_t* vpar = kpar + L->kp;
-    /* keys: per channel over the G tokens ([QKV] per-channel grouping, [KIVI]) */
+    uint8_t* kout = vpar + L->vp;
+    uint8_t* vout = kout + L->ko;
+    int k = c->outliers;
+    uint32_t ent[8];
+    /* keys: per channel over the G tokens ([QKV] per-channel grouping, [KIVI]), minus the
+       channel's k outliers ([KVQ]) */
     for (int ch = 0; ch < D; ch++) {
         uint16_t s, z;
-        kvqo_qb_group(K + ch, G, D, bits, &s, &z, codes);
+        kvqo_qb_group_sparse(K + ch, G, D, bits, k, &s, &z, codes, ent);
+        for (int e = 0; e < k; e++) put_u32(kout + 4 * ((int64_t)e * D + ch), ent[e]);
         put_u16(kpar + 2 * ch, s);
         put_u16(kpar + 2 * D + 2 * ch, z);
         for (int i = 0; i < G; i++) put_bits(kcodes, ((int64_t)i * D + ch) * bits, bits, codes[i]);
@@ -643,7 +707,9 @@ static void kivi_quantise_group(const kvqo_config* c, const layout_t* L, uint8_t
     for (int i = 0; i < G; i++) {
         for (int j = 0; j < ngv; j++) {
             uint16_t s, z;
-            kvqo_qb_group(V + (int64_t)i * D + (int64_t)j * Gv, Gv, 1, bits, &s, &z, codes);
+            kvqo_qb_group_sparse(V + (int64_t)i * D + (int64_t)j * Gv, Gv, 1, bits, k, &s, &z, codes, ent);
+            for (int e = 0; e < k; e++)
+                put_u32(vout + 4 * ((int64_t)e * ngv * G) + 2 * vparam_byte(G, j, i), ent[e]);
             put_u16(vpar + vparam_byte(G, j, i), s);
             put_u16(vpar + 2 * (int64_t)G * ngv + vparam_byte(G, j, i), z);
             for (int cc = 0; cc < Gv; cc++) {
@@ -728,10 +794,10 @@ uint32_t kvqo_append(const kvqo_config* c, uint8_t* img, int l, int seq_begin, i
                 for (int64_t t = (n > qn2 ? n : qn2); t < n + m; t++) {
                     uint8_t* slot = img + L.ring + (u * cap + t % cap) * 4 * D;
                     input_row(c, k_new, n_new, bi, (int)(t - n), h, row);
-                    for (int ch = 0; ch < D; ch++) put_u16(slot + 2 * ch, float_to_bf16_exact(row[ch]));
+                    for (int ch = 0; ch < D; ch++) put_u16(slot + 2 * ch, bf16_bits_of(row[ch]));
                     input_row(c, v_new, n_new, bi, (int)(t - n), h, row);
                     for (int ch = 0; ch < D; ch++)
-                        put_u16(slot + 2 * D + 2 * ch, float_to_bf16_exact(row[ch]));
+                        put_u16(slot + 2 * D + 2 * ch, bf16_bits_of(row[ch]));
                 }
             }
             s[0] = (int32_t)(n + m);
@@ -849,6 +915,19 @@ void kvqo_dequant_token(const kvqo_config* c, const uint8_t* img, int l, int b, 
                 int j = ch / Gv;
                 vout[ch] = kvqo_qb_dequant(vc, get_u16(vpar + vparam_byte(G, j, i)),
                                            get_u16(vpar + 2 * (int64_t)G * L.ngv + vparam_byte(G, j, i)));
+            }
+            /* outliers hold their own bfloat16 values ([KVQ], kvqo_qb_group_sparse) */
+            const uint8_t* kside = vpar + L.vp;
+            const uint8_t* vside = kside + L.ko;
+            for (int e = 0; e < c->outliers; e++) {
+                for (int ch = 0; ch < D; ch++) {
+                    uint32_t w = get_u32(kside + 4 * ((int64_t)e * D + ch));
+                    if ((int)(w & 0xffffu) == i) kout[ch] = bf16_to_float((uint16_t)(w >> 16));
+                }
+                for (int j = 0; j < L.ngv; j++) {
+                    uint32_t w = get_u32(vside + 4 * ((int64_t)e * L.ngv * G) + 2 * vparam_byte(G, j, i));
+                    vout[j * Gv + (int)(w & 0xffffu)] = bf16_to_float((uint16_t)(w >> 16));
+                }
             }
         } else {
             int64_t u = ((int64_t)l * c->batch + b) * c->kv_heads + h;

@@ -929,3 +929,179 @@ def test_rope_decode_is_attention_over_rotated_keys():
         p = np.exp(s - s.max(axis=1, keepdims=True))
         want = (p / p.sum(axis=1, keepdims=True)) @ vals
         assert np.allclose(out, want, rtol=1e-12, atol=1e-12), residual
+
+
+# ------------------------------------------------------------------- dense-and-sparse outliers
+# "kv cache quantization" (the KVQuant summary), "Summary": a small fraction of outliers is
+# moved, per vector, into a separate sparse representation ("Key points": 1% outliers).
+def test_sparse_qb_golden_cases():
+    rows = _golden("qb_sparse_cases.txt")
+    assert len(rows) >= 5
+    for bits, k, vals, sbits, zbits, codes, ents in rows:
+        x = np.array([float(v) for v in vals.split()], np.float32)
+        s, z, c, e = O.qb_group_sparse(x, int(bits), int(k))
+        assert (s, z) == (int(sbits, 16), int(zbits, 16)), (vals, hex(s), hex(z))
+        assert list(c) == [int(v) for v in codes.split()], vals
+        assert [int(w) for w in e] == [int(w, 16) for w in ents.split()], (vals, [hex(w) for w in e])
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_sparse_qb_is_the_dense_rule_on_what_remains(bits):
+    # brute force: the side list names the k elements of largest |x| (ties to the lower
+    # index), in that order, with their exact bf16 values; the dense part is the (pinned)
+    # Q_b rule applied to the other elements alone, and the outliers' codes are 0
+    rng = np.random.default_rng(40 + bits)
+    for kind in ("normal", "outlier", "shifted", "wide"):
+        for n in (16, 32, 128):
+            for k in (1, 2, 4):
+                x = _bf16_group(rng, n, kind)
+                if kind == "normal":
+                    x[rng.integers(0, n, 2)] = x[0]          # repeated magnitudes
+                    x[3] = -x[0]
+                s, z, c, e = O.qb_group_sparse(x, bits, k)
+                order = sorted(range(n), key=lambda i: (-abs(float(x[i])), i))[:k]
+                assert [int(w) & 0xffff for w in e] == order, (kind, n, k)
+                assert [int(w) >> 16 for w in e] == [int(v) for v in _bf16_bits(torch.tensor(x[order]).to(torch.bfloat16))]
+                rest = [i for i in range(n) if i not in order]
+                s2, z2, c2 = O.qb_group(x[rest], bits)
+                assert (s, z) == (s2, z2)
+                assert list(c[rest]) == list(c2) and not c[order].any()
+
+
+def test_sparse_qb_without_outliers_is_the_dense_rule():
+    rng = np.random.default_rng(7)
+    x = _bf16_group(rng, 32, "outlier")
+    s, z, c, e = O.qb_group_sparse(x, 2, 0)
+    assert (s, z, list(c)) == (lambda r: (r[0], r[1], list(r[2])))(O.qb_group(x, 2)) and e.size == 0
+
+
+def test_sparse_layout_golden_record():
+    cfg = O.make_config(scheme=0, batch=1, kv_heads=1, q_heads=1, head_dim=64, bits=2, group_k=16,
+                        group_v=16, residual=0, max_tokens=16, outliers=1)
+    img = O.Image(cfg)
+    t = np.arange(16)[:, None]
+    c = np.arange(64)[None, :]
+    K = ((c + t) % 4).astype(np.float32)
+    V = ((c + c // 8 + t + t // 8) % 4).astype(np.float32)
+    for ch in range(64):
+        K[ch % 16, ch] = 100 + ch
+    for tt in range(16):
+        for j in range(4):
+            V[tt, 16 * j + tt] = -50 - tt
+    kb = _bf16_bits(torch.tensor(K).to(torch.bfloat16)).reshape(1, 16, 1, 64)
+    vb = _bf16_bits(torch.tensor(V).to(torch.bfloat16)).reshape(1, 16, 1, 64)
+    assert img.append(0, 0, kb, vb) == 0
+    rec = img.buf[img.regions()["data"]:]
+    rows = _golden("layout_sparse.txt")
+    assert len(rows) >= 20
+    for off, byte in rows:
+        assert rec[int(off)] == int(byte, 16), off
+    # the dense layout plus the two side lists: 4 k D and 4 k NGv G bytes
+    assert img.regions()["unit"] == 16 * 64 * 2 // 8 * 2 + 4 * 64 + 4 * 16 * 4 + 4 * 64 + 4 * 4 * 16
+    # every element comes back: the spikes exactly, the rest as their (exact) codes
+    for tt in range(16):
+        kd, vd = img.dequant_token(0, 0, 0, tt)
+        np.testing.assert_array_equal(kd, K[tt])
+        np.testing.assert_array_equal(vd, V[tt])
+
+
+def test_sparse_cache_round_trip_and_outliers_exact():
+    # after appends (bulk, single tokens, a flush), every packed element dequantises to its
+    # own bf16 value when it is an outlier of its key channel or value group, and within
+    # half a step of its vector's (outlier-free) scale otherwise; at least k elements of
+    # every vector are exact
+    G, Gv, D, k = 16, 32, 64, 2
+    cfg = _kivi_cfg(batch=1, q_heads=2, kv_heads=1, head_dim=D, group_k=G, group_v=Gv, residual=8,
+                    max_tokens=120, bits=4, outliers=k)
+    img = O.Image(cfg)
+    g = torch.Generator().manual_seed(5)
+    kx = torch.randn(1, 90, 1, D, generator=g)
+    kx[..., 5] *= 14.0
+    kx[0, 17, 0, 9] = 300.0
+    vx = torch.randn(1, 90, 1, D, generator=g) * torch.where(torch.rand(1, 90, 1, 1, generator=g) < 0.1, 9.0, 1.0)
+    kb16, vb16 = kx.to(torch.bfloat16), vx.to(torch.bfloat16)
+    img.append(0, 0, _bf16_bits(kb16[:, :60]), _bf16_bits(vb16[:, :60]))
+    for tt in range(60, 90):
+        img.append(0, 0, _bf16_bits(kb16[:, tt:tt + 1]), _bf16_bits(vb16[:, tt:tt + 1]))
+    n, qn = img.state(0, 0)
+    assert (n, qn) == (90, 80)
+    K, Vv = kb16.float().numpy()[0, :, 0], vb16.float().numpy()[0, :, 0]
+    Kd = np.stack([img.dequant_token(0, 0, 0, t)[0] for t in range(qn)])
+    Vd = np.stack([img.dequant_token(0, 0, 0, t)[1] for t in range(qn)])
+    for g0 in range(0, qn, G):
+        for ch in range(D):
+            col, got = K[g0:g0 + G, ch], Kd[g0:g0 + G, ch]
+            order = sorted(range(G), key=lambda i: (-abs(float(col[i])), i))[:k]
+            rest = [i for i in range(G) if i not in order]
+            assert np.array_equal(got[order], col[order])
+            s, z, _ = O.qb_group(col[rest], 4)
+            assert np.all(np.abs(got[rest] - col[rest]) <= O.half_to_float(s) / 2 * (1 + 2 ** -20) + 1e-6)
+    for t in range(qn):
+        for j in range(D // Gv):
+            row, got = Vv[t, j * Gv:(j + 1) * Gv], Vd[t, j * Gv:(j + 1) * Gv]
+            order = sorted(range(Gv), key=lambda i: (-abs(float(row[i])), i))[:k]
+            rest = [i for i in range(Gv) if i not in order]
+            assert np.array_equal(got[order], row[order])
+            s, z, _ = O.qb_group(row[rest], 4)
+            assert np.all(np.abs(got[rest] - row[rest]) <= O.half_to_float(s) / 2 * (1 + 2 ** -20) + 1e-6)
+    # the window holds the newest tokens unchanged
+    for t in range(qn, n):
+        kd, vd = img.dequant_token(0, 0, 0, t)
+        np.testing.assert_array_equal(kd, K[t])
+        np.testing.assert_array_equal(vd, Vv[t])
+
+
+def test_sparse_attention_brute_force():
+    # attention written out over keys and values rebuilt here: per vector, the k largest
+    # magnitudes exact and the rest by the pinned Q_b rule on the rest ("Why values per
+    # token": o = sum_t p_t V_t over every cached token)
+    G, Gv, R, D, n, bits, k = 16, 16, 24, 64, 70, 2, 1
+    cfg = _kivi_cfg(batch=1, q_heads=4, kv_heads=2, head_dim=D, bits=bits, group_k=G, group_v=Gv,
+                    residual=R, max_tokens=96, outliers=k)
+    img = O.Image(cfg)
+    g = torch.Generator().manual_seed(33)
+    kx = torch.randn(1, n, 2, D, generator=g) * 1.5
+    kx[..., 7] *= 11.0
+    kx = kx.to(torch.bfloat16)
+    vx = (torch.randn(1, n, 2, D, generator=g) * torch.where(torch.rand(1, n, 1, 1, generator=g) < 0.05, 8.0, 1.0)).to(torch.bfloat16)
+    img.append(0, 0, _bf16_bits(kx[:, :50]), _bf16_bits(vx[:, :50]))
+    for t in range(50, n):
+        img.append(0, 0, _bf16_bits(kx[:, t:t + 1]), _bf16_bits(vx[:, t:t + 1]))
+    qn = G * ((n - R) // G)
+    kf, vf = kx.float().numpy()[0], vx.float().numpy()[0]
+    q = torch.randn(1, 4, D, generator=g).to(torch.bfloat16).float().numpy()
+    scale = 0.2
+    out = img.decode(0, q, scale)
+
+    def rebuild(vec):
+        order = sorted(range(vec.size), key=lambda i: (-abs(float(vec[i])), i))[:k]
+        rest = [i for i in range(vec.size) if i not in order]
+        s, z, codes = O.qb_group(vec[rest], bits)
+        r = np.array(vec, np.float64)
+        r[rest] = [O.qb_dequant(int(c), s, z) for c in codes]
+        return r
+
+    for hq in range(4):
+        h = hq // 2
+        K = np.array(kf[:, h], np.float64)
+        V = np.array(vf[:, h], np.float64)
+        for g0 in range(0, qn, G):
+            for ch in range(D):
+                K[g0:g0 + G, ch] = rebuild(kf[g0:g0 + G, h, ch])
+        for t in range(qn):
+            for j in range(D // Gv):
+                V[t, j * Gv:(j + 1) * Gv] = rebuild(vf[t, h, j * Gv:(j + 1) * Gv])
+        sc = [scale * sum(float(q[0, hq, i]) * K[t, i] for i in range(D)) for t in range(n)]
+        e = [math.exp(x - max(sc)) for x in sc]
+        den = sum(e)
+        ref = [sum(e[t] / den * V[t, i] for t in range(n)) for i in range(D)]
+        np.testing.assert_allclose(out[0, hq], ref, rtol=1e-11, atol=1e-13)
+
+
+def test_sparse_config_rules():
+    with pytest.raises(ValueError):
+        O.make_config(scheme=0, group_k=16, group_v=16, outliers=5)
+    with pytest.raises(ValueError):
+        O.make_config(scheme=1, outliers=1)
+    with pytest.raises(ValueError):
+        O.make_config(scheme=0, group_k=16, group_v=16, outliers=16)
