@@ -142,6 +142,16 @@ enum kvq_status_bits {
  *               each sequence.  Read by every call that reads or writes group records
  *               (appends, flushes, decodes), so the caller may hand a sequence new pages
  *               between calls; unused for the contiguous layout.
+ *   outliers    KIVI dense-and-sparse quantisation: in every quantisation vector (a key
+ *               channel over the G tokens of a group, a token's values over one group of Gv
+ *               channels) the `outliers` elements of largest magnitude are kept aside in
+ *               bf16 and the Q_b parameters are fitted to the other elements ("KVQuant:
+ *               Towards 10 Million Context Length ...", "Summary": a small fraction of
+ *               outlier values is moved, per vector, into a separate sparse representation;
+ *               "Key points": 1% outliers).  0 (plain KIVI) to 4, KIVI only.  Magnitude is
+ *               the bf16 pattern with its sign cleared, compared as an integer (a NaN ranks
+ *               above an infinity); equal magnitudes go to the lower index first.  The
+ *               outliers' dense codes are 0 and the decode uses their bf16 values.
  * Paged layout ("KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache", "Key
  * Takeaways for Interviews": KIVI pairs with PagedAttention, whose fixed-size pages are
  * found through a per-sequence block table): the packed group records live in a pool of
@@ -169,6 +179,7 @@ typedef struct kvq_config {
     int32_t num_pages;
     const int32_t* block_table;
     float rope_base;
+    int32_t outliers;
 } kvq_config;
 
 /*

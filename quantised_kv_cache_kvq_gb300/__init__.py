@@ -24,9 +24,10 @@ _SCHEMES = {"kivi": KVQ_SCHEME_KIVI, "int8": KVQ_SCHEME_INT8, "fp8": KVQ_SCHEME_
 
 def make_config(scheme, layers, batch, q_heads, kv_heads, head_dim, max_tokens, bits=None,
                 group_k=32, group_v=32, residual=0, in_dtype="bf16", page_groups=0, num_pages=0,
-                block_table=None, rope_base=0.0) -> KvqConfig:
+                block_table=None, rope_base=0.0, outliers=0) -> KvqConfig:
     """block_table: paged KIVI layout, a device int32 tensor [batch][max_pages]; rope_base:
-    KIVI keys cached before the rotary embedding (its base; 0 for keys cached as given)."""
+    KIVI keys cached before the rotary embedding (its base; 0 for keys cached as given);
+    outliers: KIVI dense-and-sparse, elements per quantisation vector kept aside in bf16."""
     s = _SCHEMES[scheme] if isinstance(scheme, str) else int(scheme)
     if bits is None:
         bits = {KVQ_SCHEME_KIVI: 2, KVQ_SCHEME_INT4: 4}.get(s, 8)
@@ -37,6 +38,7 @@ def make_config(scheme, layers, batch, q_heads, kv_heads, head_dim, max_tokens, 
     c.in_dtype = KVQ_DTYPE_BF16 if in_dtype in ("bf16", KVQ_DTYPE_BF16) else KVQ_DTYPE_F32
     c.page_groups, c.num_pages = page_groups, num_pages
     c.rope_base = float(rope_base)
+    c.outliers = int(outliers)
     c.set_block_table(block_table)
     return c
 

@@ -31,7 +31,7 @@ class KvqConfig(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "scheme", "layers", "batch", "q_heads", "kv_heads", "head_dim", "bits", "group_k",
         "group_v", "residual", "max_tokens", "in_dtype", "page_groups", "num_pages")] + [
-        ("block_table", C.c_void_p), ("rope_base", C.c_float)]
+        ("block_table", C.c_void_p), ("rope_base", C.c_float), ("outliers", C.c_int32)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

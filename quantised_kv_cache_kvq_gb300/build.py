@@ -35,6 +35,12 @@ UNITS = {
     "kvq_decode_kivi2_paged_steal.cu": [],
     "kvq_decode_kivi4_paged_steal.cu": [],
     "kvq_decode_kivi8_paged_steal.cu": [],
+    "kvq_decode_kivi2_sparse.cu": [],
+    "kvq_decode_kivi4_sparse.cu": [],
+    "kvq_decode_kivi8_sparse.cu": [],
+    "kvq_decode_kivi2_sparse_paged.cu": [],
+    "kvq_decode_kivi4_sparse_paged.cu": [],
+    "kvq_decode_kivi8_sparse_paged.cu": [],
     "kvq_decode_rows.cu": [],
     "kvq_decode_fp8.cu": [],
     "kvq_decode_rope.cu": [],

@@ -57,7 +57,11 @@ int make_layout(const kvq_config* c, int64_t max_tokens, Layout* out) {
         lo.vc = D * lo.G * lo.bits / 8;
         lo.kp = 4 * D;
         lo.vp = 4 * lo.G * lo.NGv;
-        lo.rec = lo.kc + lo.vc + lo.kp + lo.vp;
+        if (c->outliers < 0 || c->outliers > 4) return KVQ_ERR_ARG;
+        lo.K = c->outliers;
+        lo.ko = 4 * lo.K * D;
+        lo.vo = 4 * lo.K * lo.NGv * lo.G;
+        lo.rec = lo.kc + lo.vc + lo.kp + lo.vp + lo.ko + lo.vo;
         lo.unit = (int64_t)lo.NG * lo.rec;
         lo.data_off = pos;
         if (c->page_groups > 0) {
@@ -77,6 +81,7 @@ int make_layout(const kvq_config* c, int64_t max_tokens, Layout* out) {
     } else {
         if (c->page_groups > 0) return KVQ_ERR_UNSUPPORTED;   // pages hold KIVI group records
         if (c->rope_base > 0.0f) return KVQ_ERR_UNSUPPORTED;  // pre-RoPE keys: KIVI caches
+        if (c->outliers != 0) return KVQ_ERR_UNSUPPORTED;     // dense-and-sparse: KIVI caches
         if (!pow2_in(D, 32, 256)) return KVQ_ERR_UNSUPPORTED;
         if (is_rows(c->scheme)) {
             lo.unit = (int64_t)lo.T16 * ((c->scheme == KVQ_SCHEME_INT8 ? 2 * D : D) + 8);

@@ -140,20 +140,63 @@ __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int 
     }
     __syncthreads();
     // keys: one thread per channel, statistics over the G tokens of the group
-    for (int c = threadIdx.x; c < D; c += blockDim.x) {
-        float mn = bf16_bits_to_float(ks[c]), mx = mn;
-        bad |= nonfinite(mn);
-        for (int i = 1; i < G; ++i) {
-            const float x = bf16_bits_to_float(ks[i * D + c]);
-            bad |= nonfinite(x);
-            mn = fminf(mn, x);
-            mx = fmaxf(mx, x);
+    if (lo.K == 0) {
+        for (int c = threadIdx.x; c < D; c += blockDim.x) {
+            float mn = bf16_bits_to_float(ks[c]), mx = mn;
+            bad |= nonfinite(mn);
+            for (int i = 1; i < G; ++i) {
+                const float x = bf16_bits_to_float(ks[i * D + c]);
+                bad |= nonfinite(x);
+                mn = fminf(mn, x);
+                mx = fmaxf(mx, x);
+            }
+            QbParams p = qb_params(mn, mx, flevels);
+            kpar[c] = p.s;
+            kpar[D + c] = p.z;
+            for (int i = 0; i < G; ++i)
+                codes[i * D + c] = static_cast<uint8_t>(qb_code(bf16_bits_to_float(ks[i * D + c]), p, levels));
         }
-        QbParams p = qb_params(mn, mx, flevels);
-        kpar[c] = p.s;
-        kpar[D + c] = p.z;
-        for (int i = 0; i < G; ++i)
-            codes[i * D + c] = static_cast<uint8_t>(qb_code(bf16_bits_to_float(ks[i * D + c]), p, levels));
+    } else {
+        // dense-and-sparse ("KVQuant ...", "Summary"): the channel's K elements of largest
+        // magnitude (bf16 pattern without its sign, as an integer; the lower token first on
+        // equal magnitudes) go to the side list, entry e the e-th largest; the Q_b
+        // parameters are fitted to the other G - K tokens and the outliers' codes are 0.
+        // The channel's column of `codes` marks the chosen tokens (1) while selecting.
+        uint32_t* kside = reinterpret_cast<uint32_t*>(rec + lo.kc + lo.vc + lo.kp + lo.vp);
+        for (int c = threadIdx.x; c < D; c += blockDim.x) {
+            for (int i = 0; i < G; ++i) codes[i * D + c] = 0;
+            for (int e = 0; e < lo.K; ++e) {
+                int best = -1;
+                uint32_t bm = 0;
+                for (int i = 0; i < G; ++i) {
+                    if (codes[i * D + c]) continue;
+                    const uint32_t m = ks[i * D + c] & 0x7fffu;
+                    if (best < 0 || m > bm) {
+                        best = i;
+                        bm = m;
+                    }
+                }
+                codes[best * D + c] = 1;
+                kside[e * D + c] = (static_cast<uint32_t>(ks[best * D + c]) << 16) | static_cast<uint32_t>(best);
+            }
+            float mn = 0.0f, mx = 0.0f;
+            bool first = true;      // min and max start at the first element kept
+            for (int i = 0; i < G; ++i) {
+                const float x = bf16_bits_to_float(ks[i * D + c]);
+                bad |= nonfinite(x);
+                if (codes[i * D + c]) continue;
+                mn = first ? x : fminf(mn, x);
+                mx = first ? x : fmaxf(mx, x);
+                first = false;
+            }
+            QbParams p = qb_params(mn, mx, flevels);
+            kpar[c] = p.s;
+            kpar[D + c] = p.z;
+            for (int i = 0; i < G; ++i)
+                codes[i * D + c] = codes[i * D + c]
+                                       ? 0
+                                       : static_cast<uint8_t>(qb_code(bf16_bits_to_float(ks[i * D + c]), p, levels));
+        }
     }
     __syncthreads();
     // pack token-major: code index i*D + c at bit (i*D + c)*bits, 16-byte stores
@@ -176,10 +219,38 @@ __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int 
         const int lpg = Gv / cpl;             // lanes per value group
         for (int i = warp; i < G; i += blockDim.x / 32) {
             float x[8];
+            const int gv = (lane * cpl) / Gv;
+            // scale[gv][G] then zero[gv][G], tokens of a 16-token tile in the order 0, 8, 1, 9, ...
+            const int tt = i % 16, pos = gv * G + (i - tt) + 2 * (tt % 8) + tt / 8;
+            // dense-and-sparse: the group's K elements of largest magnitude leave the dense
+            // part (bit e of `skip`: the lane's element e), chosen by K rounds of a shuffle
+            // maximum over the group's lanes of (magnitude, lower channel first)
+            uint32_t skip = 0;
+            for (int r = 0; r < lo.K; ++r) {
+                uint32_t key = 0;
+                for (int e = 0; e < cpl; ++e) {
+                    if (skip & (1u << e)) continue;
+                    const uint32_t ch = (lane * cpl + e) % Gv;
+                    const uint32_t k = ((static_cast<uint32_t>(vs[i * D + lane * cpl + e]) & 0x7fffu) << 16) |
+                                       (0xffffu - ch);
+                    key = k > key ? k : key;
+                }
+                uint32_t best = key;
+                for (int off = 1; off < lpg; off <<= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, off));
+                const int ch = static_cast<int>(0xffffu - (best & 0xffffu));
+                const int owner = ch / cpl, e = ch % cpl;      // lane (within the group) and element
+                if (lane % lpg == owner) {
+                    skip |= 1u << e;
+                    uint32_t* vside = reinterpret_cast<uint32_t*>(rec + lo.kc + lo.vc + lo.kp + lo.vp + lo.ko);
+                    vside[r * lo.NGv * G + pos] =
+                        (static_cast<uint32_t>(vs[i * D + lane * cpl + e]) << 16) | static_cast<uint32_t>(ch);
+                }
+            }
             float mn = INFINITY, mx = -INFINITY;
             for (int e = 0; e < cpl; ++e) {
                 x[e] = bf16_bits_to_float(vs[i * D + lane * cpl + e]);
                 bad |= nonfinite(x[e]);
+                if (skip & (1u << e)) continue;
                 mn = fminf(mn, x[e]);
                 mx = fmaxf(mx, x[e]);
             }
@@ -188,17 +259,14 @@ __device__ uint32_t quantise_group(const Layout& lo, uint8_t* cache, int l, int 
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
             }
             QbParams p = qb_params(mn, mx, flevels);
-            const int gv = (lane * cpl) / Gv;
             if ((lane % lpg) == 0) {
-                // scale[gv][G] then zero[gv][G], tokens of a 16-token tile in the order
-                // 0, 8, 1, 9, ...
-                const int tt = i % 16, pos = gv * G + (i - tt) + 2 * (tt % 8) + tt / 8;
                 vpar[pos] = p.s;
                 vpar[G * lo.NGv + pos] = p.z;
             }
             // channel-major staging: code of (channel c, token i) at c*G + i
             for (int e = 0; e < cpl; ++e)
-                codes[(lane * cpl + e) * G + i] = static_cast<uint8_t>(qb_code(x[e], p, levels));
+                codes[(lane * cpl + e) * G + i] =
+                    (skip & (1u << e)) ? 0 : static_cast<uint8_t>(qb_code(x[e], p, levels));
         }
     }
     __syncthreads();

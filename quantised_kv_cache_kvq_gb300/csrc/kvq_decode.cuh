@@ -1110,7 +1110,7 @@ __device__ __forceinline__ uint32_t split_mul(__half2 s, uint32_t x, uint32_t y)
 // largest value scale seen so far times 2^Ev is below 2^15 (lowered, and what was
 // accumulated rescaled by the exact power of two, when a larger scale arrives); the code
 // position p is fixed per accumulator element, so 2^(24 - p) is applied at the end.
-template <int D, int BITS, int NT, bool STEAL, bool PAGED>
+template <int D, int BITS, int NT, bool STEAL, bool PAGED, bool SPARSE>
 __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64_t slot,
                                         int64_t t0, int64_t t1, uint32_t phase, const StealCtx& sc) {
     const SmemOffsets so = decode_smem(a.lo, a.plan);
@@ -1322,6 +1322,12 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
         for (int mt = 0; mt < MTV; ++mt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.0f;
     }
     int Ev = 15;
+    // dense-and-sparse records: the value outliers' corrections p' (x - zero) are summed per
+    // warp in shared memory [head][D], in the units (and under the rescales) of oacc
+    float* ocw = reinterpret_cast<float*>(smem + so.oc) + warp * gqa * D;
+    if constexpr (SPARSE) {
+        for (int x = lane; x < gqa * D; x += 32) ocw[x] = 0.0f;
+    }
     // the warp's tokens start W * warp tokens into every chunk: group g0 of the chunk's
     // records, offset ti0 in it (a group may be shared by two warps)
     const int g0 = (warp * W) / G, ti0 = (warp * W) % G;
@@ -1467,6 +1473,42 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
                     ++grp;
                 }
             }
+            if constexpr (SPARSE) {
+                // key outliers of the warp's tokens: their dense code 0 scored q_c zero_c, the
+                // element is x, so s[t][head] += qs[head][c] (x - zero_c); several outliers of
+                // one token meet in one score, hence the shared-memory atomics
+                __syncwarp();
+                float* wsc0 = reinterpret_cast<float*>(smem + so.sc) + (int64_t)warp * MAXT * NT * 32 * 2;
+                const uint8_t* rp = smem + so.data + sj * stage_bytes + (int64_t)g0 * rec;
+                for (int r = 0; r < ngrp; ++r, rp += rec) {
+                    const uint32_t* side = reinterpret_cast<const uint32_t*>(rp + lo.kc + lo.vc + lo.kp + lo.vp);
+                    const __half* kz = reinterpret_cast<const __half*>(rp + kpar + 2 * D);
+                    for (int x = lane; x < lo.K * D; x += 32) {
+                        const uint32_t w = side[x];
+                        const int c = x & (D - 1);
+                        const int wt = r * G + static_cast<int>(w & 0xffffu) - ti0;   // warp token
+                        if (wt < 0 || wt >= wtok) continue;
+                        const float d = __fsub_rn(bf16_bits_to_float(static_cast<uint16_t>(w >> 16)), __half2float(kz[c]));
+                        const int it = wt >> 4, tt = wt & 15;
+                        float* dst = wsc0 + 2 * ((it * NT) * 32 + (tt & 7) * 4) + (tt >> 3);
+#pragma unroll
+                        for (int hh = 0; hh < NT * 4; ++hh)
+                            if (hh < gqa) atomicAdd(dst + 2 * ((hh >> 2) * 32 + (hh & 3)), qs[hh * D + c] * d);
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    cmax[nt] = -INFINITY;
+                    for (int it = 0; it < ntl; ++it) {
+                        const float2 v = wsc[(it * NT + nt) * 32];
+                        cmax[nt] = fmaxf(cmax[nt], fmaxf(v.x, v.y));
+                    }
+                }
+            }
+            float ocf[NT];          // rescale factor of this chunk for the value corrections
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) ocf[nt] = 1.0f;
             // value-scale exponent: the largest value scale of the records the warp's tokens
             // lie in must stay below 2^(15 - Ev); lower Ev (and rescale) when it does not
             {
@@ -1497,6 +1539,7 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
                         for (int mt = 0; mt < MTV; ++mt)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) oacc[mt][nt][e] *= f;
+                        ocf[nt] = f;
                     }
                     Ev = en;
                 }
@@ -1520,11 +1563,24 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
                     for (int mt = 0; mt < MTV; ++mt)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) oacc[mt][nt][e] *= alpha;
+                    ocf[nt] *= alpha;
                 }
                 mrun[nt] = mnew;
                 // p' = 2^(s - max + Ev): the value operand's power-of-two scale, applied
                 // in the exponent
                 mE[nt] = mnew - static_cast<float>(Ev);
+            }
+            if constexpr (SPARSE) {
+                // the value corrections follow oacc's rescales (lanes g of a head: channels
+                // g + 8 x)
+                __syncwarp();
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int head = 4 * nt + tig;
+                    if (ocf[nt] != 1.0f && head < gqa)
+                        for (int x = g; x < D; x += 8) ocw[head * D + x] *= ocf[nt];
+                }
+                __syncwarp();
             }
             // ---- pass 2: p' and the value contraction, tile by tile; the value-group
             // size is a template parameter so the per-group operand rebuilds unroll
@@ -1545,6 +1601,29 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
                             const float p0 = fast_exp2(sv.x - mE[nt]);
                             const float p1 = fast_exp2(sv.y - mE[nt]);
                             lrun[nt] += p0 + p1;
+                            if constexpr (SPARSE) {
+                                // value outliers of this lane's tokens g and g + 8 (side-list
+                                // positions 2g and 2g + 1 of the tile, like their zeros): the
+                                // dense code 0 gave zero, the element is x
+                                const int head = 4 * nt + tig;
+                                if (head < gqa) {
+                                    for (int jv = 0; jv < NGv; ++jv) {
+                                        const uint32_t zw = lds32(ro + vpar + 2 * G * NGv + 2 * (jv * G + ti) + 4 * g);
+                                        const float2 zf = __half22float2(u32_as_h2(zw));
+                                        for (int e = 0; e < lo.K; ++e) {
+                                            const uint2 w2 = lds64(ro + vpar + lo.vp + lo.ko +
+                                                                   4 * (e * NGv * G + jv * G + ti) + 8 * g);
+                                            const float d0 = __fsub_rn(bf16_bits_to_float(static_cast<uint16_t>(w2.x >> 16)), zf.x);
+                                            const float d1 = __fsub_rn(bf16_bits_to_float(static_cast<uint16_t>(w2.y >> 16)), zf.y);
+                                            // (the index is masked into the group: a record read
+                                            // through a bad page cannot write past the buffer)
+                                            const int gm = lo.Gv - 1;
+                                            atomicAdd(ocw + head * D + jv * lo.Gv + (static_cast<int>(w2.x) & gm), p0 * d0);
+                                            atomicAdd(ocw + head * D + jv * lo.Gv + (static_cast<int>(w2.y) & gm), p1 * d1);
+                                        }
+                                    }
+                                }
+                            }
                             // p' as fp16 major + minor, moved to the lanes of the value fragment
                             const __half2 pa = __floats2half2_rn(p0, p1);
                             const float2 pf = __half22float2(pa);
@@ -1651,6 +1730,7 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
     float* cw = comb + warp * gqa * D;
     const bool wlive = mrun[0] > -INFINITY;
     const float zfac = exp2i(-Ev), lfac = exp2i(-Ev);
+    if constexpr (SPARSE) __syncwarp();     // every lane's value corrections have landed
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int head = 4 * nt + tig;
@@ -1669,8 +1749,14 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
             const float f0 = exp2i(24 - code_pos<BITS>(m0) - Ev), f1 = exp2i(24 - code_pos<BITS>(m0 + 1) - Ev);
             if (head < gqa && wlive) {
                 const int c0 = 16 * mt + g;
-                cw[head * D + c0] = fmaf(oacc[mt][nt][0] + oacc[mt][nt][1], f0, oz);
-                cw[head * D + c0 + 8] = fmaf(oacc[mt][nt][2] + oacc[mt][nt][3], f1, oz);
+                float o0 = fmaf(oacc[mt][nt][0] + oacc[mt][nt][1], f0, oz);
+                float o1 = fmaf(oacc[mt][nt][2] + oacc[mt][nt][3], f1, oz);
+                if constexpr (SPARSE) {
+                    o0 = fmaf(ocw[head * D + c0], zfac, o0);
+                    o1 = fmaf(ocw[head * D + c0 + 8], zfac, o1);
+                }
+                cw[head * D + c0] = o0;
+                cw[head * D + c0 + 8] = o1;
             }
         }
         if (g == 0 && head < gqa) {
@@ -1687,7 +1773,7 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
 // BITS == 0: no packed part (INT8 rows).  STEAL: units may share their packed chunks on
 // demand (a separate instantiation: the extra code slows the kernels that never use it).
 // PAGED: the group records are found through the block table (paged layout).
-template <int D, int BITS, int NT, bool STEAL, bool PAGED>
+template <int D, int BITS, int NT, bool STEAL, bool PAGED, bool SPARSE = false>
 __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
     k_decode(const __grid_constant__ DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1707,7 +1793,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
             int r;
             if constexpr (BITS != 0) {
                 if (part == 0)
-                    r = packed_item<D, BITS, NT, STEAL, PAGED>(a, smem, b, h, slot, t0, t1, phase, sc);
+                    r = packed_item<D, BITS, NT, STEAL, PAGED, SPARSE>(a, smem, b, h, slot, t0, t1, phase, sc);
                 else
                     r = window_item<D, NT>(a, smem, b, h, slot, t0, t1, phase);
             } else {
@@ -1765,28 +1851,30 @@ int launch_wave(K fn, DecodeArgs& a, cudaStream_t stream) {
 // KIVI variants beyond the base kernel, each family in translation units of its own (so
 // the builds run in parallel): on demand (STEAL), paged layout (PAGED) and both.  The
 // paged fixed-split kernel plans its own wave (it is the paged fallback).
-template <int D, int BITS, int NT, bool STEAL, bool PAGED>
+// SPARSE: dense-and-sparse records (side lists of outliers); these kernels use the fixed
+// split and plan their own wave.
+template <int D, int BITS, int NT, bool STEAL, bool PAGED, bool SPARSE>
 int launch_kivi_variant(DecodeArgs& a, cudaStream_t stream) {
-    if constexpr (PAGED && !STEAL) {   // the fixed split, on the paged kernel's own wave
-        const int rc = plan_wave(k_decode<D, BITS, NT, false, true>, a);
+    if constexpr ((PAGED || SPARSE) && !STEAL) {   // the fixed split, on the kernel's own wave
+        const int rc = plan_wave(k_decode<D, BITS, NT, false, PAGED, SPARSE>, a);
         if (rc != KVQ_OK) return rc;
         a.plan.steal = 0;
     }
-    return launch_on_wave(k_decode<D, BITS, NT, STEAL, PAGED>, a, stream);
+    return launch_on_wave(k_decode<D, BITS, NT, STEAL, PAGED, SPARSE>, a, stream);
 }
-template <int BITS, bool STEAL, bool PAGED>
+template <int BITS, bool STEAL, bool PAGED, bool SPARSE = false>
 int launch_kivi_family(DecodeArgs& a, cudaStream_t stream) {
     const bool wide = a.lo.gqa > 4;
     switch (a.lo.D) {
         case 64:
-            return wide ? launch_kivi_variant<64, BITS, 2, STEAL, PAGED>(a, stream)
-                        : launch_kivi_variant<64, BITS, 1, STEAL, PAGED>(a, stream);
+            return wide ? launch_kivi_variant<64, BITS, 2, STEAL, PAGED, SPARSE>(a, stream)
+                        : launch_kivi_variant<64, BITS, 1, STEAL, PAGED, SPARSE>(a, stream);
         case 128:
-            return wide ? launch_kivi_variant<128, BITS, 2, STEAL, PAGED>(a, stream)
-                        : launch_kivi_variant<128, BITS, 1, STEAL, PAGED>(a, stream);
+            return wide ? launch_kivi_variant<128, BITS, 2, STEAL, PAGED, SPARSE>(a, stream)
+                        : launch_kivi_variant<128, BITS, 1, STEAL, PAGED, SPARSE>(a, stream);
         case 256:
-            return wide ? launch_kivi_variant<256, BITS, 2, STEAL, PAGED>(a, stream)
-                        : launch_kivi_variant<256, BITS, 1, STEAL, PAGED>(a, stream);
+            return wide ? launch_kivi_variant<256, BITS, 2, STEAL, PAGED, SPARSE>(a, stream)
+                        : launch_kivi_variant<256, BITS, 1, STEAL, PAGED, SPARSE>(a, stream);
         default: return KVQ_ERR_UNSUPPORTED;
     }
 }
@@ -1799,6 +1887,12 @@ int launch_decode_kivi8_paged(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi2_paged_steal(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi4_paged_steal(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi8_paged_steal(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi2_sparse(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi4_sparse(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi8_sparse(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi2_sparse_paged(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi4_sparse_paged(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi8_sparse_paged(DecodeArgs& a, cudaStream_t stream);
 
 // The base kernel sizes the wave; paged caches and on-demand splits go to their variants.
 template <int D, int BITS, int NT>

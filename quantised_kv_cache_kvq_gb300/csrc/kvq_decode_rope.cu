@@ -7,7 +7,9 @@
 // cores like the INT8 rows: a warp per token for the scores (lanes over channels; channel
 // c = lane + 32 j and its partner c + D/2 sit in the same lane), a thread per channel for the
 // values, and a running softmax across the run's chunks.  The split, the partial-result
-// slots and the merge are the KIVI decode's.
+// slots and the merge are the KIVI decode's.  Dense-and-sparse records (outliers kept aside
+// in bf16, "Summary" of the same page) are read element by element here: an outlier's
+// side entry replaces its dequantised value before the rotation.
 #include "kvq_decode.cuh"
 
 namespace kvq {
@@ -143,6 +145,18 @@ __device__ int rope_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64
                     k[j] = dequant(code_at<BITS>(rp, (ig * D + c) * BITS), half_at(kpar, 2 * c),
                                    half_at(kpar, 2 * D + 2 * c));
                 }
+                // dense-and-sparse records: a key outlier of this token holds its bf16 value
+                // (side entry [e][c]: bf16 bits << 16 | token in the group)
+                if (lo.K > 0) {
+                    const uint32_t* side = reinterpret_cast<const uint32_t*>(kpar + lo.kp + lo.vp);
+                    for (int e = 0; e < lo.K; ++e) {
+#pragma unroll
+                        for (int j = 0; j < CPL; ++j) {
+                            const uint32_t w = side[e * D + lane + 32 * j];
+                            if (static_cast<int>(w & 0xffffu) == ig) k[j] = bf16_bits_to_float(static_cast<uint16_t>(w >> 16));
+                        }
+                    }
+                }
             } else {
                 const uint16_t* row = reinterpret_cast<const uint16_t*>(data + (int64_t)i * 4 * D);
 #pragma unroll
@@ -226,8 +240,21 @@ __device__ int rope_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64
                             const int sh = bit & 31;
                             const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sw[e]));
                             const float2 zf = __half22float2(*reinterpret_cast<const __half2*>(&zw[e]));
-                            const float v0 = dequant((word >> sh) & ((1u << BITS) - 1u), sf.x, zf.x);
-                            const float v1 = dequant((word >> (sh + 16)) & ((1u << BITS) - 1u), sf.y, zf.y);
+                            float v0 = dequant((word >> sh) & ((1u << BITS) - 1u), sf.x, zf.x);
+                            float v1 = dequant((word >> (sh + 16)) & ((1u << BITS) - 1u), sf.y, zf.y);
+                            if (lo.K > 0) {
+                                // value outliers of tokens e and e + 8 (side positions 2e and
+                                // 2e + 1 of the tile): index = channel within the value group
+                                const uint32_t* side = reinterpret_cast<const uint32_t*>(
+                                    rp + lo.kc + lo.vc + lo.kp + lo.vp + lo.ko);
+                                const int base = jv * G + ig0 + 2 * e, cg = c - jv * lo.Gv;
+                                for (int ee = 0; ee < lo.K; ++ee) {
+                                    const uint32_t w0 = side[ee * lo.NGv * G + base];
+                                    const uint32_t w1 = side[ee * lo.NGv * G + base + 1];
+                                    if (static_cast<int>(w0 & 0xffffu) == cg) v0 = bf16_bits_to_float(static_cast<uint16_t>(w0 >> 16));
+                                    if (static_cast<int>(w1 & 0xffffu) == cg) v1 = bf16_bits_to_float(static_cast<uint16_t>(w1 >> 16));
+                                }
+                            }
 #pragma unroll
                             for (int hh = 0; hh < 8; ++hh)
                                 if (hh < gqa)

@@ -228,6 +228,11 @@ int launch_decode(const Layout& lo, const DecodePlan& plan, const uint8_t* cache
         for (int i = 0; i < lo.D / 2; ++i)
             a.rope_w[i] = static_cast<float>(std::pow(static_cast<double>(lo.rope_base), -2.0 * i / lo.D));
         rc = launch_decode_rope(a, stream);
+    } else if (lo.scheme == KVQ_SCHEME_KIVI && lo.K > 0) {
+        // dense-and-sparse records: the kernels that add the outliers' corrections
+        rc = lo.bits == 2 ? launch_decode_kivi2_sparse(a, stream)
+           : lo.bits == 4 ? launch_decode_kivi4_sparse(a, stream)
+                          : launch_decode_kivi8_sparse(a, stream);
     } else if (lo.scheme == KVQ_SCHEME_KIVI) {
         rc = lo.bits == 2 ? launch_decode_kivi2(a, stream)
            : lo.bits == 4 ? launch_decode_kivi4(a, stream)

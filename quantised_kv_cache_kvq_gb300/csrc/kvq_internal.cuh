@@ -20,6 +20,12 @@
 //              K params 4*D B: fp16 scale[D] then fp16 zero[D] (per channel, "min")
 //              V params 4*G*(D/Gv) B: fp16 scale[D/Gv][G] then fp16 zero[D/Gv][G], tile
 //                       token tt of a group's row at position 2 (tt mod 8) + tt / 8
+//              with K = outliers > 0 (dense-and-sparse), two side lists of 32-bit entries
+//              (bf16 bits of the element << 16 | its index in the vector), the e-th
+//              largest magnitude first:
+//              K side   4*K*D B: entry [e][c] of key channel c (index: token in the group)
+//              V side   4*K*(D/Gv)*G B: entry [e][j][position] of value group j of a token
+//                       (index: channel in the group), positions as the V params
 //            Paged layout (page_groups PG > 0): the records live in a pool of NP pages of
 //            L * H * PG records; record (l, b, h, g) is record (l * H + h) * PG + g mod PG
 //            of page block_table[b * MP + g / PG], MP = ceil(NG / PG).
@@ -53,6 +59,7 @@ struct Layout {
     int64_t state_off, scales_off, data_off, ring_off, total;
     int64_t unit;                    // bytes of one (layer, sequence, kv head) data block
     int32_t rec, kc, vc, kp, vp;     // KIVI record: total, K codes, V codes, K params, V params
+    int32_t K, ko, vo;               // KIVI dense-and-sparse: outliers per vector, K and V side lists
     int32_t PG, NP, MP;              // paged layout: records per page and sequence, pages, table row
     int64_t page;                    // paged layout: bytes of a page
     const int32_t* table;            // paged layout: the block table (device)
@@ -96,7 +103,7 @@ struct DecodePlan {
 
 // Shared-memory carve of the decode block, identical on host and device.
 struct SmemOffsets {
-    int64_t bar, red, hstat, sst, qs, qpa, qpb, pw, sc, data, total;
+    int64_t bar, red, hstat, sst, qs, qpa, qpb, pw, sc, oc, data, total;
 };
 __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const DecodePlan& p) {
     SmemOffsets o;
@@ -119,6 +126,8 @@ __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const Decod
         big = big > wsc ? big : wsc;
         off += 4 * big;
     }
+    o.oc = off;                                          // dense-and-sparse: per-warp value
+    if (lo.K > 0) off += (int64_t)4 * lo.gqa * lo.D * 4;    // corrections [warp][head][D]
     off = (off + 127) / 128 * 128;
     o.data = off;
     int64_t rows = 0, packed = 0;

@@ -30,13 +30,13 @@ def q_as_float(q: torch.Tensor) -> np.ndarray:
 class Pair:
     def __init__(self, scheme="kivi", layers=1, batch=2, q_heads=8, kv_heads=2, head_dim=128,
                  max_tokens=256, bits=2, group_k=32, group_v=32, residual=32, in_dtype="bf16",
-                 page_groups=0, num_pages=0, block_table=None, rope_base=0.0):
+                 page_groups=0, num_pages=0, block_table=None, rope_base=0.0, outliers=0):
         sch = {"kivi": 0, "int8": 1, "fp8": 2, "fp8e5m2": 3, "int4": 4}[scheme]
         dt = 0 if in_dtype == "bf16" else 1
         self.kw = dict(scheme=sch, layers=layers, batch=batch, q_heads=q_heads, kv_heads=kv_heads,
                        head_dim=head_dim, bits=bits if sch == 0 else (4 if sch == 4 else 8), group_k=group_k,
                        group_v=group_v, residual=residual, max_tokens=max_tokens, in_dtype=dt,
-                       page_groups=page_groups, num_pages=num_pages)
+                       page_groups=page_groups, num_pages=num_pages, outliers=outliers)
         self.lib_cfg = K.KvqConfig(**self.kw)
         self.lib_cfg.rope_base = rope_base
         self.kw["rope_base"] = rope_base

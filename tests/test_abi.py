@@ -74,6 +74,10 @@ def test_formula_mode_reproduces_the_pages_numbers():
     dict(bits=4, group_k=128, group_v=128, max_tokens=20000, page_groups=1, num_pages=300, layers=3),
     dict(residual=0, max_tokens=10, page_groups=3, num_pages=1),
     dict(rope_base=500000.0),                                # pre-RoPE keys change no byte of the layout
+    dict(outliers=1),                                        # dense-and-sparse side lists
+    dict(outliers=4, bits=4, group_k=128, group_v=128, max_tokens=3000, batch=1),
+    dict(outliers=2, bits=8, group_k=48, group_v=16, residual=20, head_dim=64, max_tokens=777,
+         page_groups=3, num_pages=7),
 ])
 def test_layout_size_matches_the_specification(kw):
     c = _cfg(**kw)
@@ -102,6 +106,9 @@ BAD = [
     (dict(rope_base=float("nan")), N.KVQ_ERR_ARG),
     (dict(rope_base=float("inf")), N.KVQ_ERR_ARG),
     (dict(scheme=2, head_dim=128, rope_base=10000.0), N.KVQ_ERR_UNSUPPORTED),   # pre-RoPE keys: KIVI
+    (dict(outliers=5), N.KVQ_ERR_ARG),                                          # at most 4 per vector
+    (dict(outliers=-1), N.KVQ_ERR_ARG),
+    (dict(scheme=2, head_dim=128, outliers=1), N.KVQ_ERR_UNSUPPORTED),          # dense-and-sparse: KIVI
 ]
 
 

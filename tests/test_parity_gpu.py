@@ -546,3 +546,100 @@ def test_mapped_host_inputs_and_outputs(scheme, bits, G, R):
             dev_out, _ = p.decode(0, q)
             np.testing.assert_allclose(hout.numpy(), dev_out, rtol=1e-5, atol=1e-6)
     assert p.status() == 0
+
+
+# ------------------------------------------------------------------------- dense-and-sparse
+# "KVQuant ...", "Summary": a small fraction of outlier values is moved, per vector, into a
+# separate sparse representation; the dense part is fitted to the rest.
+@pytest.mark.parametrize("bits,D,gqa,G,Gv,R,nout", [(2, 128, 4, 32, 32, 128, 1),
+                                                    (4, 128, 4, 128, 128, 128, 4),
+                                                    (8, 64, 8, 16, 16, 16, 2),
+                                                    (2, 256, 2, 64, 32, 40, 3),
+                                                    (4, 64, 1, 48, 64, 20, 1)])
+def test_sparse_outliers_bulk_steps_and_decode(bits, D, gqa, G, Gv, R, nout):
+    lens = [0, 7, R + G - 1, 700, 1203]
+    p = Pair("kivi", batch=5, q_heads=2 * gqa, kv_heads=2, head_dim=D, max_tokens=1400, bits=bits, group_k=G,
+             group_v=Gv, residual=R, outliers=nout)
+    g = gen(60 + bits + nout)
+    k, v = p.rand_kv(5, max(lens), g)
+    p.append(0, k, v, n_valid=lens)
+    p.assert_same_image()
+    for step in range(G + 2):
+        k, v = p.rand_kv(5, 1, g)
+        p.append(0, k, v)
+        if step % 11 == 0 or step == G + 1:
+            p.assert_same_image()
+            out, ref = p.decode(0, p.rand_q(g))
+            assert_close(out, ref, what="sparse %d-bit, %d outliers, step %d" % (bits, nout, step))
+    assert p.status() == 0
+
+
+def test_sparse_outliers_rescales_across_chunks():
+    # more units than half the grid, so every block runs through many chunks of several
+    # units; values double every 1024 tokens and keys grow late, so the value-scale
+    # exponent and the running maximum both move between a block's chunks and the
+    # outliers' corrections must follow the rescales.  (Much larger values make the output
+    # a small difference of large terms, finer than the tolerance allows the scores to be
+    # rounded.)
+    n, B = 5000, 40
+    p = Pair("kivi", batch=B, q_heads=16, kv_heads=8, head_dim=64, max_tokens=n, bits=2, group_k=32,
+             group_v=32, residual=64, outliers=2)
+    g = gen(71)
+    k, v = p.rand_kv(B, n, g)
+    grow = (2.0 ** (torch.arange(n) // 1024).float())[None, :, None, None]
+    v = (v.float() * grow).to(torch.bfloat16)
+    k = k.float()
+    k[:, 3500:] *= 1.5
+    k = k.to(torch.bfloat16)
+    p.append(0, k, v, n_valid=[n - 37 * i for i in range(B)])
+    del k, v
+    p.assert_same_image()
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="sparse, rescales across chunks")
+    assert p.status() == 0
+
+
+def test_sparse_outliers_paged_with_flushes():
+    kw = dict(batch=3, q_heads=8, kv_heads=2, head_dim=128, max_tokens=600, bits=4, group_k=32, group_v=64,
+              residual=24, outliers=2)
+    ng = (600 - 24) // 32
+    mp = (ng + 2) // 3
+    rng = np.random.default_rng(77)
+    p = Pair("kivi", page_groups=3, num_pages=3 * mp + 4, block_table=_table(rng, 3, mp, 4), **kw)
+    f = Pair("kivi", **kw)
+    g = gen(78)
+    lens = [333, 1, 517]
+    k, v = p.rand_kv(3, max(lens), g)
+    for x in (p, f):
+        x.append(0, k, v, n_valid=lens)
+    for step in range(40):
+        k, v = p.rand_kv(3, 1, g)
+        for x in (p, f):
+            x.append(0, k, v, flags=K.KVQ_NO_AUTOFLUSH if step % 5 == 2 else 0)
+        if step % 9 == 4:
+            for x in (p, f):
+                x.flush(0)
+    p.assert_same_image()
+    f.assert_same_image()
+    q = p.rand_q(g)
+    out, ref = p.decode(0, q)
+    out_f, _ = f.decode(0, q)
+    assert_close(out, ref, what="sparse, paged")
+    assert np.array_equal(out, out_f)
+    assert p.status() == 0
+
+
+@pytest.mark.parametrize("bits,nout", [(2, 1), (4, 3)])
+def test_sparse_outliers_with_keys_before_rope(bits, nout):
+    # KVQuant's pre-RoPE keys and its sparse outliers together: the outlier's bf16 value
+    # replaces the dequantised element before the rotation
+    lens = [5, 700, 1500]
+    p = Pair("kivi", batch=3, q_heads=8, kv_heads=2, head_dim=128, max_tokens=1600, bits=bits, group_k=32,
+             group_v=32, residual=32, rope_base=10000.0, outliers=nout)
+    g = gen(80 + bits)
+    k, v = p.rand_kv(3, max(lens), g)
+    p.append(0, k, v, n_valid=lens)
+    p.assert_same_image()
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="sparse + rope %d-bit" % bits)
+    assert p.status() == 0
