@@ -36,7 +36,8 @@ sys.path.insert(0, ROOT)
 METRIC = ("quantised-cache decode attention tokens/s and achieved HBM GB/s (% of peak), 1 GB300")
 L2_BYTES = 129 * 2 ** 20
 # the timed workloads (the tiny INT8 one is a correctness case, checked by the tests)
-SUITE = ("kivi2_llama3_8b", "kivi4_128k", "fp8_32layer", "serve_mix", "serve_mix_paged", "kivi2_llama3_8b_rope")
+SUITE = ("kivi2_llama3_8b", "kivi4_128k", "fp8_32layer", "serve_mix", "serve_mix_paged", "kivi2_llama3_8b_rope",
+         "kivi4_128k_sparse")
 
 
 def peaks():
@@ -115,6 +116,7 @@ def decode_bytes(w, lengths):
             qn = G * ((n_tokens - R) // G) if n_tokens >= R + G else 0
             r = n_tokens - qn
             rec = G * D * b // 8 * 2 + 4 * D + 4 * G * (D // w.group_v)
+            rec += 4 * w.outliers * (D + G * (D // w.group_v))      # dense-and-sparse side lists
             cache = (qn // G) * rec + r * 4 * D
         elif w.scheme == 1:
             cache = n_tokens * (2 * D + 8)
@@ -126,7 +128,8 @@ def decode_bytes(w, lengths):
 
 DECODE_SOURCES = ("kvq_api.cu", "kvq_decode.cuh", "kvq_decode_rows.cu", "kvq_internal.cuh", "kvq_launch.h")
 SCHEME_SOURCES = {0: tuple("kvq_decode_kivi%d%s.cu" % (b, v) for b in (2, 4, 8)
-                            for v in ("", "_steal", "_paged", "_paged_steal")) + ("kvq_decode_rope.cu",),
+                            for v in ("", "_steal", "_paged", "_paged_steal", "_sparse", "_sparse_paged"))
+                 + ("kvq_decode_rope.cu",),
                   1: (), 2: ("kvq_decode_fp8.cu",), 3: ("kvq_decode_fp8.cu",), 4: ()}
 
 
@@ -205,7 +208,7 @@ def run_gpu(args, w, world, all_layers, nsteps, sampler_on):
         paging = dict(page_groups=w.page_groups, num_pages=pool, block_table=table)
     cfg = K.make_config(w.scheme, layers, w.batch, w.q_heads, w.kv_heads, w.head_dim, max_tokens,
                         bits=w.bits, group_k=w.group_k, group_v=w.group_v, residual=w.residual,
-                        in_dtype=w.in_dtype, rope_base=w.rope_base, **paging)
+                        in_dtype=w.in_dtype, rope_base=w.rope_base, outliers=w.outliers, **paging)
     caches = []
     fp8 = None
     if w.scheme == 2:   # static per-(kv head) scales from the first replica's fill
@@ -474,7 +477,7 @@ def oracle_setup(w, nseq):
     kw = dict(scheme=w.scheme, layers=1, batch=nseq, q_heads=w.q_heads, kv_heads=w.kv_heads,
               head_dim=w.head_dim, bits=w.bits if w.scheme == 0 else 8, group_k=w.group_k, group_v=w.group_v,
               residual=w.residual, max_tokens=n0 + 4096, in_dtype=0 if w.in_dtype == "bf16" else 1,
-              rope_base=w.rope_base)
+              rope_base=w.rope_base, outliers=w.outliers)
     if w.page_groups:
         pool, table = W.block_table(w, kw["max_tokens"])
         kw.update(page_groups=w.page_groups, num_pages=pool, block_table=table[:nseq].numpy())
@@ -537,6 +540,9 @@ def workload_config(w, layers):
             w.page_groups, w.page_groups * w.group_k)
     if w.rope_base:
         cfg["keys"] = "cached before the rotary embedding (base %g), rotated in the decode" % w.rope_base
+    if w.outliers:
+        cfg["outliers"] = ("dense-and-sparse: %d element(s) of largest magnitude per quantisation vector kept "
+                           "in bf16 in a side list" % w.outliers)
     return cfg
 
 

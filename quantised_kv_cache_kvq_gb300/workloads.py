@@ -53,6 +53,7 @@ class Workload:
     steps: int = 1              # decode steps in the workload
     page_groups: int = 0        # KIVI paged layout: group records per page (0: contiguous)
     rope_base: float = 0.0      # KIVI keys cached before the rotary embedding (its base)
+    outliers: int = 0           # KIVI dense-and-sparse: elements per quantisation vector kept in bf16
 
     @property
     def scale(self) -> float:
@@ -93,6 +94,11 @@ WORKLOADS = {
     "kivi2_llama3_8b_rope": Workload(
         "kivi2_llama3_8b_rope", scheme=0, layers=1, batch=8, q_heads=32, kv_heads=8, head_dim=128,
         context=(4096, 4096), bits=2, group_k=32, group_v=32, residual=128, seed=1, rope_base=500000.0),
+    # the 4-bit 128k-token context with one outlier per quantisation vector kept in bf16
+    # (1 of 128 elements, 0.8%: the dense-and-sparse split at about 1%)
+    "kivi4_128k_sparse": Workload(
+        "kivi4_128k_sparse", scheme=0, layers=1, batch=1, q_heads=32, kv_heads=8, head_dim=128,
+        context=(131072, 131072), bits=4, group_k=128, group_v=128, residual=128, seed=3, outliers=1),
 }
 
 

@@ -32,6 +32,23 @@ def test_decode_bytes_4bit_and_fp8_per_token_figures():
     assert bench.decode_bytes(w3, [8192, 100]) == 8 * ((8192 + 100) * 256 + 2 * 4 * 128 * 2)
 
 
+def test_decode_bytes_sparse_side_lists():
+    # one outlier per vector at G = Gv = 128: a 4-byte key entry per channel and a 4-byte
+    # value entry per token, 8 bytes a token on top of the dense 136
+    w = W.WORKLOADS["kivi4_128k_sparse"]
+    n = 131072
+    qn = 128 * ((n - 128) // 128)
+    assert bench.decode_bytes(w, [n]) == 8 * (qn * 144 + (n - qn) * 512 + 4 * 128 * 2)
+    # the oracle's record agrees: K side 4 K D, V side 4 K (D / Gv) G
+    import ctypes as C
+    import oracle as O
+    kw = dict(scheme=0, layers=1, batch=1, q_heads=32, kv_heads=8, head_dim=128, bits=4, group_k=128,
+              group_v=128, residual=128, max_tokens=128 + 128 * 3)
+    dense = O.lib().kvqo_image_bytes(C.byref(O.make_config(**kw)))
+    sparse = O.lib().kvqo_image_bytes(C.byref(O.make_config(outliers=1, **kw)))
+    assert sparse - dense == 8 * 3 * (4 * 128 + 4 * 128)
+
+
 def test_decode_bytes_ragged_is_a_sum_and_short_sequences_are_window_only():
     w = W.WORKLOADS["serve_mix"]
     lens = [1024, 5000, 32768, 159, 160, 0]

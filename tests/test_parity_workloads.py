@@ -6,7 +6,8 @@ compared with the oracle:
 
 * KIVI 2-bit Llama-3-8B layer (8 sequences x 4096 tokens): the whole cache image byte for
   byte after the prefill and after one decode step, and every output element.
-* KIVI 4-bit, one 131072-token sequence: the whole image and every output element.
+* KIVI 4-bit, one 131072-token sequence: the whole image and every output element, also
+  with one outlier per quantisation vector kept aside in bf16 (dense-and-sparse).
 * FP8, 32 layers x 64 sequences x 8192 tokens: the cache is filled for every layer; the
   byte ranges, token counts, scales and outputs of layers {0, 31} x 4 sampled sequences
   are compared.
@@ -51,7 +52,7 @@ def _kw(w, batch, layers, max_tokens):
     return dict(scheme=w.scheme, layers=layers, batch=batch, q_heads=w.q_heads, kv_heads=w.kv_heads,
                 head_dim=w.head_dim, bits=w.bits if w.scheme == 0 else 8, group_k=w.group_k,
                 group_v=w.group_v, residual=w.residual, max_tokens=max_tokens,
-                in_dtype=0 if w.in_dtype == "bf16" else 1)
+                in_dtype=0 if w.in_dtype == "bf16" else 1, outliers=w.outliers)
 
 
 def _regions(kw):
@@ -110,7 +111,7 @@ def _assert_bytes(got, ref, what):
 
 
 # --------------------------------------------------------------------------- whole images
-@pytest.mark.parametrize("name", ["kivi2_llama3_8b", "kivi4_128k"])
+@pytest.mark.parametrize("name", ["kivi2_llama3_8b", "kivi4_128k", "kivi4_128k_sparse"])
 def test_workload_whole_image_and_outputs(name):
     from quantised_kv_cache_kvq_gb300 import workloads as W
     w = W.WORKLOADS[name]
