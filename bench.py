@@ -126,9 +126,11 @@ def decode_bytes(w, lengths):
     return total
 
 
-DECODE_SOURCES = ("kvq_api.cu", "kvq_decode.cuh", "kvq_decode_rows.cu", "kvq_internal.cuh", "kvq_launch.h")
+DECODE_SOURCES = ("kvq_api.cu", "kvq_decode.cuh", "kvq_decode_rows.cu", "kvq_internal.cuh", "kvq_launch.h",
+                  "kvq_rope.cuh")
 SCHEME_SOURCES = {0: tuple("kvq_decode_kivi%d%s.cu" % (b, v) for b in (2, 4, 8)
-                            for v in ("", "_steal", "_paged", "_paged_steal", "_sparse", "_sparse_paged"))
+                            for v in ("", "_steal", "_paged", "_paged_steal", "_sparse", "_sparse_paged", "_rope",
+                                      "_rope_paged"))
                  + ("kvq_decode_rope.cu",),
                   1: (), 2: ("kvq_decode_fp8.cu",), 3: ("kvq_decode_fp8.cu",), 4: ()}
 

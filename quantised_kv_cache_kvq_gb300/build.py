@@ -41,6 +41,12 @@ UNITS = {
     "kvq_decode_kivi2_sparse_paged.cu": [],
     "kvq_decode_kivi4_sparse_paged.cu": [],
     "kvq_decode_kivi8_sparse_paged.cu": [],
+    "kvq_decode_kivi2_rope.cu": [],
+    "kvq_decode_kivi4_rope.cu": [],
+    "kvq_decode_kivi8_rope.cu": [],
+    "kvq_decode_kivi2_rope_paged.cu": [],
+    "kvq_decode_kivi4_rope_paged.cu": [],
+    "kvq_decode_kivi8_rope_paged.cu": [],
     "kvq_decode_rows.cu": [],
     "kvq_decode_fp8.cu": [],
     "kvq_decode_rope.cu": [],

@@ -675,6 +675,12 @@ __device__ __forceinline__ void lds_words(uint32_t a, uint32_t (&w)[N]) {
     }
 }
 
+}  // namespace kvq
+
+#include "kvq_rope.cuh"
+
+namespace kvq {
+
 // ------------------------------------------------------------------------ row path (INT8, INT4)
 // Per-token rows, CHR tokens per chunk: a warp per token for the scores, a thread per
 // channel for the values, and a running softmax (per-head max M and sum L in shared memory,
@@ -1098,6 +1104,43 @@ __device__ __forceinline__ uint32_t split_mul(__half2 s, uint32_t x, uint32_t y)
     return h2_as_u32(__hfma2(s, u32_as_h2(y), e));
 }
 
+// Keys cached before RoPE: the BITS-bit codes of channels c0, c0 + 1, c0 + 8, c0 + 9 (c0 =
+// 16 p + 2 t, t < 4) of one token-major key row: one 32-bit word (2-bit), two (4-bit) or
+// two 16-bit loads (8-bit).
+template <int BITS>
+__device__ __forceinline__ void row_codes4(const uint8_t* row, int c0, int (&q)[4]) {
+    constexpr int M = (1 << BITS) - 1;
+    if constexpr (BITS == 2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(row + 4 * (c0 >> 4));
+        const int sh = 2 * (c0 & 15);
+        q[0] = (w >> sh) & M;
+        q[1] = (w >> (sh + 2)) & M;
+        q[2] = (w >> (sh + 16)) & M;
+        q[3] = (w >> (sh + 18)) & M;
+    } else if constexpr (BITS == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(row + 8 * (c0 >> 4));
+        const int sh = 4 * (c0 & 7);
+        q[0] = (w.x >> sh) & M;
+        q[1] = (w.x >> (sh + 4)) & M;
+        q[2] = (w.y >> sh) & M;
+        q[3] = (w.y >> (sh + 4)) & M;
+    } else {
+        const uint32_t lo = *reinterpret_cast<const uint16_t*>(row + c0);
+        const uint32_t hi = *reinterpret_cast<const uint16_t*>(row + c0 + 8);
+        q[0] = lo & M;
+        q[1] = lo >> 8;
+        q[2] = hi & M;
+        q[3] = hi >> 8;
+    }
+}
+// Two binary32 values as fp16 pairs: the rounded values, and the rounded remainders.
+__device__ __forceinline__ void split_pair(float x, float y, uint32_t& major, uint32_t& minor) {
+    const __half2 m = __floats2half2_rn(x, y);
+    const float2 f = __half22float2(m);
+    major = h2_as_u32(m);
+    minor = h2_as_u32(__floats2half2_rn(x - f.x, y - f.y));
+}
+
 // One packed work item: a run of chunks of CH = 4 * W tokens of one (sequence, kv head).
 // Chunks are staged by bulk copies into NSTAGE shared-memory buffers (double-buffered
 // when they fit), each warp takes W tokens of a chunk, and every warp keeps an online
@@ -1110,7 +1153,16 @@ __device__ __forceinline__ uint32_t split_mul(__half2 s, uint32_t x, uint32_t y)
 // largest value scale seen so far times 2^Ev is below 2^15 (lowered, and what was
 // accumulated rescaled by the exact power of two, when a larger scale arrives); the code
 // position p is fixed per accumulator element, so 2^(24 - p) is applied at the end.
-template <int D, int BITS, int NT, bool STEAL, bool PAGED, bool SPARSE>
+//
+// ROPE (keys cached before the rotary embedding): the key pass dequantises each tile's keys
+// in binary32 (code * s + z), turns every channel pair (c, c + D/2) by its token's angle,
+// and scores the turned keys on the tensor cores: A = the keys times 2^(14 - e) (e from the
+// group's largest possible |key|, so that no fp16 part overflows) as fp16 major + minor
+// parts, B = the query in natural channel order (major and minor in the columns of each
+// head).  Lane (g, t) holds, for k-steps p and p + D/32, the channels 16 p + 2 t + {0, 1, 8,
+// 9} and their partners, so each rotation pair stays in one lane.  The values and the
+// softmax are those of the other keys.
+template <int D, int BITS, int NT, bool STEAL, bool PAGED, bool SPARSE, bool ROPE = false>
 __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, int b, int h, int64_t slot,
                                         int64_t t0, int64_t t1, uint32_t phase, const StealCtx& sc) {
     const SmemOffsets so = decode_smem(a.lo, a.plan);
@@ -1258,9 +1310,36 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
     int qexp = 0;
     if (qmax > 0.0f) frexpf(qmax, &qexp);
     const float qdown = ldexpf(1.0f, -qexp), qup = ldexpf(1.0f, qexp);
+    if constexpr (ROPE) {
+        // row 32 nt + lane (lane = 4 g + t): for k-step ks, words 2 ks and 2 ks + 1 hold the
+        // query part (g & 1: 0 major, 1 minor) of head 4 nt + g / 2 at channels 16 ks + 2 t
+        // + {0, 1} and {8, 9}; and the rotation frequencies w_i
+        float* rw = reinterpret_cast<float*>(smem + so.rw);
+        for (int i = tid; i < D / 2; i += blockDim.x) rw[i] = a.rope_w[i];
+        for (int i = tid; i < 32 * NT * KSTEPS; i += blockDim.x) {
+            const int ks = i % KSTEPS, row = i / KSTEPS;
+            const int ln = row & 31, gg = ln >> 2, tt = ln & 3;
+            const int hh = 4 * (row >> 5) + (gg >> 1);
+            uint32_t w2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = 16 * ks + 2 * tt + 8 * e;
+                float v0 = 0.0f, v1 = 0.0f;
+                if (hh < gqa) {
+                    v0 = qs[hh * D + c] * qdown;
+                    v1 = qs[hh * D + c + 1] * qdown;
+                }
+                uint32_t mj, mn;
+                split_pair(v0, v1, mj, mn);
+                w2[e] = (gg & 1) ? mn : mj;
+            }
+            qx[row * QROW + 2 * ks] = w2[0];
+            qx[row * QROW + 2 * ks + 1] = w2[1];
+        }
+    }
     // one entry per (head hh, lane quarter tg, key pair m), written to the rows of the two
     // lanes (parts) of B columns 2 (hh mod 4) and 2 (hh mod 4) + 1
-    for (int i = tid; i < 16 * NT * NPAIR; i += blockDim.x) {
+    for (int i = tid; i < (ROPE ? 0 : 16 * NT * NPAIR); i += blockDim.x) {
         const int m = i % NPAIR, r = i / NPAIR;
         const int hh = r >> 2, tg = r & 3;
         const int wi = m / HPW, jj = m % HPW;
@@ -1354,7 +1433,7 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
             // offset term of every group of the warp: cst[group][head] = sum_c q_c zero_c,
             // as one small tensor-core product (rows = groups, k = channels in pair order)
             float cstf[NT][4];
-            {
+            if constexpr (!ROPE) {
                 uint32_t zreg[D / 8];
                 if (g < ngrp) {
                     lds_words<D / 8>(st0 + g * rec + kzero_lane, zreg);
@@ -1387,7 +1466,105 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
             float cmax[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) cmax[nt] = -INFINITY;
-            {
+            if constexpr (ROPE) {
+                const float* rw = reinterpret_cast<const float*>(smem + so.rw);
+                const uint32_t qt_lane = qx_lane;      // the natural-order query table
+                const float lv = static_cast<float>((1 << BITS) - 1);
+                // position of the warp's first token (the item starts at token t0)
+                const int64_t wpos = t0 + (int64_t)c * CH + warp * W;
+                int i = 0, ti = ti0;
+                const uint8_t* rp = smem + so.data + sj * stage_bytes + (int64_t)g0 * rec;
+#pragma unroll 1
+                while (i < ntl) {
+                    const uint8_t* kp = rp + kpar;     // fp16 scale[D], then zero[D]
+                    // the group's largest possible |key| (before and after rotation, up to
+                    // sqrt 2): scale 2^(14 - e) keeps every fp16 part finite
+                    float ksc, kf;
+                    {
+                        float m = 0.0f;
+                        for (int cc = lane; cc < D; cc += 32) {
+                            const float sv = half_at(kp, 2 * cc), zv = half_at(kp, 2 * D + 2 * cc);
+                            m = fmaxf(m, fmaxf(fabsf(zv), fabsf(fmaf(sv, lv, zv))));
+                        }
+                        m = warp_max(m);
+                        int e = 0;
+                        if (m > 0.0f) frexpf(m * 1.41421366f, &e);
+                        e = e < -100 ? -100 : (e > 120 ? 120 : e);
+                        ksc = exp2i(14 - e);
+                        kf = exp2i(e - 14) * qup;
+                    }
+                    const int nseg = min(ntl - i, (G - ti) >> 4);
+#pragma unroll 1
+                    for (int k = 0; k < nseg; ++k, ++i, ti += 16) {
+                        const uint8_t* rowg = rp + (int64_t)(ti + g) * ROWB;
+                        const uint8_t* rowg8 = rowg + 8 * ROWB;
+                        const float posg = static_cast<float>(wpos + 16 * i + g);
+                        const float posg8 = static_cast<float>(wpos + 16 * i + g + 8);
+                        float acc[NT][4];
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+#pragma unroll
+                        for (int pp = 0; pp < KSTEPS / 2; ++pp) {
+                            const int c0 = 16 * pp + 2 * tig, c2 = c0 + D / 2;
+                            int xg[4], xg8[4], yg[4], yg8[4];
+                            row_codes4<BITS>(rowg, c0, xg);
+                            row_codes4<BITS>(rowg8, c0, xg8);
+                            row_codes4<BITS>(rowg, c2, yg);
+                            row_codes4<BITS>(rowg8, c2, yg8);
+                            float xr[2][4], yr[2][4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int cl = c0 + (e & 1) + 8 * (e >> 1), ch = cl + D / 2;
+                                const float s1 = half_at(kp, 2 * cl), z1 = half_at(kp, 2 * D + 2 * cl);
+                                const float s2 = half_at(kp, 2 * ch), z2 = half_at(kp, 2 * D + 2 * ch);
+                                const float w = rw[cl];
+                                float sn, cs;
+                                {
+                                    const float x = dequant(xg[e], s1, z1), y = dequant(yg[e], s2, z2);
+                                    rope_sincos(__fmul_rn(posg, w), &sn, &cs);
+                                    xr[0][e] = (x * cs - y * sn) * ksc;
+                                    yr[0][e] = (y * cs + x * sn) * ksc;
+                                }
+                                {
+                                    const float x = dequant(xg8[e], s1, z1), y = dequant(yg8[e], s2, z2);
+                                    rope_sincos(__fmul_rn(posg8, w), &sn, &cs);
+                                    xr[1][e] = (x * cs - y * sn) * ksc;
+                                    yr[1][e] = (y * cs + x * sn) * ksc;
+                                }
+                            }
+                            // A fragments of k-steps pp (x) and pp + D/32 (y): rows g, g + 8,
+                            // columns 2t, 2t + 1 (registers 0, 1) and 2t + 8, 2t + 9 (2, 3)
+                            uint32_t xm[4], xn[4], ym[4], yn[4];
+                            split_pair(xr[0][0], xr[0][1], xm[0], xn[0]);
+                            split_pair(xr[1][0], xr[1][1], xm[1], xn[1]);
+                            split_pair(xr[0][2], xr[0][3], xm[2], xn[2]);
+                            split_pair(xr[1][2], xr[1][3], xm[3], xn[3]);
+                            split_pair(yr[0][0], yr[0][1], ym[0], yn[0]);
+                            split_pair(yr[1][0], yr[1][1], ym[1], yn[1]);
+                            split_pair(yr[0][2], yr[0][3], ym[2], yn[2]);
+                            split_pair(yr[1][2], yr[1][3], ym[3], yn[3]);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const uint2 qa = lds64(qt_lane + nt * 32 * QROW * 4 + 8 * pp);
+                                const uint2 qb = lds64(qt_lane + nt * 32 * QROW * 4 + 8 * (pp + KSTEPS / 2));
+                                mma_16816(acc[nt], xm, qa.x, qa.y);
+                                mma_16816(acc[nt], xn, qa.x, qa.y);
+                                mma_16816(acc[nt], ym, qb.x, qb.y);
+                                mma_16816(acc[nt], yn, qb.x, qb.y);
+                            }
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const float s0 = (acc[nt][0] + acc[nt][1]) * kf;
+                            const float s1 = (acc[nt][2] + acc[nt][3]) * kf;
+                            wsc[(i * NT + nt) * 32] = make_float2(s0, s1);
+                            cmax[nt] = fmaxf(cmax[nt], fmaxf(s0, s1));
+                        }
+                    }
+                    rp += rec;
+                    ti = 0;
+                }
+            } else {
                 int i = 0, grp = 0, ti = ti0;
                 uint32_t ro = st0;
 #pragma unroll 1
@@ -1773,7 +1950,9 @@ __device__ __forceinline__ int packed_item(const DecodeArgs& a, uint8_t* smem, i
 // BITS == 0: no packed part (INT8 rows).  STEAL: units may share their packed chunks on
 // demand (a separate instantiation: the extra code slows the kernels that never use it).
 // PAGED: the group records are found through the block table (paged layout).
-template <int D, int BITS, int NT, bool STEAL, bool PAGED, bool SPARSE = false>
+// ROPE: keys cached before the rotary embedding (packed tokens on the tensor cores,
+// window rows through rope_item).
+template <int D, int BITS, int NT, bool STEAL, bool PAGED, bool SPARSE = false, bool ROPE = false>
 __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
     k_decode(const __grid_constant__ DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1793,7 +1972,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (NT == 1 && D <= 128) ? 4 : 2)
             int r;
             if constexpr (BITS != 0) {
                 if (part == 0)
-                    r = packed_item<D, BITS, NT, STEAL, PAGED, SPARSE>(a, smem, b, h, slot, t0, t1, phase, sc);
+                    r = packed_item<D, BITS, NT, STEAL, PAGED, SPARSE, ROPE>(a, smem, b, h, slot, t0, t1, phase, sc);
+                else if constexpr (ROPE)
+                    r = rope_item<D, BITS>(a, smem, b, h, slot, 1, t0, t1, phase);
                 else
                     r = window_item<D, NT>(a, smem, b, h, slot, t0, t1, phase);
             } else {
@@ -1851,30 +2032,30 @@ int launch_wave(K fn, DecodeArgs& a, cudaStream_t stream) {
 // KIVI variants beyond the base kernel, each family in translation units of its own (so
 // the builds run in parallel): on demand (STEAL), paged layout (PAGED) and both.  The
 // paged fixed-split kernel plans its own wave (it is the paged fallback).
-// SPARSE: dense-and-sparse records (side lists of outliers); these kernels use the fixed
-// split and plan their own wave.
-template <int D, int BITS, int NT, bool STEAL, bool PAGED, bool SPARSE>
+// SPARSE: dense-and-sparse records (side lists of outliers); ROPE: keys cached before the
+// rotary embedding.  These kernels use the fixed split and plan their own wave.
+template <int D, int BITS, int NT, bool STEAL, bool PAGED, bool SPARSE, bool ROPE>
 int launch_kivi_variant(DecodeArgs& a, cudaStream_t stream) {
-    if constexpr ((PAGED || SPARSE) && !STEAL) {   // the fixed split, on the kernel's own wave
-        const int rc = plan_wave(k_decode<D, BITS, NT, false, PAGED, SPARSE>, a);
+    if constexpr ((PAGED || SPARSE || ROPE) && !STEAL) {   // the fixed split, on the kernel's own wave
+        const int rc = plan_wave(k_decode<D, BITS, NT, false, PAGED, SPARSE, ROPE>, a);
         if (rc != KVQ_OK) return rc;
         a.plan.steal = 0;
     }
-    return launch_on_wave(k_decode<D, BITS, NT, STEAL, PAGED, SPARSE>, a, stream);
+    return launch_on_wave(k_decode<D, BITS, NT, STEAL, PAGED, SPARSE, ROPE>, a, stream);
 }
-template <int BITS, bool STEAL, bool PAGED, bool SPARSE = false>
+template <int BITS, bool STEAL, bool PAGED, bool SPARSE = false, bool ROPE = false>
 int launch_kivi_family(DecodeArgs& a, cudaStream_t stream) {
     const bool wide = a.lo.gqa > 4;
     switch (a.lo.D) {
         case 64:
-            return wide ? launch_kivi_variant<64, BITS, 2, STEAL, PAGED, SPARSE>(a, stream)
-                        : launch_kivi_variant<64, BITS, 1, STEAL, PAGED, SPARSE>(a, stream);
+            return wide ? launch_kivi_variant<64, BITS, 2, STEAL, PAGED, SPARSE, ROPE>(a, stream)
+                        : launch_kivi_variant<64, BITS, 1, STEAL, PAGED, SPARSE, ROPE>(a, stream);
         case 128:
-            return wide ? launch_kivi_variant<128, BITS, 2, STEAL, PAGED, SPARSE>(a, stream)
-                        : launch_kivi_variant<128, BITS, 1, STEAL, PAGED, SPARSE>(a, stream);
+            return wide ? launch_kivi_variant<128, BITS, 2, STEAL, PAGED, SPARSE, ROPE>(a, stream)
+                        : launch_kivi_variant<128, BITS, 1, STEAL, PAGED, SPARSE, ROPE>(a, stream);
         case 256:
-            return wide ? launch_kivi_variant<256, BITS, 2, STEAL, PAGED, SPARSE>(a, stream)
-                        : launch_kivi_variant<256, BITS, 1, STEAL, PAGED, SPARSE>(a, stream);
+            return wide ? launch_kivi_variant<256, BITS, 2, STEAL, PAGED, SPARSE, ROPE>(a, stream)
+                        : launch_kivi_variant<256, BITS, 1, STEAL, PAGED, SPARSE, ROPE>(a, stream);
         default: return KVQ_ERR_UNSUPPORTED;
     }
 }
@@ -1890,6 +2071,12 @@ int launch_decode_kivi8_paged_steal(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi2_sparse(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi4_sparse(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi8_sparse(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi2_rope(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi4_rope(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi8_rope(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi2_rope_paged(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi4_rope_paged(DecodeArgs& a, cudaStream_t stream);
+int launch_decode_kivi8_rope_paged(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi2_sparse_paged(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi4_sparse_paged(DecodeArgs& a, cudaStream_t stream);
 int launch_decode_kivi8_sparse_paged(DecodeArgs& a, cudaStream_t stream);

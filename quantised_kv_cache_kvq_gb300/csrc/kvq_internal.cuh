@@ -103,7 +103,7 @@ struct DecodePlan {
 
 // Shared-memory carve of the decode block, identical on host and device.
 struct SmemOffsets {
-    int64_t bar, red, hstat, sst, qs, qpa, qpb, pw, sc, oc, data, total;
+    int64_t bar, red, hstat, sst, qs, qpa, qpb, pw, sc, oc, rw, data, total;
 };
 __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const DecodePlan& p) {
     SmemOffsets o;
@@ -128,6 +128,8 @@ __host__ __device__ inline SmemOffsets decode_smem(const Layout& lo, const Decod
     }
     o.oc = off;                                          // dense-and-sparse: per-warp value
     if (lo.K > 0) off += (int64_t)4 * lo.gqa * lo.D * 4;    // corrections [warp][head][D]
+    o.rw = off;                                          // keys before RoPE: w_i, i < D/2
+    if (lo.rope_base > 0.0f) off += (int64_t)2 * lo.D;
     off = (off + 127) / 128 * 128;
     o.data = off;
     int64_t rows = 0, packed = 0;
