@@ -555,7 +555,9 @@ def gpu_record(w, r, world, peak, peak_kind):
     dec_avg_ms = r["decode_ms"] / launches
     achieved = (r["dec_bytes"] / launches) / (dec_avg_ms / 1e3) / 1e9
     step_gbs = r["step_bytes"] / (r["step_ms"] / 1e3) / 1e9
-    traffic = profiled_traffic(w.name, w.scheme) if r["layers"] == 1 else None
+    from quantised_kv_cache_kvq_gb300 import workloads as W
+    # the profile summaries hold the traffic of the workload as defined (one layer, its batch)
+    traffic = profiled_traffic(w.name, w.scheme) if r["layers"] == 1 and w == W.WORKLOADS[w.name] else None
     cfg = workload_config(w, r["layers"])
     cfg.update({"steps_per_replay": r["nsteps"], "replicas": r["reps"],
                 "cache_mb_per_replica": round(r["cache_mb"], 2), "mean_context": round(r["mean_context"], 1),
@@ -607,6 +609,8 @@ def main():
     ap.add_argument("--decode-seconds", type=float, default=1.0,
                     help="minimum duration of the decode-only replays (median)")
     ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle work per workload")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's number of sequences (smaller cases for ncu captures)")
     ap.add_argument("--all-layers", action="store_true",
                     help="time every layer of the headline workload in each step (default: one layer)")
     args = ap.parse_args()
@@ -614,6 +618,9 @@ def main():
         ap.error("at least 3 warm-up steps")
     from quantised_kv_cache_kvq_gb300 import workloads as W
     w = W.WORKLOADS[args.workload]
+    if args.batch > 0:
+        import dataclasses
+        w = dataclasses.replace(w, batch=args.batch)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     peak, peak_kind = peaks()
