@@ -556,8 +556,9 @@ def gpu_record(w, r, world, peak, peak_kind):
     achieved = (r["dec_bytes"] / launches) / (dec_avg_ms / 1e3) / 1e9
     step_gbs = r["step_bytes"] / (r["step_ms"] / 1e3) / 1e9
     from quantised_kv_cache_kvq_gb300 import workloads as W
-    # the profile summaries hold the traffic of the workload as defined (one layer, its batch)
-    traffic = profiled_traffic(w.name, w.scheme) if r["layers"] == 1 and w == W.WORKLOADS[w.name] else None
+    # the profile summaries hold the traffic of one decode call (one layer) of the workload as
+    # defined (its batch); every launch of the line, one per layer, is such a call
+    traffic = profiled_traffic(w.name, w.scheme) if w == W.WORKLOADS[w.name] else None
     cfg = workload_config(w, r["layers"])
     cfg.update({"steps_per_replay": r["nsteps"], "replicas": r["reps"],
                 "cache_mb_per_replica": round(r["cache_mb"], 2), "mean_context": round(r["mean_context"], 1),
