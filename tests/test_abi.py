@@ -175,3 +175,19 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     cfg = K.make_config(0, 1, 1, 4, 4, 64, 64, bits=2, group_k=16, group_v=16, residual=0)
     with pytest.raises(RuntimeError, match="not built"):
         N.kvq_cache_bytes(cfg, 64)
+
+
+def test_config_struct_layout_matches_the_header(tmp_path):
+    # the binding's ctypes struct must lay kvq_config out as a C compiler does from
+    # include/kvq.h (size and every field offset)
+    fields = [n for n, _ in N.KvqConfig._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "kvq.h"\nint main(void) {\n'
+                   '    printf("%zu\\n", sizeof(kvq_config));\n'
+                   + "".join('    printf("%%zu\\n", offsetof(kvq_config, %s));\n' % f for f in fields)
+                   + '    return 0;\n}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == C.sizeof(N.KvqConfig)
+    assert out[1:] == [getattr(N.KvqConfig, f).offset for f in fields]
