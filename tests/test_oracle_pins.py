@@ -1105,3 +1105,49 @@ def test_sparse_config_rules():
         O.make_config(scheme=1, outliers=1)
     with pytest.raises(ValueError):
         O.make_config(scheme=0, group_k=16, group_v=16, outliers=16)
+
+
+def test_sparse_keys_before_rope_brute_force():
+    # both of KVQuant's key techniques at once ("Key points": keys quantised before RoPE; a
+    # small fraction of outliers moved, per vector, into a sparse representation): the
+    # oracle's decode equals attention over keys rebuilt here (per key channel and group the
+    # k largest magnitudes exact, the rest by the pinned Q_b rule on the rest) and then
+    # turned by their positions (base 1: `t` radians, as complex multiplication)
+    G, Gv, R, D, n, bits, k = 16, 32, 20, 64, 90, 4, 2
+    cfg = _kivi_cfg(batch=1, q_heads=2, kv_heads=1, head_dim=D, bits=bits, group_k=G, group_v=Gv,
+                    residual=R, max_tokens=112, outliers=k, rope_base=1.0)
+    img = O.Image(cfg)
+    g = torch.Generator().manual_seed(34)
+    kx = torch.randn(1, n, 1, D, generator=g)
+    kx[..., 5] *= 9.0
+    kx = kx.to(torch.bfloat16)
+    vx = torch.randn(1, n, 1, D, generator=g).to(torch.bfloat16)
+    img.append(0, 0, _bf16_bits(kx), _bf16_bits(vx))
+    qn = G * ((n - R) // G)
+    kf, vf = kx.float().numpy()[0, :, 0], vx.float().numpy()[0, :, 0]
+    q = torch.randn(1, 2, D, generator=g).to(torch.bfloat16).float().numpy()
+    scale = 0.25
+    out = img.decode(0, q, scale)
+
+    def rebuild(vec):
+        order = sorted(range(vec.size), key=lambda i: (-abs(float(vec[i])), i))[:k]
+        rest = [i for i in range(vec.size) if i not in order]
+        s, z, codes = O.qb_group(vec[rest], bits)
+        r = np.array(vec, np.float64)
+        r[rest] = [O.qb_dequant(int(c), s, z) for c in codes]
+        return r
+
+    K = np.array(kf, np.float64)
+    V = np.array(vf, np.float64)
+    for g0 in range(0, qn, G):
+        for ch in range(D):
+            K[g0:g0 + G, ch] = rebuild(kf[g0:g0 + G, ch])
+    for t in range(qn):
+        for j in range(D // Gv):
+            V[t, j * Gv:(j + 1) * Gv] = rebuild(vf[t, j * Gv:(j + 1) * Gv])
+    Kr = np.stack([_complex_rotate(K[t], np.full(D // 2, float(t))) for t in range(n)])
+    for hq in range(2):
+        s = scale * (q[0, hq].astype(np.float64) @ Kr.T)
+        p = np.exp(s - s.max())
+        ref = (p / p.sum()) @ V
+        np.testing.assert_allclose(out[0, hq], ref, rtol=1e-11, atol=1e-13)
