@@ -643,3 +643,24 @@ def test_sparse_outliers_with_keys_before_rope(bits, nout):
     out, ref = p.decode(0, p.rand_q(g))
     assert_close(out, ref, what="sparse + rope %d-bit" % bits)
     assert p.status() == 0
+
+
+def test_sparse_outliers_keys_before_rope_in_pages():
+    # all three together: dense-and-sparse records of keys cached before the rotary
+    # embedding, in a shuffled page pool
+    kw = dict(batch=2, q_heads=8, kv_heads=2, head_dim=64, max_tokens=900, bits=2, group_k=32, group_v=32,
+              residual=40, rope_base=10000.0, outliers=2)
+    ng = (900 - 40) // 32
+    mp = (ng + 3) // 4
+    p = Pair("kivi", page_groups=4, num_pages=2 * mp + 2, block_table=_table(np.random.default_rng(88), 2, mp, 2),
+             **kw)
+    g = gen(89)
+    k, v = p.rand_kv(2, 850, g)
+    p.append(0, k, v, n_valid=[850, 333])
+    for step in range(3):
+        k, v = p.rand_kv(2, 1, g)
+        p.append(0, k, v)
+    p.assert_same_image()
+    out, ref = p.decode(0, p.rand_q(g))
+    assert_close(out, ref, what="sparse + rope, paged")
+    assert p.status() == 0
