@@ -425,7 +425,8 @@ def test_paged_page_outside_the_pool_is_reported():
 # ------------------------------------------------------------------------- keys before RoPE
 @pytest.mark.parametrize("bits,D,gqa,G,Gv,R,base", [(2, 128, 4, 32, 32, 128, 500000.0),
                                                      (4, 64, 8, 128, 64, 32, 10000.0),
-                                                     (8, 256, 1, 16, 16, 16, 10000.0)])
+                                                     (8, 256, 1, 16, 16, 16, 10000.0),
+                                                     (2, 256, 8, 32, 64, 64, 10000.0)])
 def test_rope_keys_cached_before_the_embedding(bits, D, gqa, G, Gv, R, base):
     # the cache holds keys before the rotary embedding; the decode turns every dequantised
     # key (packed groups and bf16 window) by its position
@@ -555,7 +556,8 @@ def test_mapped_host_inputs_and_outputs(scheme, bits, G, R):
                                                     (4, 128, 4, 128, 128, 128, 4),
                                                     (8, 64, 8, 16, 16, 16, 2),
                                                     (2, 256, 2, 64, 32, 40, 3),
-                                                    (4, 64, 1, 48, 64, 20, 1)])
+                                                    (4, 64, 1, 48, 64, 20, 1),
+                                                    (4, 256, 8, 64, 64, 32, 2)])
 def test_sparse_outliers_bulk_steps_and_decode(bits, D, gqa, G, Gv, R, nout):
     lens = [0, 7, R + G - 1, 700, 1203]
     p = Pair("kivi", batch=5, q_heads=2 * gqa, kv_heads=2, head_dim=D, max_tokens=1400, bits=bits, group_k=G,
