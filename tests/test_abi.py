@@ -191,3 +191,32 @@ def test_config_struct_layout_matches_the_header(tmp_path):
     out = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     assert out[0] == C.sizeof(N.KvqConfig)
     assert out[1:] == [getattr(N.KvqConfig, f).offset for f in fields]
+
+
+def test_layout_size_matches_the_specification_on_random_configurations():
+    # a seeded sweep over valid KIVI, INT8, INT4 and FP8 configurations (paged, pre-RoPE and
+    # dense-and-sparse ones included): the library's allocation size is the oracle's
+    import random
+    rng = random.Random(2024)
+    lib = O.lib()
+    for _ in range(300):
+        scheme = rng.choice([0, 0, 0, 1, 2, 3, 4])
+        kv = rng.choice([1, 2, 8])
+        kw = dict(scheme=scheme, layers=rng.randint(1, 3), batch=rng.randint(1, 9), kv_heads=kv,
+                  q_heads=kv * rng.choice([1, 2, 4, 8]), max_tokens=rng.randint(1, 3000))
+        if scheme == 0:
+            D = rng.choice([64, 128, 256])
+            G = 16 * rng.randint(1, 8)
+            Gv = rng.choice([g for g in (16, 32, 64, 128, 256) if D % g == 0])
+            kw.update(head_dim=D, bits=rng.choice([2, 4, 8]), group_k=G, group_v=Gv, residual=rng.randint(0, 200),
+                      in_dtype=0, outliers=rng.choice([0, 0, 1, 2, 4]),
+                      rope_base=rng.choice([0.0, 10000.0]))
+            if rng.random() < 0.3:
+                kw.update(page_groups=rng.randint(1, 6), num_pages=rng.randint(1, 50))
+        else:
+            kw.update(head_dim=rng.choice([32, 64, 128, 256]), bits=8, in_dtype=rng.choice([0, 1]))
+        c = _cfg(**{k: v for k, v in kw.items() if k not in ("rope_base", "outliers")})
+        c.rope_base = kw.get("rope_base", 0.0)
+        c.outliers = kw.get("outliers", 0)
+        got = K.kvq_cache_bytes(c, c.max_tokens, K.KVQ_BYTES_LAYOUT)
+        assert got == lib.kvqo_image_bytes(C.byref(O.make_config(**kw))), kw
